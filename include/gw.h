@@ -1,0 +1,217 @@
+/*
+ * gw.h - C ABI of the paged hybrid decode-attention library (GB300, sm_103a).
+ *
+ * The library computes one decode step of attention for a Gemma-4-style
+ * hybrid stack, over paged KV pools, on the GPU:
+ *
+ *   - gw_kv_append           RoPE on the rotated slice of K, then page write
+ *                            (optionally rounding to e4m3) of the step's rows.
+ *   - gw_decode_attn_local   sliding-window attention, head dim 256, GQA.
+ *   - gw_decode_attn_global  global attention, head dim 512, one KV head, over
+ *                            the compressed V + k_rot pool (K rebuilt on chip)
+ *                            or over a full K + V control pool.
+ *
+ * Sources of the operations (page title, section):
+ *   [pegainfer] "Gemma 4" (pegainfer model page): intro, "Scheduling",
+ *               "Architecture notes".  Five of six layers are sliding-window
+ *               local attention at head dim 256 (window 1024, RoPE on all 256
+ *               dims, theta 10k); every sixth layer and the last are global
+ *               attention at head dim 512 with one KV head and a proportional
+ *               RoPE on 128 of 512 dims (theta 1M, denominator 512).  Each
+ *               kind has its own paged pool of 16-token pages; every active
+ *               request advances one token per batched step and a new
+ *               prompt's rows are computed in the same step.
+ *   [Gewell]    "Gewell - Gemma4 inference engine", "the Why": K and V are
+ *               tied on global layers and RoPE rotates 25% of K, so a token
+ *               can be cached as V plus the rotated K slice (0.625x of K+V);
+ *               K is rebuilt from V for the attention math.
+ *   [PR1012]    "feat(gemma4): the sliding family serves an opt in fp8 KV
+ *               pool", "Description": the sliding family's K/V may be stored
+ *               as e4m3 at scale 1.0; the element type is an enum on the
+ *               pool layout; entry points without an fp8 variant refuse a
+ *               one-byte layout.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates, frees or synchronises; every call only
+ *     enqueues work on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream) and returns.
+ *   - Arguments are validated on the host before anything is launched.  A
+ *     failure returns a non-zero gw_status and leaves a message, naming the
+ *     entry point, in gw_last_error() (thread-local).
+ *   - Values that live in device memory (slots, positions, lengths, page ids)
+ *     are checked by the kernels: an out-of-range value skips the access it
+ *     would have made and ORs a GW_DEV_* bit into *dev_status (a device int32
+ *     the caller zeroes and reads when it wants; may be NULL).  Output rows of
+ *     a sequence with out-of-range metadata are written as zeros.
+ *   - bf16 is IEEE binary32 truncated to 16 bits; e4m3 is the OCP "e4m3fn"
+ *     8-bit format (bias 7, max 448, no infinities).
+ */
+#ifndef GW_H
+#define GW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+typedef int32_t gw_status;
+#define GW_OK 0
+#define GW_ERR_INVALID_ARG 1 /* null/misaligned pointer, bad size or geometry */
+#define GW_ERR_UNSUPPORTED 2 /* valid but not implemented, e.g. e4m3 global  */
+#define GW_ERR_WORKSPACE 3   /* workspace_bytes below gw_attn_workspace_bytes */
+#define GW_ERR_CUDA 4        /* a launch failed; message has the CUDA error  */
+
+/* bits a kernel ORs into *dev_status */
+#define GW_DEV_SLOT_RANGE 1  /* append slot outside [0, num_pages*16)        */
+#define GW_DEV_POS_RANGE 2   /* append position outside [0, max_pos)          */
+#define GW_DEV_PAGE_RANGE 4  /* block-table entry outside [0, num_pages)      */
+#define GW_DEV_LEN_RANGE 8   /* seq_len < rows, or > max_pages_per_seq * 16   */
+#define GW_DEV_TIMEOUT 16    /* a bounded wait gave up (work abandoned)       */
+#define GW_DEV_WORKSPACE 32  /* the step needs more split-KV partials than the
+                                workspace was sized for (nothing computed)    */
+
+/* ---- pool description --------------------------------------------------- */
+#define GW_KV_BF16 0
+#define GW_KV_E4M3 1
+
+#define GW_LAYOUT_LOCAL 0         /* sliding-window layers                   */
+#define GW_LAYOUT_GLOBAL_FOLDED 1 /* global layers, V(512) + k_rot(128)     */
+#define GW_LAYOUT_GLOBAL_FULL 2   /* global layers, K(512) + V(512) control */
+
+/*
+ * A paged KV pool: `num_pages` pages of 16 tokens at `base` (device, 256-byte
+ * aligned).  A token lives at slot = page * 16 + offset.  Element order
+ * inside a page:
+ *
+ *   LOCAL   (dtype bf16 or e4m3, head_dim 256, rot_dim 256, kv_heads >= 1)
+ *           [kv_head][K=0 / V=1][token 16][dim 256]
+ *           -> kv_heads * 16 KiB per page (bf16), kv_heads * 8 KiB (e4m3).
+ *   GLOBAL_FOLDED (bf16, head_dim 512, rot_dim 128, kv_heads 1)
+ *           a token row is the 640-vector  V[0:512] || k_rot[0:128],
+ *           stored as [token block 2][column block 80][row 8][column 8]:
+ *           token o = 8*tb + r, row element e = 8*cb + c.  20480 B per page.
+ *   GLOBAL_FULL   (bf16, head_dim 512, rot_dim 128, kv_heads 1)
+ *           a token row is K[0:512] || V[0:512], same 8x8 blocking with 128
+ *           column blocks.  32768 B per page.
+ *
+ * In the folded layout the unrotated dims of K are not stored: attention uses
+ * K = k_rot || V[128:512].  The caller folds the k_norm gain of those dims
+ * into q (exact up to rounding order).
+ */
+typedef struct gw_kv_pool {
+  int32_t layout;    /* GW_LAYOUT_* */
+  int32_t dtype;     /* GW_KV_*     */
+  void* base;        /* device pointer, 256-byte aligned */
+  int64_t num_pages; /* >= 1 */
+  int32_t page_size; /* must be 16 */
+  int32_t kv_heads;  /* local: 1..64; global: 1 */
+  int32_t head_dim;  /* local: 256; global: 512 */
+  int32_t rot_dim;   /* local: 256; global: 128 */
+} gw_kv_pool;
+
+/* Bytes of one page of `pool`, 0 if the description is invalid. */
+size_t gw_pool_page_bytes(const gw_kv_pool* pool);
+
+/*
+ * gw_kv_append - write the step's K/V rows into `pool`.
+ *
+ * [pegainfer] "Architecture notes" (RoPE of each family; global K and V from
+ * one projection), [Gewell] "the Why" (store V + rotated K slice),
+ * [PR1012] "Description" (e4m3 at scale 1.0 for the sliding family).
+ *
+ *   k, v     bf16.  LOCAL: [num_rows][kv_heads][256].  GLOBAL: [num_rows][512]
+ *            (FOLDED reads only k[:, 0:128]; FULL stores k[:, 128:512] as is).
+ *   slot     int32 [num_rows]: page * 16 + offset of each row.
+ *   pos      int32 [num_rows]: the row's absolute position (RoPE angle).
+ *   rope_cs  float32 [max_pos][rot_dim/2][2]: (cos, sin) of pos * inv_f_i,
+ *            inv_f_i = theta^(-2i / head_dim), computed in float64 and
+ *            rounded once to float32.
+ *
+ * For i in [0, rot_dim/2), with x0 = k[i], x1 = k[i + rot_dim/2] (exact
+ * fp32 of the bf16 inputs) and (c, s) = rope_cs[pos][i], the stored rotated
+ * pair is  r0 = fl(fl(x0*c) - fl(x1*s)),  r1 = fl(fl(x1*c) + fl(x0*s))
+ * (binary32, no fused multiply-add), then rounded once to the pool type:
+ * bf16 round-to-nearest-even, or e4m3 round-to-nearest-even saturating to
+ * +-448.  V (and the unrotated K dims of a FULL pool) are copied (bf16) or
+ * rounded once to e4m3.  Rows whose slot or pos is out of range are skipped
+ * (GW_DEV_SLOT_RANGE / GW_DEV_POS_RANGE).  num_rows == 0 is a no-op.
+ * Alignment: k, v 16 B; slot, pos, rope_cs 4 B.
+ * Errors: GW_ERR_INVALID_ARG, GW_ERR_UNSUPPORTED (e4m3 on a global pool:
+ * "supports only local"), GW_ERR_CUDA.
+ */
+gw_status gw_kv_append(const gw_kv_pool* pool, const void* k, const void* v, int32_t num_rows,
+                       const int32_t* slot, const int32_t* pos, const float* rope_cs, int32_t max_pos,
+                       int32_t* dev_status, void* stream);
+
+/*
+ * gw_decode_attn_local - sliding-window attention on a LOCAL pool.
+ *
+ * [pegainfer] "Architecture notes", "Scheduling".  Sequence b holds tokens
+ * [0, seq_lens[b]) (after this step's append) and contributes
+ * n_b = cu_q_rows[b+1] - cu_q_rows[b] query rows, at positions
+ * p = seq_lens[b] - n_b + r.  Row r of q head h attends to keys
+ * j in [max(0, p - window + 1), p] of KV head h / (num_q_heads / kv_heads):
+ *
+ *   o = sum_j softmax_j(scale * q . K_j) V_j      (fp32 accumulation)
+ *
+ * Rows with n_b == 1 take the split-KV decode kernel (partials in
+ * `workspace`, then a log-sum-exp combine); rows of sequences with n_b > 1
+ * (prompt rows of a mixed step) take the causal prompt-row kernel.  The split
+ * plan of a sequence depends only on its own length, so its result is
+ * bit-identical whatever else is in the batch.
+ *
+ *   q, out       bf16 [total_rows][num_q_heads][256], total_rows = cu_q_rows[batch].
+ *   cu_q_rows    int32 [batch+1], non-decreasing, cu_q_rows[0] = 0.
+ *   seq_lens     int32 [batch].
+ *   block_table  int32 [batch][max_pages_per_seq]: physical page of each
+ *                logical page; entries before the window may be anything.
+ *   max_q_rows   host bound on n_b (1 for a pure decode step).
+ *   window       >= 1 (1024 for the served model).
+ *   workspace    device scratch of at least gw_attn_workspace_bytes(...),
+ *                16-byte aligned; contents need no initialisation.
+ * Errors: GW_ERR_INVALID_ARG, GW_ERR_WORKSPACE, GW_ERR_UNSUPPORTED
+ * (num_q_heads / kv_heads not in {1,2,4,8}), GW_ERR_CUDA.
+ */
+gw_status gw_decode_attn_local(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,
+                               int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,
+                               const int32_t* block_table, int32_t max_pages_per_seq, int32_t max_q_rows,
+                               int32_t window, float scale, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream);
+
+/*
+ * gw_decode_attn_global - global attention on a GLOBAL_FOLDED or GLOBAL_FULL
+ * pool: as gw_decode_attn_local with no window (j in [0, p]) and head dim 512.
+ *
+ * [pegainfer] "Architecture notes"; [Gewell] "the Why".  On a FOLDED pool the
+ * kernel forms K_j = k_rot_j || V_j[128:512] on chip from the same page tile
+ * that supplies V_j.  num_q_heads must be 8, 16 or 32.  Errors as above;
+ * GW_ERR_UNSUPPORTED for an e4m3 pool ("supports only local").
+ */
+gw_status gw_decode_attn_global(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,
+                                int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,
+                                const int32_t* block_table, int32_t max_pages_per_seq, int32_t max_q_rows,
+                                float scale, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                void* stream);
+
+/*
+ * Workspace bytes an attention call on `pool` needs for `batch` sequences of
+ * at most `max_seq_len` tokens and `max_q_rows` rows each (window ignored for
+ * global pools).  0 on an invalid description.
+ */
+size_t gw_attn_workspace_bytes(const gw_kv_pool* pool, int32_t num_q_heads, int32_t batch,
+                               int32_t max_seq_len, int32_t max_q_rows, int32_t window);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* gw_last_error(void);
+
+/* ABI version of this library. */
+int32_t gw_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GW_H */

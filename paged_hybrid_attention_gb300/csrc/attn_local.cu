@@ -1,0 +1,418 @@
+// Sliding-window (local) decode attention over the paged LOCAL pool.
+//
+// "Gemma 4" (pegainfer model page), "Architecture notes" and "Scheduling":
+// five of six layers attend over the last 1024 tokens with head dim 256 and
+// grouped KV heads, each in its own pool of 16-token pages; every active
+// request advances one token per batched step.  "feat(gemma4): the sliding
+// family serves an opt in fp8 KV pool", "Description": the pool may hold
+// e4m3 at scale 1.0; here it is widened to fp32 on the load path.
+//
+// Design (split-KV flash decoding on CUDA cores; a GQA group of G <= 8 query
+// heads per KV head is too narrow for a tensor-core contraction):
+//   * Work unit = (sequence, KV head, chunk of up to 4 bf16 / 8 e4m3 pages of
+//     the window).  A plan kernel turns lengths into unit offsets; the split
+//     depends on the sequence's own length only.
+//   * Persistent CTAs, one per SM, of 8 independent warps.  Each warp takes
+//     units from an atomic counter and streams 8 KiB stages (8 tokens of K and
+//     V for bf16, 16 for e4m3) with cp.async.bulk into a private 3-stage ring,
+//     prefetching across unit boundaries.
+//   * Lane l owns head dims [8l, 8l+8).  q.K partial dot products are reduced
+//     across lanes with a transpose-reduction whose token order is permuted by
+//     lane bits, so every level is one shuffle + add per value (no selects).
+//   * Online softmax in base 2 (scale * log2 e folded into q), fp32 throughout.
+//   * Each unit writes an unnormalised partial (m, l, o); a combine kernel
+//     merges a sequence's partials in chunk order (log-sum-exp) into bf16.
+#include "common.cuh"
+
+namespace gw {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kStages = 3;
+constexpr int kStageBytes = 8192;
+constexpr int kRing = kStages + 2;
+
+struct Unit {
+  int32_t s, g, hp_lo, n, tok_lo, tok_hi, unit, row;
+};
+
+struct __align__(128) WarpSmem {
+  uint8_t stage[kStages][kStageBytes];
+  uint64_t bar[kStages];
+  int32_t valid[kStages];
+  int32_t pad_;
+  Unit ring[kRing];
+  float pbuf[16 * 8];
+};
+
+template <int DT>
+struct Traits {
+  static constexpr int kEs = DT == GW_KV_BF16 ? 2 : 1;
+  static constexpr int kTok = kStageBytes / (2 * 256 * kEs);  // tokens per stage: 8 / 16
+  static constexpr int kSpp = kPage / kTok;                   // stages per page: 2 / 1
+  static constexpr int kLevels = kTok == 16 ? 4 : 3;          // halving levels of the reduction
+  static constexpr int kChunk = DT == GW_KV_BF16 ? kLocalChunkPagesBf16 : kLocalChunkPagesE4m3;
+};
+
+__host__ __device__ __forceinline__ int local_chunks(int L, int window, int chunk) {
+  const int first = L > window ? L - window : 0;
+  const int p0 = first / kPage, p1 = (L - 1) / kPage;
+  return (p1 - p0 + chunk) / chunk;
+}
+
+__device__ __forceinline__ bool len_ok(const LocalArgs& a, int L, int n) {
+  return L >= 1 && L >= n && static_cast<int64_t>(L) <= static_cast<int64_t>(a.max_pages) * kPage;
+}
+
+// One CTA: unit_base[s] = units of sequences before s (decode rows only),
+// counter = 0.
+__global__ void plan_local_kernel(const LocalArgs a, int chunk) {
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < a.batch; base += blockDim.x) {
+    const int s = base + threadIdx.x;
+    int units = 0;
+    if (s < a.batch) {
+      const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
+      const int L = a.seq_lens[s];
+      if (n == 1) {
+        if (len_ok(a, L, n))
+          units = a.kv_heads * local_chunks(L, a.window, chunk);
+        else
+          set_status(a.status, GW_DEV_LEN_RANGE);
+      }
+    }
+    // block exclusive scan
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = units;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(~0u, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      int v = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(~0u, v, o);
+        if (lane >= o) v += y;
+      }
+      warp_sums[lane] = v;
+    }
+    __syncthreads();
+    const int excl = carry + (w > 0 ? warp_sums[w - 1] : 0) + x - units;
+    if (s < a.batch) a.unit_base[s] = excl;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = excl + units;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    a.unit_base[a.batch] = carry;
+    *a.counter = 0;
+    if (carry > a.max_units) set_status(a.status, GW_DEV_WORKSPACE);
+  }
+}
+
+template <class T>
+__device__ __forceinline__ Unit decode_unit(const LocalArgs& a, int u) {
+  int lo = 0, hi = a.batch;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.unit_base[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  Unit d;
+  d.s = lo;
+  const int L = a.seq_lens[lo];
+  const int first = L > a.window ? L - a.window : 0;
+  const int p0 = first / kPage, p1 = (L - 1) / kPage;
+  const int nc = (p1 - p0 + T::kChunk) / T::kChunk;
+  const int r = u - a.unit_base[lo];
+  d.g = r / nc;
+  const int c = r % nc;
+  const int lpa = p0 + c * T::kChunk;
+  const int lpb = min(lpa + T::kChunk, p1 + 1);
+  d.tok_lo = max(first, lpa * kPage);
+  d.tok_hi = min(L, lpb * kPage);
+  d.hp_lo = d.tok_lo / T::kTok;
+  d.n = (d.tok_hi - 1) / T::kTok + 1 - d.hp_lo;
+  d.unit = u;
+  d.row = a.cu_q_rows[lo];
+  return d;
+}
+
+template <int DT>
+__device__ __forceinline__ void load_row8(const uint8_t* row_base, int lane, float (&f)[8]) {
+  if constexpr (DT == GW_KV_BF16) {
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(row_base + lane * 16), f);
+  } else {
+    e4m3x8_to_f32(*reinterpret_cast<const uint2*>(row_base + lane * 8), f);
+  }
+}
+
+// Transpose-reduction over the 32 lanes of x[N] (N = tokens per stage) whose
+// entry j holds token j ^ perm(lane).  Each halving level keeps the lower half
+// and adds the partner's upper half; afterwards x[0] is the full sum for token
+// perm(lane), replicated over the remaining butterfly lanes.
+template <int N, int O>
+__device__ __forceinline__ void xreduce(float* x) {
+  if constexpr (O >= 1) {
+    if constexpr (N > 1) {
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i + N / 2], O);
+      xreduce<N / 2, O / 2>(x);
+    } else {
+      x[0] += __shfl_xor_sync(0xffffffffu, x[0], O);
+      xreduce<1, O / 2>(x);
+    }
+  }
+}
+
+template <int DT, int G>
+__global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const LocalArgs a) {
+  using T = Traits<DT>;
+  constexpr int kTok = T::kTok;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WarpSmem& sm = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
+  const int total_units = a.unit_base[a.batch];
+  if (total_units > a.max_units) return;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) mbar_init(&sm.bar[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const uint64_t pol = policy_evict_first();
+  const int64_t head_bytes = 2LL * kPage * 256 * T::kEs;  // K + V of one KV head in one page
+  const int perm = (lane >> (5 - T::kLevels)) & (kTok - 1);
+  const bool canon = (lane & ((1 << (5 - T::kLevels)) - 1)) == 0;
+
+  int f_slot = 0, f_i = 0;
+  bool f_done = false;
+  uint32_t issued = 0, consumed = 0;
+
+  auto grab = [&](int slot) -> bool {
+    int u = 0;
+    if (lane == 0) u = atomicAdd(a.counter, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if (u >= total_units) return false;
+    const Unit d = decode_unit<T>(a, u);
+    if (lane == 0) sm.ring[slot] = d;
+    __syncwarp();
+    return true;
+  };
+
+  auto issue = [&]() {
+    const Unit d = sm.ring[f_slot];
+    const int st = issued % kStages;
+    const int hp = d.hp_lo + f_i;
+    const int lp = hp / T::kSpp, half = hp % T::kSpp;
+    if (lane == 0) {
+      const int32_t phys = a.block_table[static_cast<int64_t>(d.s) * a.max_pages + lp];
+      if (phys < 0 || phys >= a.num_pages) {
+        sm.valid[st] = 0;
+        set_status(a.status, GW_DEV_PAGE_RANGE);
+        mbar_arrive(&sm.bar[st]);
+      } else {
+        sm.valid[st] = 1;
+        const uint8_t* kb = a.pool + (static_cast<int64_t>(phys) * a.kv_heads + d.g) * head_bytes +
+                            static_cast<int64_t>(half) * kTok * 256 * T::kEs;
+        mbar_arrive_expect_tx(&sm.bar[st], kStageBytes);
+        bulk_g2s(sm.stage[st], kb, kStageBytes / 2, &sm.bar[st], pol);
+        bulk_g2s(sm.stage[st] + kStageBytes / 2, kb + kPage * 256 * T::kEs, kStageBytes / 2, &sm.bar[st], pol);
+      }
+    }
+    ++issued;
+    if (++f_i == d.n) {
+      f_i = 0;
+      f_slot = (f_slot + 1) % kRing;
+      f_done = !grab(f_slot);
+    }
+  };
+
+  f_done = !grab(0);
+  while (!f_done && issued - consumed < kStages) issue();
+
+  float qf[G][8], o[G][8], m[G], lsum[G];
+  int c_slot = 0, c_i = 0;
+  while (consumed < issued) {
+    const Unit d = sm.ring[c_slot];
+    if (c_i == 0) {
+      const uint16_t* qrow = a.q + (static_cast<int64_t>(d.row) * a.num_q_heads + d.g * G) * 256 + lane * 8;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float t[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(qrow + h * 256), t);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          qf[h][i] = t[i] * a.scale_log2;
+          o[h][i] = 0.f;
+        }
+        m[h] = -INFINITY;
+        lsum[h] = 0.f;
+      }
+    }
+    const int st = consumed % kStages;
+    if (!mbar_wait(&sm.bar[st], (consumed / kStages) & 1, a.status)) {
+      // abandon: drain whatever is still in flight (bounded) and leave
+      for (uint32_t k = consumed + 1; k < issued; ++k) mbar_wait(&sm.bar[k % kStages], (k / kStages) & 1, nullptr);
+      return;
+    }
+    const uint8_t* Ks = sm.stage[st];
+    const uint8_t* Vs = Ks + kStageBytes / 2;
+    const int t0 = (d.hp_lo + c_i) * kTok;
+
+    // ---- logits: x[h][j] = q_h . K[j ^ perm] over this lane's 8 dims
+    float x[G][kTok];
+#pragma unroll
+    for (int j = 0; j < kTok; ++j) {
+      float kf[8];
+      load_row8<DT>(Ks + (j ^ perm) * 256 * T::kEs, lane, kf);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float acc = qf[h][0] * kf[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) acc = fmaf(qf[h][i], kf[i], acc);
+        x[h][j] = acc;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) xreduce<kTok, 16>(x[h]);
+
+    const int tabs = t0 + perm;
+    const bool valid = sm.valid[st] && tabs >= d.tok_lo && tabs < d.tok_hi;
+    float p[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float s = valid ? x[h][0] : -INFINITY;
+      float mx = s;
+#pragma unroll
+      for (int O = 1 << (5 - T::kLevels); O < 32; O <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, O));
+      const float mnew = fmaxf(m[h], mx);
+      const float alpha = mnew == -INFINITY ? 1.f : ex2(m[h] - mnew);
+      p[h] = valid ? ex2(s - mnew) : 0.f;
+      m[h] = mnew;
+      lsum[h] = lsum[h] * alpha + (canon ? p[h] : 0.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[h][i] *= alpha;
+    }
+    if (canon) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) sm.pbuf[perm * G + h] = p[h];
+    }
+    __syncwarp();
+
+    // ---- o += p[t] * V[t]
+#pragma unroll
+    for (int t = 0; t < kTok; ++t) {
+      float vf[8];
+      load_row8<DT>(Vs + t * 256 * T::kEs, lane, vf);
+      float pt[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) pt[h] = sm.pbuf[t * G + h];
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[h][i] = fmaf(pt[h], vf[i], o[h][i]);
+    }
+    __syncwarp();
+    ++consumed;
+    if (++c_i == d.n) {
+      // ---- unit done: write the unnormalised partial
+      float* po = a.part_o + static_cast<int64_t>(d.unit) * G * 256 + lane * 8;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float l = lsum[h];
+#pragma unroll
+        for (int O = 1; O < 32; O <<= 1) l += __shfl_xor_sync(0xffffffffu, l, O);
+        *reinterpret_cast<float4*>(po + h * 256) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+        *reinterpret_cast<float4*>(po + h * 256 + 4) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+        if (lane == h) a.part_ml[static_cast<int64_t>(d.unit) * G + h] = make_float2(m[h], l);
+      }
+      c_i = 0;
+      c_slot = (c_slot + 1) % kRing;
+    }
+    while (!f_done && issued - consumed < kStages) issue();
+  }
+}
+
+// One warp per (sequence, q head): merge the sequence's partials for that head.
+template <int G, int kChunk>
+__global__ void local_combine_kernel(const LocalArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  if (w >= static_cast<int64_t>(a.batch) * a.num_q_heads) return;
+  const int s = static_cast<int>(w / a.num_q_heads), h = static_cast<int>(w % a.num_q_heads);
+  const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
+  if (n != 1) return;
+  const int L = a.seq_lens[s];
+  uint16_t* dst = a.out + (static_cast<int64_t>(a.cu_q_rows[s]) * a.num_q_heads + h) * 256 + lane * 8;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float den = 0.f;
+  if (len_ok(a, L, 1) && a.unit_base[a.batch] <= a.max_units) {
+    const int nc = local_chunks(L, a.window, kChunk);
+    const int g = h / G, hh = h % G;
+    const int64_t ub = a.unit_base[s] + static_cast<int64_t>(g) * nc;
+    float M = -INFINITY;
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, a.part_ml[(ub + c) * G + hh].x);
+    if (M != -INFINITY) {
+      for (int c = 0; c < nc; ++c) {
+        const float2 ml = a.part_ml[(ub + c) * G + hh];
+        const float wgt = ex2(ml.x - M);
+        den += wgt * ml.y;
+        const float* po = a.part_o + ((ub + c) * G + hh) * 256 + lane * 8;
+        const float4 u0 = *reinterpret_cast<const float4*>(po);
+        const float4 u1 = *reinterpret_cast<const float4*>(po + 4);
+        acc[0] += wgt * u0.x; acc[1] += wgt * u0.y; acc[2] += wgt * u0.z; acc[3] += wgt * u0.w;
+        acc[4] += wgt * u1.x; acc[5] += wgt * u1.y; acc[6] += wgt * u1.z; acc[7] += wgt * u1.w;
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint32_t wv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+    wv[i] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+}
+
+template <int DT, int G>
+cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
+  using T = Traits<DT>;
+  plan_local_kernel<<<1, 1024, 0, st>>>(a, T::kChunk);
+  const size_t smem = sizeof(WarpSmem) * kWarps;
+  auto kern = local_decode_kernel<DT, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms(), kWarps * 32, smem, st>>>(a);
+  const int64_t warps = static_cast<int64_t>(a.batch) * a.num_q_heads;
+  const int blocks = static_cast<int>((warps + 7) / 8);
+  local_combine_kernel<G, T::kChunk><<<blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_dt(int group, const LocalArgs& a, cudaStream_t st) {
+  switch (group) {
+    case 1: return launch_typed<DT, 1>(a, st);
+    case 2: return launch_typed<DT, 2>(a, st);
+    case 4: return launch_typed<DT, 4>(a, st);
+    case 8: return launch_typed<DT, 8>(a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_local_decode(int dtype, int group, const LocalArgs& a, cudaStream_t st) {
+  return dtype == GW_KV_BF16 ? launch_dt<GW_KV_BF16>(group, a, st) : launch_dt<GW_KV_E4M3>(group, a, st);
+}
+
+}  // namespace gw

@@ -1,0 +1,79 @@
+// Internal interface between the C-ABI layer (gw_abi.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/gw.h"
+
+namespace gw {
+
+// ---- split-KV plan constants ------------------------------------------------
+// A local decode work unit is (sequence, KV head, chunk of kLocalChunkPages
+// logical pages of that sequence's window); a global unit is (sequence, chunk
+// of kGlobalChunkPages pages).  Chunks depend only on the sequence's own
+// length, so a row's arithmetic never depends on the rest of the batch.
+constexpr int kLocalChunkPagesBf16 = 4;
+constexpr int kLocalChunkPagesE4m3 = 8;
+constexpr int kGlobalChunkPages = 16;
+
+// Workspace layout (offsets from the 256-byte aligned workspace base):
+//   [0, 256)          int32 work counter (+ padding)
+//   [256, ub_end)     int32 unit_base[batch + 1], rounded up to 256 bytes
+//   [ub_end, ml_end)  float2 (m, l) per (unit, head of the unit)
+//   [ml_end, ...)     float  o[unit][head of the unit][head_dim]
+struct WsLayout {
+  size_t counter, unit_base, ml, o, total;
+  int64_t max_units;
+  int heads_per_unit;
+};
+
+WsLayout ws_layout(int layout, int dtype, int kv_heads, int num_q_heads, int batch, int max_seq_len,
+                   int window);
+
+struct LocalArgs {
+  const uint8_t* pool;
+  int64_t num_pages;
+  int32_t kv_heads;
+  int32_t num_q_heads;
+  const uint16_t* q;  // bf16 bits
+  uint16_t* out;      // bf16 bits
+  int32_t batch;
+  const int32_t* cu_q_rows;
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  int32_t max_pages;
+  int32_t window;  // local; ignored for global
+  float scale_log2;  // softmax scale * log2(e)
+  int32_t* counter;
+  int32_t* unit_base;
+  float2* part_ml;
+  float* part_o;
+  int64_t max_units;
+  int32_t* status;
+};
+
+struct AppendArgs {
+  uint8_t* pool;
+  int64_t num_pages;
+  int32_t kv_heads;
+  const uint16_t* k;
+  const uint16_t* v;
+  int32_t num_rows;
+  const int32_t* slot;
+  const int32_t* pos;
+  const float* rope_cs;
+  int32_t max_pos;
+  int32_t* status;
+};
+
+int num_sms();
+
+cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream_t st);
+cudaError_t launch_local_decode(int dtype, int group, const LocalArgs& a, cudaStream_t st);
+cudaError_t launch_global_decode(int layout, const LocalArgs& a, cudaStream_t st);
+cudaError_t launch_local_prompt(int dtype, int group, const LocalArgs& a, int max_q_rows, cudaStream_t st);
+cudaError_t launch_global_prompt(int layout, const LocalArgs& a, int max_q_rows, cudaStream_t st);
+
+}  // namespace gw

@@ -1,0 +1,210 @@
+// gw_kv_append kernels: RoPE on the rotated slice of K, then page write.
+//
+// "Gemma 4" (pegainfer model page), "Architecture notes": local K rotates all
+// 256 dims (theta 10k); global K rotates 128 of 512 dims with the full head
+// dim as frequency denominator (theta 1M); global V is K's projection without
+// RoPE.  "Gewell - Gemma4 inference engine", "the Why": a global token is
+// cached as V plus the rotated K slice.  "feat(gemma4): the sliding family
+// serves an opt in fp8 KV pool", "Description": local K/V may be stored e4m3
+// at scale 1.0.
+//
+// Every thread handles 8 rotation pairs (or 8 copied elements): one 16-byte
+// load per operand and one 16-byte (bf16) or 8-byte (e4m3) store per output
+// chunk.  The rotation is evaluated with explicitly rounded binary32 multiply
+// and add (__fmul_rn / __fsub_rn / __fadd_rn), so no multiply-add is fused
+// and the stored bits are exactly those of the stated operation order.
+#include "common.cuh"
+
+namespace gw {
+namespace {
+
+struct Pack8 {
+  uint4 bf;   // 8 bf16
+  uint2 e4;   // 8 e4m3
+};
+
+__device__ __forceinline__ void load_bf16x8(const uint16_t* p, float (&f)[8]) {
+  bf16x8_to_f32(*reinterpret_cast<const uint4*>(p), f);
+}
+
+__device__ __forceinline__ uint4 f32x8_to_bf16(const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);  // .x = low half
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint2 f32x8_to_e4m3(const float (&f)[8]) {
+  uint32_t w[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i], f[4 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+    uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i + 2], f[4 * i + 3]), __NV_SATFINITE, __NV_E4M3);
+    w[i] = (lo & 0xFFFFu) | (hi << 16);
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+// Rotate 8 pairs (x0[i], x1[i]) with table entries cs[2i], cs[2i+1].
+__device__ __forceinline__ void rotate8(float (&x0)[8], float (&x1)[8], const float* cs) {
+  float c[8], s[8];
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    float4 t = *reinterpret_cast<const float4*>(cs + 2 * i);
+    c[i] = t.x;
+    s[i] = t.y;
+    c[i + 1] = t.z;
+    s[i + 1] = t.w;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float r0 = __fsub_rn(__fmul_rn(x0[i], c[i]), __fmul_rn(x1[i], s[i]));
+    const float r1 = __fadd_rn(__fmul_rn(x1[i], c[i]), __fmul_rn(x0[i], s[i]));
+    x0[i] = r0;
+    x1[i] = r1;
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void store8(uint8_t* base, int64_t elem, const float (&f)[8]) {
+  if constexpr (DT == GW_KV_BF16) {
+    *reinterpret_cast<uint4*>(base + elem * 2) = f32x8_to_bf16(f);
+  } else {
+    *reinterpret_cast<uint2*>(base + elem) = f32x8_to_e4m3(f);
+  }
+}
+
+__device__ __forceinline__ bool row_ok(const AppendArgs& a, int64_t row, int32_t& slot, int32_t& pos,
+                                       bool report) {
+  slot = a.slot[row];
+  pos = a.pos[row];
+  if (slot < 0 || static_cast<int64_t>(slot) >= a.num_pages * kPage) {
+    if (report) set_status(a.status, GW_DEV_SLOT_RANGE);
+    return false;
+  }
+  if (pos < 0 || pos >= a.max_pos) {
+    if (report) set_status(a.status, GW_DEV_POS_RANGE);
+    return false;
+  }
+  return true;
+}
+
+// LOCAL: one work item = (row, kv head, j in [0,16)): pairs (8j+i, 128+8j+i)
+// of K, and V chunks 8j and 128+8j.
+template <int DT>
+__global__ void append_local_kernel(const AppendArgs a) {
+  const int64_t total = static_cast<int64_t>(a.num_rows) * a.kv_heads * 16;
+  for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
+       w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(w % 16);
+    const int64_t rh = w / 16;
+    const int g = static_cast<int>(rh % a.kv_heads);
+    const int64_t row = rh / a.kv_heads;
+    int32_t slot, pos;
+    if (!row_ok(a, row, slot, pos, j == 0 && g == 0)) continue;
+    const int64_t page = slot / kPage, off = slot % kPage;
+    const uint16_t* krow = a.k + (row * a.kv_heads + g) * 256;
+    const uint16_t* vrow = a.v + (row * a.kv_heads + g) * 256;
+    float x0[8], x1[8];
+    load_bf16x8(krow + 8 * j, x0);
+    load_bf16x8(krow + 128 + 8 * j, x1);
+    rotate8(x0, x1, a.rope_cs + (static_cast<int64_t>(pos) * 128 + 8 * j) * 2);
+    const int64_t kbase = (((page * a.kv_heads + g) * 2 + 0) * kPage + off) * 256;
+    const int64_t vbase = (((page * a.kv_heads + g) * 2 + 1) * kPage + off) * 256;
+    store8<DT>(a.pool, kbase + 8 * j, x0);
+    store8<DT>(a.pool, kbase + 128 + 8 * j, x1);
+    if constexpr (DT == GW_KV_BF16) {
+      uint16_t* p = reinterpret_cast<uint16_t*>(a.pool);
+      *reinterpret_cast<uint4*>(p + vbase + 8 * j) = *reinterpret_cast<const uint4*>(vrow + 8 * j);
+      *reinterpret_cast<uint4*>(p + vbase + 128 + 8 * j) = *reinterpret_cast<const uint4*>(vrow + 128 + 8 * j);
+    } else {
+      float v0[8], v1[8];
+      load_bf16x8(vrow + 8 * j, v0);
+      load_bf16x8(vrow + 128 + 8 * j, v1);
+      store8<DT>(a.pool, vbase + 8 * j, v0);
+      store8<DT>(a.pool, vbase + 128 + 8 * j, v1);
+    }
+  }
+}
+
+// Element index of (page, token o, row element e) in a GLOBAL page whose
+// rows have kRow elements, blocked 8 tokens x 8 elements.
+template <int kRow>
+__device__ __forceinline__ int64_t tiled(int64_t page, int o, int e) {
+  constexpr int kBlk = kRow / 8;
+  return page * (kPage * kRow) + ((static_cast<int64_t>(o / 8) * kBlk + e / 8) * 8 + (o % 8)) * 8 + (e % 8);
+}
+
+// GLOBAL FOLDED: row = V[0:512] || k_rot[0:128]; items per row: 64 V chunks
+// + 8 rotation items (pairs 8t..8t+7 and 64+8t..).
+// GLOBAL FULL:   row = K[0:512] || V[0:512]; items per row: 8 rotation items,
+// 48 copies of k[128:512], 64 V chunks.
+template <int LAYOUT>
+__global__ void append_global_kernel(const AppendArgs a) {
+  constexpr bool kFolded = LAYOUT == GW_LAYOUT_GLOBAL_FOLDED;
+  constexpr int kRow = kFolded ? 640 : 1024;
+  constexpr int kItems = kFolded ? 72 : 120;
+  const int64_t total = static_cast<int64_t>(a.num_rows) * kItems;
+  uint16_t* pool = reinterpret_cast<uint16_t*>(a.pool);
+  for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
+       w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int it = static_cast<int>(w % kItems);
+    const int64_t row = w / kItems;
+    int32_t slot, pos;
+    if (!row_ok(a, row, slot, pos, it == 0)) continue;
+    const int64_t page = slot / kPage;
+    const int off = slot % kPage;
+    const uint16_t* krow = a.k + row * 512;
+    const uint16_t* vrow = a.v + row * 512;
+    const int rot_item = kFolded ? it - 64 : it;  // rotation items
+    if (rot_item >= 0 && rot_item < 8) {
+      const int t = rot_item;
+      float x0[8], x1[8];
+      load_bf16x8(krow + 8 * t, x0);
+      load_bf16x8(krow + 64 + 8 * t, x1);
+      rotate8(x0, x1, a.rope_cs + (static_cast<int64_t>(pos) * 64 + 8 * t) * 2);
+      const int e0 = kFolded ? 512 + 8 * t : 8 * t;
+      *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, e0)) = f32x8_to_bf16(x0);
+      *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, e0 + 64)) = f32x8_to_bf16(x1);
+    } else if (kFolded) {  // V chunk it in [0, 64)
+      *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, 8 * it)) =
+          *reinterpret_cast<const uint4*>(vrow + 8 * it);
+    } else if (it < 56) {  // K[128:512] chunk
+      const int e = 128 + 8 * (it - 8);
+      *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, e)) = *reinterpret_cast<const uint4*>(krow + e);
+    } else {  // V chunk
+      const int e = 8 * (it - 56);
+      *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, 512 + e)) =
+          *reinterpret_cast<const uint4*>(vrow + e);
+    }
+  }
+}
+
+int grid_for(int64_t items, int block) {
+  int64_t blocks = (items + block - 1) / block;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+  return static_cast<int>(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream_t st) {
+  constexpr int kBlock = 256;
+  if (layout == GW_LAYOUT_LOCAL) {
+    const int grid = grid_for(static_cast<int64_t>(a.num_rows) * a.kv_heads * 16, kBlock);
+    if (dtype == GW_KV_BF16)
+      append_local_kernel<GW_KV_BF16><<<grid, kBlock, 0, st>>>(a);
+    else
+      append_local_kernel<GW_KV_E4M3><<<grid, kBlock, 0, st>>>(a);
+  } else if (layout == GW_LAYOUT_GLOBAL_FOLDED) {
+    append_global_kernel<GW_LAYOUT_GLOBAL_FOLDED><<<grid_for(static_cast<int64_t>(a.num_rows) * 72, kBlock), kBlock, 0, st>>>(a);
+  } else {
+    append_global_kernel<GW_LAYOUT_GLOBAL_FULL><<<grid_for(static_cast<int64_t>(a.num_rows) * 120, kBlock), kBlock, 0, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gw

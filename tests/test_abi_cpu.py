@@ -1,0 +1,116 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared
+symbol, and refuses bad arguments on the host before launching anything."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import rope
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+gw = pytest.importorskip("paged_hybrid_attention_gb300.gw", reason="libgw.so not built")
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "gw.h")) as f:
+        src = f.read()
+    return sorted(set(re.findall(r"^\s*(?:gw_status|size_t|const char\*|int32_t)\s+(gw_\w+)\s*\(", src, re.M)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(gw.lib(), n), n
+        assert n in gw.EXPORTS
+
+
+def _desc(layout=gw.LAYOUT_LOCAL, dtype=gw.KV_BF16, page=16, kvh=16, hd=256, rd=256, base=1 << 20):
+    return gw.PoolDesc(layout, dtype, base, 100, page, kvh, hd, rd)
+
+
+def test_page_bytes_and_bad_descriptions():
+    L = gw.lib()
+    assert L.gw_pool_page_bytes(ctypes.byref(_desc())) == 16 * 16384
+    assert L.gw_pool_page_bytes(ctypes.byref(_desc(dtype=gw.KV_E4M3))) == 16 * 8192
+    assert L.gw_pool_page_bytes(ctypes.byref(_desc(gw.LAYOUT_GLOBAL_FOLDED, kvh=1, hd=512, rd=128))) == 20480
+    assert L.gw_pool_page_bytes(ctypes.byref(_desc(gw.LAYOUT_GLOBAL_FULL, kvh=1, hd=512, rd=128))) == 32768
+    assert L.gw_pool_page_bytes(ctypes.byref(_desc(page=32))) == 0
+    assert "page_size" in gw.last_error()
+    assert L.gw_pool_page_bytes(ctypes.byref(_desc(base=(1 << 20) + 16))) == 0
+    assert L.gw_pool_page_bytes(ctypes.byref(_desc(gw.LAYOUT_GLOBAL_FOLDED, gw.KV_E4M3, kvh=1, hd=512, rd=128))) == 0
+    assert "supports only local" in gw.last_error()
+
+
+def _fake(n=1 << 24):
+    return ctypes.c_void_p(n)
+
+
+def test_append_refuses_e4m3_global_and_bad_geometry():
+    L = gw.lib()
+    d = _desc(gw.LAYOUT_GLOBAL_FOLDED, gw.KV_E4M3, kvh=1, hd=512, rd=128)
+    st = L.gw_kv_append(ctypes.byref(d), _fake(), _fake(), 4, _fake(), _fake(), _fake(), 10, None, None)
+    assert st == gw.GW_ERR_UNSUPPORTED
+    assert gw.last_error().startswith("gw_kv_append:") and "supports only local" in gw.last_error()
+    d = _desc(hd=128)
+    assert L.gw_kv_append(ctypes.byref(d), _fake(), _fake(), 4, _fake(), _fake(), _fake(), 10, None, None) == \
+        gw.GW_ERR_INVALID_ARG
+    d = _desc()
+    st = L.gw_kv_append(ctypes.byref(d), _fake((1 << 24) + 2), _fake(), 4, _fake(), _fake(), _fake(), 10, None, None)
+    assert st == gw.GW_ERR_INVALID_ARG and "aligned" in gw.last_error()
+    assert L.gw_kv_append(ctypes.byref(d), None, None, 0, None, None, None, 0, None, None) == gw.GW_OK
+
+
+def _local_call(d, hq=32, batch=2, window=1024, ws_bytes=1 << 30, mq=1, scale=0.0625):
+    L = gw.lib()
+    f = _fake()
+    return L.gw_decode_attn_local(ctypes.byref(d), f, f, hq, batch, f, f, f, 64, mq, window, scale, _fake(1 << 28),
+                                  ws_bytes, None, None)
+
+
+def test_attention_host_validation():
+    d = _desc()
+    assert _local_call(d, hq=24) == gw.GW_ERR_INVALID_ARG            # not a multiple of kv heads
+    assert _local_call(d, hq=16 * 16) == gw.GW_ERR_UNSUPPORTED        # group 16
+    assert _local_call(d, window=0) == gw.GW_ERR_INVALID_ARG
+    assert _local_call(d, scale=float("nan")) == gw.GW_ERR_INVALID_ARG
+    assert _local_call(d, ws_bytes=100) == gw.GW_ERR_WORKSPACE
+    assert "workspace_bytes" in gw.last_error()
+    assert _local_call(d, batch=0) == gw.GW_OK                        # empty batch: nothing to do
+    g = _desc(gw.LAYOUT_GLOBAL_FOLDED, kvh=1, hd=512, rd=128)
+    assert _local_call(g) == gw.GW_ERR_INVALID_ARG                    # global pool on the local entry
+    L = gw.lib()
+    f = _fake()
+    st = L.gw_decode_attn_global(ctypes.byref(g), f, f, 12, 2, f, f, f, 64, 1, 0.04, _fake(1 << 28), 1 << 30,
+                                 None, None)
+    assert st == gw.GW_ERR_UNSUPPORTED and gw.last_error().startswith("gw_decode_attn_global:")
+
+
+def test_workspace_size_grows_with_batch_and_length():
+    L = gw.lib()
+    d = _desc()
+    a = L.gw_attn_workspace_bytes(ctypes.byref(d), 32, 16, 8192, 1, 1024)
+    b = L.gw_attn_workspace_bytes(ctypes.byref(d), 32, 32, 8192, 1, 1024)
+    assert 0 < a < b
+    g = _desc(gw.LAYOUT_GLOBAL_FOLDED, kvh=1, hd=512, rd=128)
+    assert L.gw_attn_workspace_bytes(ctypes.byref(g), 32, 8, 131072, 1, 0) > \
+        L.gw_attn_workspace_bytes(ctypes.byref(g), 32, 8, 8192, 1, 0)
+
+
+@pytest.mark.parametrize("theta,R,D", [(1e4, 256, 256), (1e6, 128, 512), (1e4, 128, 512)])
+def test_rope_table_matches_oracle(theta, R, D):
+    """The library's table builder (torch float64) and the oracle's (NumPy
+    float64) agree to one float32 ulp (1e-10 absolute near zero, the float64 ulp of angles up to 1.4e5).  They are not always bit-identical: an
+    ulp of difference between two float64 pow/cos implementations moves the
+    float32 rounding of values that sit near a rounding boundary.  Parity
+    tests therefore hand both sides the same table bytes (the table is an
+    input of gw_kv_append)."""
+    mine = gw.rope_table(theta, R, D, 140000).numpy()
+    ref = rope.rope_table(theta, R, D, 140000)
+    tol = np.maximum(np.spacing(np.abs(ref)).astype(np.float64), 1e-10)
+    assert np.all(np.abs(mine.astype(np.float64) - ref) <= tol)
+    assert np.count_nonzero(mine.view(np.uint32) != ref.view(np.uint32)) < 1e-4 * ref.size
