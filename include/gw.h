@@ -113,7 +113,8 @@ typedef struct gw_kv_pool {
   int32_t rot_dim;   /* local: 256; global: 128 */
 } gw_kv_pool;
 
-/* Bytes of one page of `pool`, 0 if the description is invalid. */
+/* Bytes of one page of `pool`, 0 if the description is invalid (base may be
+ * NULL here: the size is needed before the pool is allocated). */
 size_t gw_pool_page_bytes(const gw_kv_pool* pool);
 
 /*

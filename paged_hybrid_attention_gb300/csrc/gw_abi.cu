@@ -30,9 +30,12 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Pool description checks shared by every entry point.
-gw_status check_pool(const gw_kv_pool* p, const char* fn) {
+// `need_base` is false for the size queries, which may run before the pool
+// memory exists.
+gw_status check_pool(const gw_kv_pool* p, const char* fn, bool need_base = true) {
   if (!p) return fail(GW_ERR_INVALID_ARG, fn, "pool is NULL");
-  if (!p->base || !aligned(p->base, 256)) return fail(GW_ERR_INVALID_ARG, fn, "pool base is NULL or not 256-byte aligned");
+  if (need_base && (!p->base || !aligned(p->base, 256)))
+    return fail(GW_ERR_INVALID_ARG, fn, "pool base is NULL or not 256-byte aligned");
   if (p->num_pages < 1) return fail(GW_ERR_INVALID_ARG, fn, "num_pages must be >= 1");
   if (p->page_size != 16) return fail(GW_ERR_INVALID_ARG, fn, "page_size must be 16 (got %d)", p->page_size);
   if (p->dtype != GW_KV_BF16 && p->dtype != GW_KV_E4M3) return fail(GW_ERR_INVALID_ARG, fn, "unknown dtype %d", p->dtype);
@@ -114,7 +117,7 @@ const char* gw_last_error(void) { return g_err; }
 int32_t gw_version(void) { return 1; }
 
 size_t gw_pool_page_bytes(const gw_kv_pool* pool) {
-  if (check_pool(pool, "gw_pool_page_bytes") != GW_OK) return 0;
+  if (check_pool(pool, "gw_pool_page_bytes", false) != GW_OK) return 0;
   return page_bytes(pool);
 }
 
@@ -150,7 +153,7 @@ gw_status gw_kv_append(const gw_kv_pool* pool, const void* k, const void* v, int
 size_t gw_attn_workspace_bytes(const gw_kv_pool* pool, int32_t num_q_heads, int32_t batch, int32_t max_seq_len,
                                int32_t max_q_rows, int32_t window) {
   (void)max_q_rows;
-  if (check_pool(pool, "gw_attn_workspace_bytes") != GW_OK) return 0;
+  if (check_pool(pool, "gw_attn_workspace_bytes", false) != GW_OK) return 0;
   if (num_q_heads < 1 || batch < 0 || max_seq_len < 0) return 0;
   if (pool->layout == GW_LAYOUT_LOCAL && window < 1) return 0;
   if (num_q_heads % pool->kv_heads) return 0;

@@ -41,7 +41,7 @@ def test_page_bytes_and_bad_descriptions():
     assert L.gw_pool_page_bytes(ctypes.byref(_desc(gw.LAYOUT_GLOBAL_FULL, kvh=1, hd=512, rd=128))) == 32768
     assert L.gw_pool_page_bytes(ctypes.byref(_desc(page=32))) == 0
     assert "page_size" in gw.last_error()
-    assert L.gw_pool_page_bytes(ctypes.byref(_desc(base=(1 << 20) + 16))) == 0
+    assert L.gw_pool_page_bytes(ctypes.byref(_desc(base=0))) == 16 * 16384   # size query before allocation
     assert L.gw_pool_page_bytes(ctypes.byref(_desc(gw.LAYOUT_GLOBAL_FOLDED, gw.KV_E4M3, kvh=1, hd=512, rd=128))) == 0
     assert "supports only local" in gw.last_error()
 
@@ -59,6 +59,9 @@ def test_append_refuses_e4m3_global_and_bad_geometry():
     d = _desc(hd=128)
     assert L.gw_kv_append(ctypes.byref(d), _fake(), _fake(), 4, _fake(), _fake(), _fake(), 10, None, None) == \
         gw.GW_ERR_INVALID_ARG
+    d = _desc(base=(1 << 20) + 16)
+    st = L.gw_kv_append(ctypes.byref(d), _fake(), _fake(), 4, _fake(), _fake(), _fake(), 10, None, None)
+    assert st == gw.GW_ERR_INVALID_ARG and "256-byte" in gw.last_error()
     d = _desc()
     st = L.gw_kv_append(ctypes.byref(d), _fake((1 << 24) + 2), _fake(), 4, _fake(), _fake(), _fake(), 10, None, None)
     assert st == gw.GW_ERR_INVALID_ARG and "aligned" in gw.last_error()
