@@ -1,0 +1,490 @@
+// Global decode attention on the tensor cores (tcgen05 / TMEM), head dim 512,
+// one KV head shared by all q heads.
+//
+// "Gemma 4" (pegainfer model page), "Architecture notes": global layers have a
+// single KV head of dim 512; K and V come from one projection, K through
+// k_norm and RoPE on 128 of the 512 dims.  "Gewell - Gemma4 inference
+// engine", "the Why": so a token can be cached as V plus the rotated K slice
+// (0.625x of K+V) and K rebuilt for the math.  Here that rebuild costs
+// nothing: the folded page tile in shared memory holds V[0:512] and
+// k_rot[0:128] as 8x8 core matrices, and the QK^T contraction simply points
+// its K-dimension descriptors at k_rot for dims [0,128) and at V for dims
+// [128,512) - the same V bytes then feed P.V.
+//
+// All q heads share one KV head, so per 64-token tile the work is two real
+// dense contractions (~51 flop per KV byte):
+//   S^T[64 tok x HQ] = K_tile[64 x 512] . Q^T        (UMMA M=64, N=HQ, K=512)
+//   O^T[512 x HQ]   += V_tile^T[512 x 64] . P^T      (UMMA M=128 x4, N=HQ, K=16 per page)
+// with fp32 accumulators in tensor memory.
+//
+// Warp roles (224 threads, one persistent CTA per SM):
+//   warps 0-3  softmax + epilogue: warp w owns TMEM lanes [32w, 32w+32), i.e.
+//              tokens [16w, 16w+16) of the tile (the M=64 accumulator uses
+//              lanes 0-15 of each 32-lane quadrant) and dims of O^T.
+//   warp 4     producer: takes split-KV units (sequence, chunk of pages) from
+//              an atomic counter and streams whole pages with cp.async.bulk
+//              into a double-buffered 4-page tile (single buffer for the full
+//              K+V control layout, whose pages are 1.6x larger).
+//   warp 5     MMA issuer (one thread) and TMEM owner.
+//   warp 6     loads each unit's q rows into the K-major Q operand.
+// Softmax is base 2 with a lazily updated reference max: a tile only
+// rescales the accumulators when some logit exceeds the reference by more
+// than 8 (p <= 256 otherwise), which after a unit's first tile is rare.
+// Each unit writes an unnormalised partial (m, l, o) for the shared combine.
+#include "tcgen05.cuh"
+
+namespace gw {
+namespace {
+
+constexpr int kTilePages = 4;  // 64 tokens = UMMA M for QK^T
+constexpr int kRing = 4;       // tile descriptors in flight
+constexpr int kThreads = 224;
+constexpr float kLazyThreshold = 8.f;
+
+template <int LAYOUT>
+struct GTraits;
+template <>
+struct GTraits<GW_LAYOUT_GLOBAL_FOLDED> {
+  static constexpr int kPageBytes = 20480;
+  static constexpr int kBlk = 80;   // 8-column blocks per 8-token block
+  static constexpr int kNumBuf = 2;
+  static constexpr int kVcb = 0;    // column block of V dim 0
+  // column block holding K dims [16 ks, 16 ks + 16)
+  __device__ static int k_cb(int ks) { return ks < 8 ? 64 + 2 * ks : 2 * ks; }
+};
+template <>
+struct GTraits<GW_LAYOUT_GLOBAL_FULL> {
+  static constexpr int kPageBytes = 32768;
+  static constexpr int kBlk = 128;
+  static constexpr int kNumBuf = 1;
+  static constexpr int kVcb = 64;
+  __device__ static int k_cb(int ks) { return 2 * ks; }
+};
+
+struct TileDesc {
+  int32_t unit, s, q_row, L;
+  int32_t tok0;    // absolute position of the tile's first token
+  int32_t flags;   // bit0 first tile of unit, bit1 last tile, bit2 end; bits 8..11 page valid
+  int32_t ntiles;  // tiles of this unit
+  int32_t pad;
+};
+constexpr int kFirst = 1, kLast = 2, kEnd = 4;
+
+template <int LAYOUT, int HQ>
+struct GSmem {
+  using T = GTraits<LAYOUT>;
+  static constexpr int kNP = HQ < 16 ? 16 : HQ;  // P.V N (M=128 needs N % 16 == 0)
+  uint8_t tiles[T::kNumBuf][kTilePages * T::kPageBytes];
+  uint8_t q[HQ * 512 * 2];     // K-major Q: [hb][cb 64][8][8] bf16
+  uint8_t p[2][64 * kNP * 2];  // MN-major P^T: [tb 8][hb][8 tokens][8 heads] bf16
+  float stage[64 * 33];        // [token][head] staging for max / l reductions
+  float mvec[32];              // reference max per head (log2 units)
+  TileDesc ring[kRing];
+  uint64_t full[T::kNumBuf], empty[T::kNumBuf];
+  uint64_t s_ready[2], p_ready[2], pfree[2], o_done[2], o_free[2], q_ready;
+  uint32_t tmem_base;
+  int32_t flag;
+};
+
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+
+template <int LAYOUT, int HQ>
+__global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalArgs a) {
+  using T = GTraits<LAYOUT>;
+  using SM = GSmem<LAYOUT, HQ>;
+  constexpr int NB = T::kNumBuf;
+  constexpr int NP = SM::kNP;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  SM& sm = *reinterpret_cast<SM*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int total_units = a.unit_base[a.batch];
+  if (total_units > a.max_units) return;
+  int32_t* st = a.status;
+
+  // Stale tile / P slots must hold finite values: masked tokens get p = 0 and
+  // 0 * finite = 0 in the P.V contraction.
+  {
+    uint4* z = reinterpret_cast<uint4*>(sm.tiles);
+    for (int i = tid; i < static_cast<int>(sizeof(sm.tiles) / 16); i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    uint4* zp = reinterpret_cast<uint4*>(sm.p);
+    for (int i = tid; i < static_cast<int>(sizeof(sm.p) / 16); i += kThreads) zp[i] = make_uint4(0, 0, 0, 0);
+  }
+  if (tid == 0) {
+    for (int b = 0; b < NB; ++b) {
+      mbar_init(&sm.full[b], 1);
+      mbar_init(&sm.empty[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.s_ready[b], 1);
+      mbar_init(&sm.p_ready[b], 128);
+      mbar_init(&sm.pfree[b], 1);
+      mbar_init(&sm.o_done[b], 1);
+      mbar_init(&sm.o_free[b], 128);
+    }
+    mbar_init(&sm.q_ready, 1);
+    sm.flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tc::alloc(&sm.tmem_base, 512);
+    tc::relinquish();
+  }
+  fence_proxy_async_smem();
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  // TMEM columns: S^T buffers at 0 and 32; O^T buffers at 64 and 192 (4 blocks of 32).
+
+  if (warp == 4) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t fill = 0;
+      bool stop = false;
+      while (!stop) {
+        const int u = atomicAdd(a.counter, 1);
+        const bool end = u >= total_units;
+        int s = 0, L = 0, p0 = 0, p1 = 0, ntiles = 1, q_row = 0;
+        if (!end) {
+          int lo = 0, hi = a.batch;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.unit_base[mid] <= u) lo = mid; else hi = mid - 1;
+          }
+          s = lo;
+          L = a.seq_lens[s];
+          const int cpg = global_chunk_pages(L);
+          p0 = (u - a.unit_base[s]) * cpg;
+          p1 = min(p0 + cpg, (L + kPage - 1) / kPage);
+          ntiles = (p1 - p0 + kTilePages - 1) / kTilePages;
+          q_row = a.cu_q_rows[s];
+        }
+        for (int t = 0; t < ntiles; ++t) {
+          const int b = fill % NB;
+          if (fill >= NB && !mbar_wait(&sm.empty[b], ((fill / NB) - 1) & 1, st)) {
+            stop = true;
+            break;
+          }
+          TileDesc d{};
+          int phys[kTilePages];
+          uint32_t bytes = 0;
+          if (end) {
+            d.flags = kEnd;
+          } else {
+            d.unit = u;
+            d.s = s;
+            d.q_row = q_row;
+            d.L = L;
+            d.tok0 = (p0 + t * kTilePages) * kPage;
+            d.ntiles = ntiles;
+            d.flags = (t == 0 ? kFirst : 0) | (t == ntiles - 1 ? kLast : 0);
+            const int32_t* bt = a.block_table + static_cast<int64_t>(s) * a.max_pages;
+#pragma unroll
+            for (int j = 0; j < kTilePages; ++j) {
+              const int lp = p0 + t * kTilePages + j;
+              phys[j] = -1;
+              if (lp < p1) {
+                const int32_t pg = bt[lp];
+                if (pg >= 0 && pg < a.num_pages) {
+                  phys[j] = pg;
+                  d.flags |= 1 << (8 + j);
+                  bytes += T::kPageBytes;
+                } else {
+                  set_status(st, GW_DEV_PAGE_RANGE);
+                }
+              }
+            }
+          }
+          sm.ring[fill % kRing] = d;
+          mbar_arrive_expect_tx(&sm.full[b], bytes);
+          if (!end) {
+#pragma unroll
+            for (int j = 0; j < kTilePages; ++j)
+              if (phys[j] >= 0)
+                bulk_g2s(sm.tiles[b] + j * T::kPageBytes, a.pool + static_cast<int64_t>(phys[j]) * T::kPageBytes,
+                         T::kPageBytes, &sm.full[b], pol);
+          }
+          ++fill;
+        }
+        if (end) stop = true;
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      const uint32_t id_qk = tc::idesc_bf16(64, HQ, false, false);
+      const uint32_t id_pv = tc::idesc_bf16(128, NP, true, true);
+      const uint32_t q_addr = smem_u32(sm.q);
+      uint32_t gi = 0;
+      int uidx = -1, prev_u = -1;
+      TileDesc prev{};
+      bool has_prev = false, ok = true;
+
+      auto pv = [&](const TileDesc& d, uint32_t i, int ui) -> bool {
+        if (!mbar_wait(&sm.p_ready[i & 1], (i >> 1) & 1, st)) return false;
+        const int ob = ui & 1;
+        if ((d.flags & kFirst) && ui >= 2 && !mbar_wait(&sm.o_free[ob], ((ui >> 1) - 1) & 1, st)) return false;
+        tc::fence_after();
+        const uint32_t tile = smem_u32(sm.tiles[i % NB]);
+        const uint32_t pb = smem_u32(sm.p[i & 1]);
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+          for (int j = 0; j < kTilePages; ++j) {
+            const uint64_t ad = tc::smem_desc(tile + j * T::kPageBytes + (T::kVcb + 16 * blk) * 128,
+                                              T::kBlk * 128, 128);
+            const uint64_t bd = tc::smem_desc(pb + 2 * j * (NP / 8) * 128, (NP / 8) * 128, 128);
+            tc::mma_bf16(tmem + 64 + 128 * ob + 32 * blk, ad, bd, id_pv, !((d.flags & kFirst) && j == 0));
+          }
+        }
+        tc::commit(&sm.empty[i % NB]);
+        tc::commit(&sm.pfree[i & 1]);
+        if (d.flags & kLast) tc::commit(&sm.o_done[ob]);
+        return true;
+      };
+
+      while (true) {
+        const int b = gi % NB;
+        if (!mbar_wait(&sm.full[b], (gi / NB) & 1, st)) { ok = false; break; }
+        const TileDesc d = sm.ring[gi % kRing];
+        if (d.flags & kEnd) break;
+        if (d.flags & kFirst) {
+          ++uidx;
+          if (!mbar_wait(&sm.q_ready, uidx & 1, st)) { ok = false; break; }
+        }
+        tc::fence_after();
+        const uint32_t tile = smem_u32(sm.tiles[b]);
+        const uint32_t d_s = tmem + 32 * (gi & 1);
+#pragma unroll 8
+        for (int ks = 0; ks < 32; ++ks) {
+          const uint64_t ad = tc::smem_desc(tile + T::k_cb(ks) * 128, 128, T::kBlk * 128);
+          const uint64_t bd = tc::smem_desc(q_addr + 2 * ks * 128, 128, 64 * 128);
+          tc::mma_bf16(d_s, ad, bd, id_qk, ks > 0);
+        }
+        tc::commit(&sm.s_ready[gi & 1]);
+        if (has_prev && !pv(prev, gi - 1, prev_u)) { ok = false; break; }
+        prev = d;
+        prev_u = uidx;
+        has_prev = true;
+        ++gi;
+      }
+      if (ok && has_prev) pv(prev, gi - 1, prev_u);
+    }
+  } else if (warp == 6) {
+    // -------------------------------------------------------------- q loader
+    uint32_t first = 0;
+    int last_prev = -1;
+    while (true) {
+      if (!mbar_wait(&sm.full[first % NB], (first / NB) & 1, st)) break;
+      const TileDesc d = sm.ring[first % kRing];
+      if (d.flags & kEnd) break;
+      if (last_prev >= 0 && !mbar_wait(&sm.s_ready[last_prev & 1], (last_prev >> 1) & 1, st)) break;
+      const uint16_t* src = a.q + static_cast<int64_t>(d.q_row) * HQ * 512;
+      for (int c = lane; c < HQ * 64; c += 32) {
+        const int h = c >> 6, cb = c & 63;
+        cp_async16(sm.q + (((h >> 3) * 64 + cb) * 128 + (h & 7) * 16), src + h * 512 + cb * 8);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.q_ready);
+      last_prev = static_cast<int>(first + d.ntiles - 1);
+      first += d.ntiles;
+    }
+  } else {
+    // ------------------------------------------------- softmax + epilogue
+    const bool active = lane < 16;
+    const int t = 16 * warp + lane;  // token of the tile (active lanes)
+    const int j = warp;              // page of the tile
+    float m_run[HQ], l_acc[HQ];
+#pragma unroll
+    for (int h = 0; h < HQ; ++h) {
+      m_run[h] = -INFINITY;
+      l_acc[h] = 0.f;
+    }
+    uint32_t gi = 0;
+    int uidx = -1;
+    while (true) {
+      const int b = gi % NB;
+      if (!mbar_wait(&sm.full[b], (gi / NB) & 1, st)) break;
+      const TileDesc d = sm.ring[gi % kRing];
+      if (d.flags & kEnd) break;
+      const bool first = d.flags & kFirst;
+      if (first) ++uidx;
+      if (!mbar_wait(&sm.s_ready[gi & 1], (gi >> 1) & 1, st)) break;
+      tc::fence_after();
+      uint32_t r[32];
+      tc::ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * (gi & 1), r);
+      tc::wait_ld();
+      const int tabs = d.tok0 + t;
+      const bool pvalid = (d.flags >> (8 + j)) & 1;
+      const bool valid = active && pvalid && tabs < d.L;
+      float s[HQ];
+      bool need = false;
+#pragma unroll
+      for (int h = 0; h < HQ; ++h) {
+        s[h] = valid ? __uint_as_float(r[h]) * a.scale_log2 : -INFINITY;
+        need |= s[h] > m_run[h] + kLazyThreshold;
+      }
+      if (need) sm.flag = 1;
+      softmax_bar();
+      if (first || sm.flag) {
+        // ---- slow path: tile max per head, maybe rescale
+        if (active) {
+#pragma unroll
+          for (int h = 0; h < HQ; ++h) sm.stage[t * 33 + h] = s[h];
+        }
+        softmax_bar();
+        {
+          const int hh = tid >> 2, qq = tid & 3;
+          float mx = -INFINITY;
+          if (hh < HQ) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mx = fmaxf(mx, sm.stage[(16 * qq + i) * 33 + hh]);
+          }
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          if (hh < HQ && qq == 0) {
+            const float mo = first ? -INFINITY : sm.mvec[hh];
+            sm.mvec[hh] = (first || mx > mo + kLazyThreshold) ? fmaxf(mo, mx) : mo;
+          }
+        }
+        softmax_bar();
+        if (tid == 0) sm.flag = 0;
+        float alpha[HQ];
+        bool rescale = false;
+#pragma unroll
+        for (int h = 0; h < HQ; ++h) {
+          const float mn = sm.mvec[h];
+          alpha[h] = (first || m_run[h] == -INFINITY) ? 0.f : ex2(m_run[h] - mn);
+          rescale |= !first && mn != m_run[h];
+          m_run[h] = mn;
+          l_acc[h] = first ? 0.f : l_acc[h] * alpha[h];
+        }
+        if (rescale) {
+          // O^T *= alpha per head column, once P.V of the previous tile is done
+          if (!mbar_wait(&sm.pfree[(gi - 1) & 1], ((gi - 1) >> 1) & 1, st)) break;
+          tc::fence_after();
+          const uint32_t ob = uidx & 1;
+#pragma unroll 1
+          for (int blk = 0; blk < 4; ++blk) {
+            const uint32_t ad = tmem + (static_cast<uint32_t>(32 * warp) << 16) + 64 + 128 * ob + 32 * blk;
+            uint32_t o[32];
+            tc::ld32(ad, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int h = 0; h < HQ; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+            tc::st32(ad, o);
+          }
+          tc::wait_st();
+        }
+      }
+      // ---- P^T (bf16) for this tile; wait until P.V two tiles back released the buffer
+      if (gi >= 2 && !mbar_wait(&sm.pfree[gi & 1], ((gi >> 1) - 1) & 1, st)) break;
+      if (active) {
+        uint8_t* pdst = sm.p[gi & 1] + ((t >> 3) * (NP / 8)) * 128 + (t & 7) * 16;
+#pragma unroll
+        for (int hb = 0; hb < HQ / 8; ++hb) {
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int h0 = hb * 8 + 2 * k;
+            const float p0 = valid ? ex2(s[h0] - m_run[h0]) : 0.f;
+            const float p1 = valid ? ex2(s[h0 + 1] - m_run[h0 + 1]) : 0.f;
+            __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            l_acc[h0] += __low2float(pb);
+            l_acc[h0 + 1] += __high2float(pb);
+            w[k] = *reinterpret_cast<uint32_t*>(&pb);
+          }
+          *reinterpret_cast<uint4*>(pdst + hb * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (pvalid && tabs >= d.L) {
+          // token past the end of the sequence in a valid page: clear its row
+          // so whatever the pool holds there cannot reach P.V
+          uint8_t* row = sm.tiles[b] + j * T::kPageBytes + (lane >> 3) * T::kBlk * 128 + (lane & 7) * 16;
+          for (int cb = 0; cb < T::kBlk; ++cb) *reinterpret_cast<uint4*>(row + cb * 128) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      tc::fence_before();
+      mbar_arrive(&sm.p_ready[gi & 1]);
+
+      if (d.flags & kLast) {
+        // ---- epilogue: unnormalised partial (m, l, o) of this unit
+        const uint32_t ob = uidx & 1;
+        if (!mbar_wait(&sm.o_done[ob], (uidx >> 1) & 1, st)) break;
+        tc::fence_after();
+        float* po = a.part_o + static_cast<int64_t>(d.unit) * HQ * 512;
+#pragma unroll 1
+        for (int blk = 0; blk < 4; ++blk) {
+          uint32_t o[32];
+          tc::ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 64 + 128 * ob + 32 * blk, o);
+          tc::wait_ld();
+          const int dim = 128 * blk + 32 * warp + lane;
+#pragma unroll
+          for (int h = 0; h < HQ; ++h) po[h * 512 + dim] = __uint_as_float(o[h]);
+        }
+        if (active) {
+#pragma unroll
+          for (int h = 0; h < HQ; ++h) sm.stage[t * 33 + h] = l_acc[h];
+        }
+        softmax_bar();
+        if (tid < HQ) {
+          float l = 0.f;
+          for (int k = 0; k < 64; ++k) l += sm.stage[k * 33 + tid];
+          a.part_ml[static_cast<int64_t>(d.unit) * HQ + tid] = make_float2(sm.mvec[tid], l);
+        }
+        softmax_bar();
+        tc::fence_before();
+        mbar_arrive(&sm.o_free[ob]);
+      }
+      ++gi;
+    }
+  }
+
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc::fence_after();
+    tc::dealloc(tmem, 512);
+  }
+}
+
+template <int LAYOUT, int HQ>
+cudaError_t launch_layout(const LocalArgs& a, cudaStream_t stream) {
+  cudaError_t e = launch_plan(a, kSplitGlobal, 0, stream);
+  if (e != cudaSuccess) return e;
+  auto kern = global_decode_kernel<LAYOUT, HQ>;
+  const size_t smem = sizeof(GSmem<LAYOUT, HQ>);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms(), kThreads, smem, stream>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_combine(a, kSplitGlobal, HQ, 512, 0, stream);
+}
+
+template <int LAYOUT>
+cudaError_t launch_hq(const LocalArgs& a, cudaStream_t stream) {
+  switch (a.num_q_heads) {
+    case 8: return launch_layout<LAYOUT, 8>(a, stream);
+    case 16: return launch_layout<LAYOUT, 16>(a, stream);
+    case 32: return launch_layout<LAYOUT, 32>(a, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_global_decode(int layout, const LocalArgs& a, cudaStream_t stream) {
+  return layout == GW_LAYOUT_GLOBAL_FOLDED ? launch_hq<GW_LAYOUT_GLOBAL_FOLDED>(a, stream)
+                                           : launch_hq<GW_LAYOUT_GLOBAL_FULL>(a, stream);
+}
+
+}  // namespace gw

@@ -54,69 +54,6 @@ struct Traits {
   static constexpr int kChunk = DT == GW_KV_BF16 ? kLocalChunkPagesBf16 : kLocalChunkPagesE4m3;
 };
 
-__host__ __device__ __forceinline__ int local_chunks(int L, int window, int chunk) {
-  const int first = L > window ? L - window : 0;
-  const int p0 = first / kPage, p1 = (L - 1) / kPage;
-  return (p1 - p0 + chunk) / chunk;
-}
-
-__device__ __forceinline__ bool len_ok(const LocalArgs& a, int L, int n) {
-  return L >= 1 && L >= n && static_cast<int64_t>(L) <= static_cast<int64_t>(a.max_pages) * kPage;
-}
-
-// One CTA: unit_base[s] = units of sequences before s (decode rows only),
-// counter = 0.
-__global__ void plan_local_kernel(const LocalArgs a, int chunk) {
-  __shared__ int32_t warp_sums[32];
-  __shared__ int32_t carry;
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
-  for (int base = 0; base < a.batch; base += blockDim.x) {
-    const int s = base + threadIdx.x;
-    int units = 0;
-    if (s < a.batch) {
-      const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
-      const int L = a.seq_lens[s];
-      if (n == 1) {
-        if (len_ok(a, L, n))
-          units = a.kv_heads * local_chunks(L, a.window, chunk);
-        else
-          set_status(a.status, GW_DEV_LEN_RANGE);
-      }
-    }
-    // block exclusive scan
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int x = units;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(~0u, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sums[w] = x;
-    __syncthreads();
-    if (w == 0) {
-      int v = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(~0u, v, o);
-        if (lane >= o) v += y;
-      }
-      warp_sums[lane] = v;
-    }
-    __syncthreads();
-    const int excl = carry + (w > 0 ? warp_sums[w - 1] : 0) + x - units;
-    if (s < a.batch) a.unit_base[s] = excl;
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) carry = excl + units;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    a.unit_base[a.batch] = carry;
-    *a.counter = 0;
-    if (carry > a.max_units) set_status(a.status, GW_DEV_WORKSPACE);
-  }
-}
-
 template <class T>
 __device__ __forceinline__ Unit decode_unit(const LocalArgs& a, int u) {
   int lo = 0, hi = a.batch;
@@ -341,61 +278,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
   }
 }
 
-// One warp per (sequence, q head): merge the sequence's partials for that head.
-template <int G, int kChunk>
-__global__ void local_combine_kernel(const LocalArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int64_t w = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
-  if (w >= static_cast<int64_t>(a.batch) * a.num_q_heads) return;
-  const int s = static_cast<int>(w / a.num_q_heads), h = static_cast<int>(w % a.num_q_heads);
-  const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
-  if (n != 1) return;
-  const int L = a.seq_lens[s];
-  uint16_t* dst = a.out + (static_cast<int64_t>(a.cu_q_rows[s]) * a.num_q_heads + h) * 256 + lane * 8;
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  float den = 0.f;
-  if (len_ok(a, L, 1) && a.unit_base[a.batch] <= a.max_units) {
-    const int nc = local_chunks(L, a.window, kChunk);
-    const int g = h / G, hh = h % G;
-    const int64_t ub = a.unit_base[s] + static_cast<int64_t>(g) * nc;
-    float M = -INFINITY;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, a.part_ml[(ub + c) * G + hh].x);
-    if (M != -INFINITY) {
-      for (int c = 0; c < nc; ++c) {
-        const float2 ml = a.part_ml[(ub + c) * G + hh];
-        const float wgt = ex2(ml.x - M);
-        den += wgt * ml.y;
-        const float* po = a.part_o + ((ub + c) * G + hh) * 256 + lane * 8;
-        const float4 u0 = *reinterpret_cast<const float4*>(po);
-        const float4 u1 = *reinterpret_cast<const float4*>(po + 4);
-        acc[0] += wgt * u0.x; acc[1] += wgt * u0.y; acc[2] += wgt * u0.z; acc[3] += wgt * u0.w;
-        acc[4] += wgt * u1.x; acc[5] += wgt * u1.y; acc[6] += wgt * u1.z; acc[7] += wgt * u1.w;
-      }
-    }
-  }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  uint32_t wv[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-    wv[i] = *reinterpret_cast<uint32_t*>(&b);
-  }
-  *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-}
-
 template <int DT, int G>
 cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   using T = Traits<DT>;
-  plan_local_kernel<<<1, 1024, 0, st>>>(a, T::kChunk);
+  cudaError_t e = launch_plan(a, kSplitLocal, T::kChunk, st);
+  if (e != cudaSuccess) return e;
   const size_t smem = sizeof(WarpSmem) * kWarps;
   auto kern = local_decode_kernel<DT, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   kern<<<num_sms(), kWarps * 32, smem, st>>>(a);
-  const int64_t warps = static_cast<int64_t>(a.batch) * a.num_q_heads;
-  const int blocks = static_cast<int>((warps + 7) / 8);
-  local_combine_kernel<G, T::kChunk><<<blocks, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_combine(a, kSplitLocal, G, 256, T::kChunk, st);
 }
 
 template <int DT>

@@ -92,8 +92,9 @@ WsLayout ws_layout(int layout, int dtype, int kv_heads, int num_q_heads, int bat
     units = static_cast<int64_t>(batch) * kv_heads * ceil_div(pages, chunk);
     w.heads_per_unit = num_q_heads / kv_heads;
   } else {
-    const int64_t pages = ceil_div(max_seq_len, 16);
-    units = static_cast<int64_t>(batch) * ceil_div(pages, kGlobalChunkPages);
+    // global_chunks(L) <= min(kGlobalMaxChunks, ceil(pages(L) / 16)) for every L
+    const int64_t c16 = ceil_div(ceil_div(max_seq_len, 16), kGlobalChunkPagesMin);
+    units = static_cast<int64_t>(batch) * (c16 < kGlobalMaxChunks ? c16 : kGlobalMaxChunks);
     w.heads_per_unit = num_q_heads;
   }
   const int D = layout == GW_LAYOUT_LOCAL ? 256 : 512;

@@ -12,11 +12,36 @@ namespace gw {
 // ---- split-KV plan constants ------------------------------------------------
 // A local decode work unit is (sequence, KV head, chunk of kLocalChunkPages
 // logical pages of that sequence's window); a global unit is (sequence, chunk
-// of kGlobalChunkPages pages).  Chunks depend only on the sequence's own
+// of global_chunk_pages(L) pages).  Chunks depend only on the sequence's own
 // length, so a row's arithmetic never depends on the rest of the batch.
 constexpr int kLocalChunkPagesBf16 = 4;
 constexpr int kLocalChunkPagesE4m3 = 8;
-constexpr int kGlobalChunkPages = 16;
+// Global chunks start at 16 pages and double until a sequence has at most
+// kGlobalMaxChunks of them (long contexts get long chunks, so the partials
+// stay a small fraction of the KV bytes).
+constexpr int kGlobalChunkPagesMin = 16;
+constexpr int kGlobalMaxChunks = 128;
+
+constexpr int kSplitLocal = 0;
+constexpr int kSplitGlobal = 1;
+
+__host__ __device__ __forceinline__ int local_chunks(int L, int window, int chunk) {
+  const int first = L > window ? L - window : 0;
+  const int p0 = first / 16, p1 = (L - 1) / 16;
+  return (p1 - p0 + chunk) / chunk;
+}
+
+__host__ __device__ __forceinline__ int global_chunk_pages(int L) {
+  const int pages = (L + 15) / 16;
+  int cpg = kGlobalChunkPagesMin;
+  while ((pages + cpg - 1) / cpg > kGlobalMaxChunks) cpg *= 2;
+  return cpg;
+}
+
+__host__ __device__ __forceinline__ int global_chunks(int L) {
+  const int cpg = global_chunk_pages(L);
+  return ((L + 15) / 16 + cpg - 1) / cpg;
+}
 
 // Workspace layout (offsets from the 256-byte aligned workspace base):
 //   [0, 256)          int32 work counter (+ padding)
@@ -69,6 +94,14 @@ struct AppendArgs {
 };
 
 int num_sms();
+
+// Split-KV plan: unit_base[s] = units of the decode-row sequences before s;
+// zeroes the work counter.  mode: kSplitLocal (units = kv_heads * chunks of
+// `chunk` pages of the window) or kSplitGlobal (units = global_chunks(L)).
+cudaError_t launch_plan(const LocalArgs& a, int mode, int chunk, cudaStream_t st);
+// Log-sum-exp merge of each decode row's partials into bf16 `out`.
+cudaError_t launch_combine(const LocalArgs& a, int mode, int heads_per_unit, int head_dim, int chunk,
+                           cudaStream_t st);
 
 cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_local_decode(int dtype, int group, const LocalArgs& a, cudaStream_t st);
