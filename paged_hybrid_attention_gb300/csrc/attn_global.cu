@@ -81,7 +81,7 @@ struct GSmem {
   float mvec[32];              // reference max per head (log2 units)
   TileDesc ring[kRing];
   uint64_t full[T::kNumBuf], empty[T::kNumBuf];
-  uint64_t s_ready[2], p_ready[2], pfree[2], o_done[2], o_free[2], q_ready;
+  uint64_t s_ready[2], p_ready[2], pfree[2], o_done[2], o_free[2], q_ready, q_free;
   uint32_t tmem_base;
   int32_t flag;
 };
@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       mbar_init(&sm.o_free[b], 128);
     }
     mbar_init(&sm.q_ready, 1);
+    mbar_init(&sm.q_free, 1);
     sm.flag = 0;
     fence_mbar_init();
   }
@@ -267,23 +268,33 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
           tc::mma_bf16(d_s, ad, bd, id_qk, ks > 0);
         }
         tc::commit(&sm.s_ready[gi & 1]);
-        if (has_prev && !pv(prev, gi - 1, prev_u)) { ok = false; break; }
-        prev = d;
-        prev_u = uidx;
-        has_prev = true;
+        if (d.flags & kLast) tc::commit(&sm.q_free);  // Q may be replaced once this completes
+        if constexpr (NB == 1) {
+          // one tile buffer: the next tile cannot load before this P.V is done
+          if (!pv(d, gi, uidx)) { ok = false; break; }
+        } else {
+          // two buffers: QK^T of this tile overlaps the softmax of the previous one
+          if (has_prev && !pv(prev, gi - 1, prev_u)) { ok = false; break; }
+          prev = d;
+          prev_u = uidx;
+          has_prev = true;
+        }
         ++gi;
       }
-      if (ok && has_prev) pv(prev, gi - 1, prev_u);
+      if (NB > 1 && ok && has_prev) pv(prev, gi - 1, prev_u);
     }
   } else if (warp == 6) {
     // -------------------------------------------------------------- q loader
+    // Ordering: wait until the last QK^T of the previous unit has completed
+    // (q_free), which also guarantees that every earlier tile has landed, so
+    // the `full` wait below is never more than one phase behind.
     uint32_t first = 0;
-    int last_prev = -1;
+    int u = 0;
     while (true) {
+      if (u > 0 && !mbar_wait(&sm.q_free, (u - 1) & 1, st)) break;
       if (!mbar_wait(&sm.full[first % NB], (first / NB) & 1, st)) break;
       const TileDesc d = sm.ring[first % kRing];
       if (d.flags & kEnd) break;
-      if (last_prev >= 0 && !mbar_wait(&sm.s_ready[last_prev & 1], (last_prev >> 1) & 1, st)) break;
       const uint16_t* src = a.q + static_cast<int64_t>(d.q_row) * HQ * 512;
       for (int c = lane; c < HQ * 64; c += 32) {
         const int h = c >> 6, cb = c & 63;
@@ -294,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.q_ready);
-      last_prev = static_cast<int>(first + d.ntiles - 1);
       first += d.ntiles;
+      ++u;
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
