@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Decode-attention benchmark for the gw library on one GB300 (or N, weak scaling).
+
+A step is one pass of the whole hot path over one batch: for every layer of a
+5 local + 1 global group, append the step's K/V rows (gw_kv_append) and run
+decode attention (gw_decode_attn_local / gw_decode_attn_global).  Each layer
+has its own pools, so a step reads ~1.4 GB of KV (inputs larger than L2).
+
+Default workload: 16 decode slots, lengths U[512, 8192], 32 q heads; local 16
+KV heads hd256, window 1024, bf16; global one KV head hd512, folded V + k_rot.
+
+Printed: ONE JSON line (rank 0) with value = algorithmic KV GB/s of the whole
+step (KV bytes the method must read / device time), steps/s, a roofline
+object for the dominant call (the local attention call), an e2e number through
+the C ABI with host buffers, the oracle timed on host cores (cpu_baseline),
+clock samples and kernel launch counts.
+
+--impl reference times the float64 CPU oracle (the reference arm) on a
+bounded sample of the same workload.
+"""
+
+import os
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_hybrid_attention_gb300 import synth  # noqa: E402
+
+METRIC = "decode-attn KV GB/s (frac of HBM peak) & batched decode steps/s, 1×GB300"
+UNIT = "GB/s"
+
+# ncu DRAM traffic (read + write bytes) per launch of the dominant kernel, with
+# the SHA-256 of the kernel source it was taken from; reported as null once the
+# source no longer matches.  (bytes, sha256 of csrc/attn_local.cu)
+NCU_TRAFFIC = {"local_decode": None}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="serving",
+                    help="serving (default), fp8_local, long_global, long_global_full, mixed")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- setup
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured", float(d.get("sm_max_mhz", 2070.0))
+    return 6800.0, "fallback", 2070.0
+
+
+def workload_layers(name, rank):
+    """[(Layer, family key)] of one step; each layer has its own page tables."""
+    base = {"long_global_full": "long_global"}.get(name, name)
+    sp = synth.spec(base)
+    if rank:
+        sp = synth.custom(sp.name, sp.seed + 7919 * rank, sp.num_q_heads, sp.lens, sp.n_rows, sp.families,
+                          sp.n_local_layers, sp.n_global_layers)
+    layers = []
+    lkey = "local"
+    gkey = "global_full" if name == "long_global_full" else "global"
+    for i in range(sp.n_local_layers):
+        layers.append(synth.Layer(sp, lkey, layer=i))
+    for i in range(sp.n_global_layers):
+        layers.append(synth.Layer(sp, gkey, layer=100 + i))
+    return sp, layers
+
+
+def kv_bytes(layer):
+    """Algorithmic KV bytes one attention call must read (keys in range x bytes per token)."""
+    fam, sp = layer.fam, layer.spec
+    tot = 0
+    for L, n in zip(sp.lens.astype(np.int64), sp.n_rows.astype(np.int64)):
+        if n == 0:
+            continue
+        if fam.kind == "local":
+            toks = min(int(L), int(n) - 1 + fam.window)
+            per = fam.kv_heads * 2 * 256 * (2 if fam.dtype == "bf16" else 1)
+        else:
+            toks = int(L)
+            per = 1280 if fam.layout == "folded" else 2048
+        tot += toks * per
+    return tot
+
+
+class GpuLayer:
+    def __init__(self, layer, gw, gen, dev):
+        fam, sp = layer.fam, layer.spec
+        self.layer, self.fam = layer, fam
+        self.pool = gw.KVPool(fam.layout, fam.dtype, layer.num_pages, fam.kv_heads, device=dev)
+        max_pos = int(np.max(sp.lens)) + 1
+        self.table = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, max_pos).to(dev)
+        sig = fam.sigma
+        # history: every token the step reads that was cached before it
+        _, slot, pos = layer.index("history")
+        self._append_random(gw, gen, dev, slot, pos, sig)
+        # the step's own inputs
+        _, slot, pos = layer.index("new")
+        n = len(slot)
+        shape = (n, fam.kv_heads, 256) if fam.kind == "local" else (n, 512)
+        self.v_new = (torch.randn(*shape, generator=gen, device=dev) * sig).to(torch.bfloat16)
+        self.k_new = (torch.randn(*shape, generator=gen, device=dev) * sig).to(torch.bfloat16) \
+            if fam.kind == "local" else self.v_new.clone()
+        self.slot_new = torch.from_numpy(slot).to(dev)
+        self.pos_new = torch.from_numpy(pos).to(dev)
+        rows = int(sp.n_rows.sum())
+        self.q = torch.randn(rows, sp.num_q_heads, fam.head_dim, generator=gen, device=dev).to(torch.bfloat16)
+        self.out = torch.empty_like(self.q)
+        self.cu = torch.from_numpy(layer.cu_rows()).to(dev)
+        self.lens = torch.from_numpy(sp.lens.astype(np.int32)).to(dev)
+        self.bt = torch.from_numpy(layer.block_table).to(dev)
+        self.max_q_rows = int(max(1, sp.n_rows.max()))
+        self.ws = gw.alloc_workspace(self.pool, sp.num_q_heads, len(sp.lens), self.bt.shape[1], self.max_q_rows,
+                                     max(1, fam.window), device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.kv_bytes = kv_bytes(layer)
+        # pinned host copies for the end-to-end leg
+        self.host_in = {k: getattr(self, k).cpu().pin_memory() for k in
+                        ("q", "k_new", "v_new", "slot_new", "pos_new", "cu", "lens", "bt")}
+        self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+
+    def _append_random(self, gw, gen, dev, slot, pos, sig, chunk=1 << 18):
+        fam = self.fam
+        for a in range(0, len(slot), chunk):
+            s_ = torch.from_numpy(slot[a:a + chunk]).to(dev)
+            p_ = torch.from_numpy(pos[a:a + chunk]).to(dev)
+            n = len(s_)
+            shape = (n, fam.kv_heads, 256) if fam.kind == "local" else (n, 512)
+            v = (torch.randn(*shape, generator=gen, device=dev) * sig).to(torch.bfloat16)
+            k = (torch.randn(*shape, generator=gen, device=dev) * sig).to(torch.bfloat16) \
+                if fam.kind == "local" else v
+            gw.kv_append(self.pool, k, v, s_, p_, self.table, self.status)
+
+    def in_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host_in.values())
+
+    def run(self, gw, stream, ev=None):
+        gw.kv_append(self.pool, self.k_new, self.v_new, self.slot_new, self.pos_new, self.table, self.status, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        if self.fam.kind == "local":
+            gw.decode_attn_local(self.pool, self.q, self.out, self.cu, self.lens, self.bt, self.ws, self.fam.window,
+                                 max_q_rows=self.max_q_rows, dev_status=self.status, stream=stream)
+        else:
+            gw.decode_attn_global(self.pool, self.q, self.out, self.cu, self.lens, self.bt, self.ws,
+                                  max_q_rows=self.max_q_rows, dev_status=self.status, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def upload(self, stream):
+        for k, h in self.host_in.items():
+            getattr(self, k).copy_(h, non_blocking=True)
+
+    def download(self):
+        self.host_out.copy_(self.out, non_blocking=True)
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxes.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "samples": len(sms),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- oracle legs
+def oracle_sample(name, budget_s):
+    """Time the float64 oracle (append + attention) on whole sequences until
+    about budget_s seconds of work; returns (GB/s, description, seconds)."""
+    from oracle import attention, pages, rope  # test infrastructure: CPU baseline leg only
+    from oracle.formats import bf16_bits_to_f64
+    sp, layers = workload_layers(name, 0)
+    done_bytes, t_used, seqs = 0, 0.0, []
+    order = [(li, s) for s in range(len(sp.lens)) for li in range(len(layers))]
+    rng = np.random.Generator(np.random.PCG64(17))
+    rng.shuffle(order)
+    tables, pools = {}, {}
+    for li, s in order:
+        layer = layers[li]
+        fam = layer.fam
+        if sp.n_rows[s] == 0:
+            continue
+        key = (fam.theta, fam.rot_dim, fam.head_dim)
+        if key not in tables:
+            tables[key] = rope.rope_table(fam.theta, fam.rot_dim, fam.head_dim, int(sp.lens.max()) + 1)
+        table = tables[key]
+        k, v, slot, pos = layer.gather([s])
+        q = bf16_bits_to_f64(layer.q(s))
+        L = int(sp.lens[s])
+        if li not in pools:
+            pb = pages.local_page_bytes(fam.kv_heads, fam.dtype) if fam.layout == "local" else (
+                pages.folded_page_bytes() if fam.layout == "folded" else pages.full_page_bytes())
+            pools[li] = pages.new_pool(layer.num_pages, pb)
+        pool = pools[li]
+        t0 = time.perf_counter()
+        if fam.layout == "local":
+            pages.write_local(pool, fam.kv_heads, fam.dtype, k, v, slot, pos, table)
+            attention.local_rows(pool, fam.kv_heads, fam.dtype, layer.block_table[s], L, q, fam.window,
+                                 1.0 / math.sqrt(256))
+        else:
+            pages.write_global(pool, fam.layout, k, v, slot, pos, table)
+            attention.global_rows(pool, fam.layout, layer.block_table[s], L, q, 1.0 / math.sqrt(512))
+        t_used += time.perf_counter() - t0
+        one = synth.custom("one", 0, sp.num_q_heads, sp.lens[s:s + 1], sp.n_rows[s:s + 1], sp.families)
+        done_bytes += kv_bytes(synth.Layer(one, layer.fam_key, layer=layer.layer))
+        seqs.append((li, s))
+        if t_used >= budget_s:
+            break
+    desc = "%d (layer, sequence) pairs of the %s step (append + attention per pair), float64 NumPy, 1 thread" % (
+        len(seqs), name)
+    return done_bytes / t_used / 1e9, desc, t_used
+
+
+# --------------------------------------------------------------------------- main
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    peak, peak_kind, _ = peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        ref_steps = []
+        desc = ""
+        for _ in range(args.warmup + args.steps):
+            gbs, desc, secs = oracle_sample(args.workload, budget_s=max(1.0, 60.0 / max(1, args.steps + args.warmup)))
+            ref_steps.append(gbs)
+        val = statistics.median(ref_steps[args.warmup:]) if args.steps else ref_steps[-1]
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload, "l2": "n/a (CPU)"},
+                "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    from paged_hybrid_attention_gb300 import gw
+
+    sp, layers = workload_layers(args.workload, rank)
+    gen = torch.Generator(device=dev).manual_seed(sp.seed + 17 * rank)
+    glayers = [GpuLayer(l, gw, gen, dev) for l in layers]
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    step_bytes = sum(g.kv_bytes for g in glayers)
+    locals_ = [g for g in glayers if g.fam.kind == "local"]
+    dom = locals_ if locals_ else glayers
+    dom_name = "local decode attention call (plan + split-KV decode + combine)" if locals_ else \
+        "global decode attention call (plan + tcgen05 decode + combine)"
+    dom_bytes = statistics.mean(g.kv_bytes for g in dom)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        for g in glayers:
+            g.run(gw, stream)
+    torch.cuda.synchronize()
+    for g in glayers:
+        g.status.zero_()
+
+    # ---- device-timed region
+    K = args.steps
+    evs = {id(g): [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+           for g in dom}
+    clocks = ClockSampler(dev.index)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(K):
+        for g in glayers:
+            g.run(gw, stream, evs[id(g)][k] if id(g) in evs else None)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    ms = t0.elapsed_time(t1) / K
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    dom_ms = statistics.mean(e0.elapsed_time(e1) for g in dom for e0, e1 in evs[id(g)])
+    status = int(sum(int(g.status.item()) for g in glayers))
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h2d = sum(g.in_bytes() for g in glayers)
+        d2h = sum(g.host_out.numel() * g.host_out.element_size() for g in glayers)
+        for _ in range(2):
+            for g in glayers:
+                g.upload(stream)
+                g.run(gw, stream)
+                g.download()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            for g in glayers:
+                g.upload(stream)
+                g.run(gw, stream)
+                g.download()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / K
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        return
+    value = world * step_bytes / (ms * 1e-3) / 1e9
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    src = os.path.join(ROOT, "paged_hybrid_attention_gb300", "csrc", "attn_local.cu")
+    traffic = None
+    if NCU_TRAFFIC.get("local_decode"):
+        tb, sha = NCU_TRAFFIC["local_decode"]
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() == sha:
+                traffic = tb
+    cpu = None
+    if not args.no_cpu:
+        gbs, desc, _ = oracle_sample(args.workload, budget_s=12.0)
+        cpu = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+    launches_per_step = sum(1 + 3 + (1 if g.max_q_rows > 1 else 0) for g in glayers)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "steps_per_s": 1000.0 / ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": "%d local + %d global" % (sp.n_local_layers,
+                                                                                   sp.n_global_layers),
+                   "batch": int(len(sp.lens)), "kv_bytes_per_step": step_bytes, "q_heads": sp.num_q_heads,
+                   "l2": "inputs larger than L2: %.2f GB of KV read per step" % (step_bytes / 1e9),
+                   "parallelism": "dp%d (sequences sharded, no collective)" % world},
+        "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dom_bytes, "ms_per_launch": dom_ms},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "device_status": status,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

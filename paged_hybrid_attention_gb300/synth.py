@@ -207,6 +207,19 @@ class Layer:
         return (np.concatenate(ks), np.concatenate(vs),
                 np.concatenate(ss).astype(np.int32), np.concatenate(ps).astype(np.int32))
 
+    def index(self, part="all"):
+        """(seq, slot, pos) int arrays of the tokens gather() would return, without values."""
+        ss, sl, ps = [], [], []
+        for s in range(self.B):
+            L, n = int(self.spec.lens[s]), int(self.spec.n_rows[s])
+            lo = int(self.first_pos[s]) if part != "new" else L - n
+            hi = L - n if part == "history" else L
+            pos = np.arange(lo, hi, dtype=np.int64)
+            ss.append(np.full(len(pos), s, np.int32))
+            ps.append(pos)
+            sl.append(self.slots(s, pos) if len(pos) else np.zeros(0, np.int32))
+        return (np.concatenate(ss), np.concatenate(sl).astype(np.int32), np.concatenate(ps).astype(np.int32))
+
     def queries(self, seqs=None):
         seqs = range(self.B) if seqs is None else seqs
         return np.concatenate([self.q(s) for s in seqs])
