@@ -115,6 +115,7 @@ class GpuLayer:
         max_pos = int(np.max(sp.lens)) + 1
         self.table = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, max_pos).to(dev)
         sig = fam.sigma
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         # history: every token the step reads that was cached before it
         _, slot, pos = layer.index("history")
         self._append_random(gw, gen, dev, slot, pos, sig)
@@ -136,7 +137,6 @@ class GpuLayer:
         self.max_q_rows = int(max(1, sp.n_rows.max()))
         self.ws = gw.alloc_workspace(self.pool, sp.num_q_heads, len(sp.lens), self.bt.shape[1], self.max_q_rows,
                                      max(1, fam.window), device=dev)
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.kv_bytes = kv_bytes(layer)
         # pinned host copies for the end-to-end leg
         self.host_in = {k: getattr(self, k).cpu().pin_memory() for k in

@@ -206,6 +206,37 @@ gw_status gw_decode_attn_global(const gw_kv_pool* pool, const void* q, void* out
 size_t gw_attn_workspace_bytes(const gw_kv_pool* pool, int32_t num_q_heads, int32_t batch,
                                int32_t max_seq_len, int32_t max_q_rows, int32_t window);
 
+/*
+ * gw_decode_attn_local_noalloc - gw_decode_attn_local without a workspace
+ * argument, for callers that cannot allocate device memory when they run
+ * attention (a CUDA graph whose memory plan is already fixed, an embedding
+ * runtime without a device allocator, a host that forbids allocation after
+ * start-up).  The pages this library follows have no counterpart of this
+ * entry point; it exists only for such callers.
+ *
+ * Same arguments, semantics, results and errors as gw_decode_attn_local,
+ * minus workspace/workspace_bytes.  The split-KV scratch is a file-scope
+ * device array of gw_noalloc_scratch_bytes() = 32 MiB that every GPU loading
+ * this library keeps until the process exits; the call allocates and frees
+ * nothing.  A call whose gw_attn_workspace_bytes(...) (with max_seq_len =
+ * max_pages_per_seq * 16) exceeds 32 MiB returns GW_ERR_WORKSPACE.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (each call re-initialises what it needs), so calls
+ * whose executions overlap on the GPU (different streams without ordering)
+ * race on it.  Sequences with more than one query row are not supported here
+ * any more than on gw_decode_attn_local today.
+ */
+gw_status gw_decode_attn_local_noalloc(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,
+                                       int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,
+                                       const int32_t* block_table, int32_t max_pages_per_seq, int32_t max_q_rows,
+                                       int32_t window, float scale, int32_t* dev_status, void* stream);
+
+/* Bytes of the static scratch behind gw_decode_attn_local_noalloc. */
+size_t gw_noalloc_scratch_bytes(void);
+
 /* Message of the calling thread's last failed call ("" if none). */
 const char* gw_last_error(void);
 

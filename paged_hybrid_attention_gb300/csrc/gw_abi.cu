@@ -69,6 +69,16 @@ int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
 }  // namespace
 
+gw_status set_error(gw_status code, const char* fn, const char* fmt, ...) {
+  int n = std::snprintf(g_err, sizeof(g_err), "%s: ", fn);
+  if (n < 0) n = 0;
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_err + n, sizeof(g_err) - static_cast<size_t>(n), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
 int num_sms() {
   static int cached = 0;
   static std::once_flag once;

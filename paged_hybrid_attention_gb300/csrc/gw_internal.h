@@ -95,6 +95,10 @@ struct AppendArgs {
 
 int num_sms();
 
+// Records `fmt` (printf-style) as the calling thread's gw_last_error message,
+// prefixed by `fn`, and returns `code`.
+gw_status set_error(gw_status code, const char* fn, const char* fmt, ...);
+
 // Split-KV plan: unit_base[s] = units of the decode-row sequences before s;
 // zeroes the work counter.  mode: kSplitLocal (units = kv_heads * chunks of
 // `chunk` pages of the window) or kSplitGlobal (units = global_chunks(L)).

@@ -28,7 +28,8 @@ LAYOUT_LOCAL, LAYOUT_GLOBAL_FOLDED, LAYOUT_GLOBAL_FULL = 0, 1, 2
 LAYOUTS = {"local": LAYOUT_LOCAL, "folded": LAYOUT_GLOBAL_FOLDED, "full": LAYOUT_GLOBAL_FULL}
 DTYPES = {"bf16": KV_BF16, "e4m3": KV_E4M3}
 EXPORTS = ["gw_pool_page_bytes", "gw_kv_append", "gw_decode_attn_local", "gw_decode_attn_global",
-           "gw_attn_workspace_bytes", "gw_last_error", "gw_version"]
+           "gw_attn_workspace_bytes", "gw_last_error", "gw_version", "gw_decode_attn_local_noalloc",
+           "gw_noalloc_scratch_bytes"]
 
 
 class GwError(RuntimeError):
@@ -57,6 +58,11 @@ _lib.gw_decode_attn_global.argtypes = [_P, _vp, _vp, _i32, _i32, _vp, _vp, _vp, 
 _lib.gw_decode_attn_global.restype = _i32
 _lib.gw_attn_workspace_bytes.argtypes = [_P, _i32, _i32, _i32, _i32, _i32]
 _lib.gw_attn_workspace_bytes.restype = _sz
+_lib.gw_decode_attn_local_noalloc.argtypes = [_P, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _f32,
+                                              _vp, _vp]
+_lib.gw_decode_attn_local_noalloc.restype = _i32
+_lib.gw_noalloc_scratch_bytes.argtypes = []
+_lib.gw_noalloc_scratch_bytes.restype = _sz
 _lib.gw_last_error.argtypes = []
 _lib.gw_last_error.restype = ctypes.c_char_p
 _lib.gw_version.argtypes = []
@@ -169,3 +175,14 @@ def decode_attn_global(pool, q, out, cu_q_rows, seq_lens, block_table, workspace
                                       _ptr(cu_q_rows), _ptr(seq_lens), _ptr(block_table), int(block_table.shape[1]),
                                       int(max_q_rows), float(scale), _ptr(workspace), int(workspace.numel()),
                                       _ptr(dev_status), _stream(stream)))
+
+
+def decode_attn_local_noalloc(pool, q, out, cu_q_rows, seq_lens, block_table, window, scale=None, max_q_rows=1,
+                              dev_status=None, stream=None):
+    """gw_decode_attn_local_noalloc: same as decode_attn_local, scratch from the library's static array."""
+    hq = int(q.shape[1])
+    scale = 1.0 / math.sqrt(256) if scale is None else scale
+    _check(_lib.gw_decode_attn_local_noalloc(ctypes.byref(pool.desc), _ptr(q), _ptr(out), hq,
+                                             int(seq_lens.numel()), _ptr(cu_q_rows), _ptr(seq_lens),
+                                             _ptr(block_table), int(block_table.shape[1]), int(max_q_rows),
+                                             int(window), float(scale), _ptr(dev_status), _stream(stream)))
