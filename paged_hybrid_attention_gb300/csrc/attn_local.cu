@@ -244,9 +244,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
     }
     __syncwarp();
 
-    // ---- o += p[t] * V[t]
+    // ---- o += p[t] * V[t]; masked tokens are skipped, not multiplied by
+    // zero: their bytes may be anything the pool held (even NaN patterns)
+    const bool stage_ok = sm.valid[st] != 0;
 #pragma unroll
     for (int t = 0; t < kTok; ++t) {
+      if (!stage_ok || t0 + t < d.tok_lo || t0 + t >= d.tok_hi) continue;
       float vf[8];
       load_row8<DT>(Vs + t * 256 * T::kEs, lane, vf);
       float pt[G];

@@ -47,9 +47,10 @@ __host__ __device__ __forceinline__ int global_chunks(int L) {
 //   [0, 256)          int32 work counter (+ padding)
 //   [256, ub_end)     int32 unit_base[batch + 1], rounded up to 256 bytes
 //   [ub_end, ml_end)  float2 (m, l) per (unit, head of the unit)
-//   [ml_end, ...)     float  o[unit][head of the unit][head_dim]
+//   [ml_end, o_end)   float  o[unit][head of the unit][head_dim]
+//   [o_end, ...)      int32 prompt_base[batch + 1] (prompt-row tile offsets)
 struct WsLayout {
-  size_t counter, unit_base, ml, o, total;
+  size_t counter, unit_base, ml, o, prompt_base, total;
   int64_t max_units;
   int heads_per_unit;
 };
@@ -77,6 +78,7 @@ struct LocalArgs {
   float* part_o;
   int64_t max_units;
   int32_t* status;
+  int32_t* prompt_base;  // tile offsets of the prompt-row kernels
 };
 
 struct AppendArgs {

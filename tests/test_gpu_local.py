@@ -165,3 +165,18 @@ def test_zero_row_sequences_are_skipped():
     layer = synth.Layer(sp, "local")
     out, ref, _ = _run(layer)
     _compare(layer, out, ref, [0, 2])
+
+
+def test_local_garbage_outside_window_is_ignored():
+    """Unwritten bytes of the window's first and last pages (NaN patterns
+    here) must not reach the output."""
+    fam = synth.Family("local", "bf16", "local", 2, 256, 256, 1e4, 40)
+    layer = synth.Layer(synth.custom("lnan", 13, 4, [100, 57, 333, 16], [1, 1, 1, 1], {"local": fam}), "local")
+    tab = gw.rope_table(1e4, 256, 256, 334)
+    pool = G.new_pool(layer, fill=0xFF)
+    G.append(layer, pool, tab.cuda())
+    out = G.attend(layer, pool)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    ref = H.build_pool(layer, tab.numpy())
+    _compare(layer, out, ref, range(layer.B))
