@@ -101,8 +101,6 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  const int total_units = a.unit_base[a.batch];
-  if (total_units > a.max_units) return;
   int32_t* st = a.status;
 
   // Stale tile / P slots must hold finite values: masked tokens get p = 0 and
@@ -130,6 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     sm.flag = 0;
     fence_mbar_init();
   }
+  pdl_wait();
+  pdl_trigger();
+  const int total_units = a.unit_base[a.batch];
+  if (total_units > a.max_units) return;  // uniform; nothing allocated yet
   if (warp == 5) {
     tc::alloc(&sm.tmem_base, 512);
     tc::relinquish();
@@ -473,10 +475,9 @@ cudaError_t launch_layout(const LocalArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   auto kern = global_decode_kernel<LAYOUT, HQ>;
   const size_t smem = sizeof(GSmem<LAYOUT, HQ>);
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  e = set_smem_once(kern, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreads, smem, stream>>>(a);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3(num_sms()), dim3(kThreads), smem, stream, a);
   if (e != cudaSuccess) return e;
   return launch_combine(a, kSplitGlobal, HQ, 512, 0, stream);
 }

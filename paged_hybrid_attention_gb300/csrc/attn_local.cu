@@ -115,15 +115,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WarpSmem& sm = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
-  const int total_units = a.unit_base[a.batch];
-  if (total_units > a.max_units) return;
-
   if (lane == 0) {
 #pragma unroll
     for (int i = 0; i < kStages; ++i) mbar_init(&sm.bar[i], 1);
     fence_mbar_init();
   }
   __syncwarp();
+  pdl_wait();
+  pdl_trigger();
+  const int total_units = a.unit_base[a.batch];
+  if (total_units > a.max_units) return;
   const uint64_t pol = policy_evict_first();
   const int64_t head_bytes = 2LL * kPage * 256 * T::kEs;  // K + V of one KV head in one page
   const int perm = (lane >> (5 - T::kLevels)) & (kTok - 1);
@@ -288,10 +289,9 @@ cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(WarpSmem) * kWarps;
   auto kern = local_decode_kernel<DT, G>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  e = set_smem_once(kern, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kWarps * 32, smem, st>>>(a);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3(num_sms()), dim3(kWarps * 32), smem, st, a);
   if (e != cudaSuccess) return e;
   return launch_combine(a, kSplitLocal, G, 256, T::kChunk, st);
 }

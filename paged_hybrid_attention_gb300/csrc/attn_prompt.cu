@@ -81,6 +81,8 @@ __device__ __forceinline__ int find_seq(const int32_t* base, int batch, int t) {
 __global__ void plan_prompt_kernel(const LocalArgs a, int heads_factor, int queries_per_tile) {
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -142,6 +144,8 @@ __global__ void __launch_bounds__(kLocalThreads, 2) local_prompt_kernel(const Lo
   LocalPromptSmem& sm = *reinterpret_cast<LocalPromptSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, c4 = lane & 3;
+  pdl_wait();
+  pdl_trigger();
   const int total = a.prompt_base[a.batch];
   const uint32_t q_s = smem_u32(sm.q);
   const int64_t head_elems = 2LL * kPage * 256;  // K + V of one KV head in one page
@@ -366,6 +370,8 @@ __global__ void __launch_bounds__(kGlobalThreads, 1) global_prompt_kernel(const 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, c4 = lane & 3;
   const int rg = warp >> 1, dh = warp & 1;  // row group (16 rows) and head-dim half
+  pdl_wait();
+  pdl_trigger();
   const int total = a.prompt_base[a.batch];
   const uint32_t q_s = smem_u32(sm.q);
   if (tid == 0) {
@@ -580,24 +586,24 @@ __global__ void __launch_bounds__(kGlobalThreads, 1) global_prompt_kernel(const 
 
 template <int G>
 cudaError_t launch_local_g(const LocalArgs& a, cudaStream_t st) {
-  plan_prompt_kernel<<<1, 1024, 0, st>>>(a, a.kv_heads, kRows / G);
+  cudaError_t e = launch_pdl(plan_prompt_kernel, dim3(1), dim3(1024), 0, st, a, a.kv_heads, kRows / G);
+  if (e != cudaSuccess) return e;
   auto kern = local_prompt_kernel<G>;
   const size_t smem = sizeof(LocalPromptSmem);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  e = set_smem_once(kern, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms() * 2, kLocalThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(num_sms() * 2), dim3(kLocalThreads), smem, st, a);
 }
 
 template <int LAYOUT, int HQ>
 cudaError_t launch_global_hq(const LocalArgs& a, cudaStream_t st) {
-  plan_prompt_kernel<<<1, 1024, 0, st>>>(a, 1, kRows / HQ);
+  cudaError_t e = launch_pdl(plan_prompt_kernel, dim3(1), dim3(1024), 0, st, a, 1, kRows / HQ);
+  if (e != cudaSuccess) return e;
   auto kern = global_prompt_kernel<LAYOUT, HQ>;
   const size_t smem = sizeof(GlobalPromptSmem<LAYOUT>);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  e = set_smem_once(kern, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kGlobalThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(num_sms()), dim3(kGlobalThreads), smem, st, a);
 }
 
 template <int LAYOUT>

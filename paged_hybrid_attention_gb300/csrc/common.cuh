@@ -5,7 +5,9 @@
 // unpacking used on the KV load path.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -126,6 +128,46 @@ __device__ __forceinline__ void e4m3x8_to_f32(const uint2& w, float (&f)[8]) {
 
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bit) {
   if (status) atomicOr(status, bit);
+}
+
+// ---- programmatic dependent launch ---------------------------------------
+// Every gw kernel is launched with programmatic stream serialisation allowed,
+// so its CTAs may be scheduled while the previous kernel of the stream is
+// still running.  pdl_wait() blocks until that kernel has completed and its
+// memory is visible; each kernel calls it before touching any memory the
+// caller or an earlier kernel may still be writing.  pdl_trigger() lets the
+// next kernel's CTAs be scheduled early (they still wait in pdl_wait()).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+template <typename K>
+inline cudaError_t set_smem_once(K kern, size_t bytes) {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 }  // namespace gw

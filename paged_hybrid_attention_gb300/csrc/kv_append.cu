@@ -18,11 +18,6 @@
 namespace gw {
 namespace {
 
-struct Pack8 {
-  uint4 bf;   // 8 bf16
-  uint2 e4;   // 8 e4m3
-};
-
 __device__ __forceinline__ void load_bf16x8(const uint16_t* p, float (&f)[8]) {
   bf16x8_to_f32(*reinterpret_cast<const uint4*>(p), f);
 }
@@ -96,6 +91,8 @@ __device__ __forceinline__ bool row_ok(const AppendArgs& a, int64_t row, int32_t
 // of K, and V chunks 8j and 128+8j.
 template <int DT>
 __global__ void append_local_kernel(const AppendArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = static_cast<int64_t>(a.num_rows) * a.kv_heads * 16;
   for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
        w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -147,6 +144,8 @@ __global__ void append_global_kernel(const AppendArgs a) {
   constexpr bool kFolded = LAYOUT == GW_LAYOUT_GLOBAL_FOLDED;
   constexpr int kRow = kFolded ? 640 : 1024;
   constexpr int kItems = kFolded ? 72 : 120;
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = static_cast<int64_t>(a.num_rows) * kItems;
   uint16_t* pool = reinterpret_cast<uint16_t*>(a.pool);
   for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
@@ -195,16 +194,14 @@ cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream
   constexpr int kBlock = 256;
   if (layout == GW_LAYOUT_LOCAL) {
     const int grid = grid_for(static_cast<int64_t>(a.num_rows) * a.kv_heads * 16, kBlock);
-    if (dtype == GW_KV_BF16)
-      append_local_kernel<GW_KV_BF16><<<grid, kBlock, 0, st>>>(a);
-    else
-      append_local_kernel<GW_KV_E4M3><<<grid, kBlock, 0, st>>>(a);
-  } else if (layout == GW_LAYOUT_GLOBAL_FOLDED) {
-    append_global_kernel<GW_LAYOUT_GLOBAL_FOLDED><<<grid_for(static_cast<int64_t>(a.num_rows) * 72, kBlock), kBlock, 0, st>>>(a);
-  } else {
-    append_global_kernel<GW_LAYOUT_GLOBAL_FULL><<<grid_for(static_cast<int64_t>(a.num_rows) * 120, kBlock), kBlock, 0, st>>>(a);
+    if (dtype == GW_KV_BF16) return launch_pdl(append_local_kernel<GW_KV_BF16>, dim3(grid), dim3(kBlock), 0, st, a);
+    return launch_pdl(append_local_kernel<GW_KV_E4M3>, dim3(grid), dim3(kBlock), 0, st, a);
   }
-  return cudaGetLastError();
+  if (layout == GW_LAYOUT_GLOBAL_FOLDED)
+    return launch_pdl(append_global_kernel<GW_LAYOUT_GLOBAL_FOLDED>,
+                      dim3(grid_for(static_cast<int64_t>(a.num_rows) * 72, kBlock)), dim3(kBlock), 0, st, a);
+  return launch_pdl(append_global_kernel<GW_LAYOUT_GLOBAL_FULL>,
+                    dim3(grid_for(static_cast<int64_t>(a.num_rows) * 120, kBlock)), dim3(kBlock), 0, st, a);
 }
 
 }  // namespace gw

@@ -21,6 +21,8 @@ __device__ __forceinline__ int seq_units(const LocalArgs& a, int mode, int chunk
 __global__ void plan_kernel(const LocalArgs a, int mode, int chunk) {
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -68,21 +70,21 @@ __global__ void plan_kernel(const LocalArgs a, int mode, int chunk) {
   }
 }
 
-// One warp per (sequence, q head); lane l covers dims [D/32 * l, D/32 * (l+1)).
+// One thread per (sequence, q head, 4 dims): merges that head's partials of
+// the sequence in chunk order (log-sum-exp, base 2) and writes bf16.
 template <int D>
 __global__ void combine_kernel(const LocalArgs a, int mode, int G, int chunk) {
-  constexpr int kPer = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int64_t w = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
-  if (w >= static_cast<int64_t>(a.batch) * a.num_q_heads) return;
-  const int s = static_cast<int>(w / a.num_q_heads), h = static_cast<int>(w % a.num_q_heads);
+  pdl_wait();
+  pdl_trigger();
+  constexpr int kQ = D / 4;
+  const int s = blockIdx.y;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= a.num_q_heads * kQ) return;
+  const int h = idx / kQ, d4 = idx % kQ;
   const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
   if (n != 1) return;
   const int L = a.seq_lens[s];
-  uint16_t* dst = a.out + (static_cast<int64_t>(a.cu_q_rows[s]) * a.num_q_heads + h) * D + lane * kPer;
-  float acc[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
   if (len_ok(a, L, 1) && a.unit_base[a.batch] <= a.max_units) {
     const int nc = mode == kSplitLocal ? local_chunks(L, a.window, chunk) : global_chunks(L);
@@ -91,51 +93,40 @@ __global__ void combine_kernel(const LocalArgs a, int mode, int G, int chunk) {
     float M = -INFINITY;
     for (int c = 0; c < nc; ++c) M = fmaxf(M, a.part_ml[(ub + c) * G + hh].x);
     if (M != -INFINITY) {
+#pragma unroll 4
       for (int c = 0; c < nc; ++c) {
         const float2 ml = a.part_ml[(ub + c) * G + hh];
         const float wgt = ex2(ml.x - M);
         den += wgt * ml.y;
-        const float* po = a.part_o + ((ub + c) * G + hh) * D + lane * kPer;
-#pragma unroll
-        for (int i = 0; i < kPer; i += 4) {
-          const float4 u = *reinterpret_cast<const float4*>(po + i);
-          acc[i] += wgt * u.x;
-          acc[i + 1] += wgt * u.y;
-          acc[i + 2] += wgt * u.z;
-          acc[i + 3] += wgt * u.w;
-        }
+        const float4 u = *reinterpret_cast<const float4*>(a.part_o + ((ub + c) * G + hh) * D + d4 * 4);
+        acc.x += wgt * u.x;
+        acc.y += wgt * u.y;
+        acc.z += wgt * u.z;
+        acc.w += wgt * u.w;
       }
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
-#pragma unroll
-  for (int i = 0; i < kPer; i += 8) {
-    uint32_t wv[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(acc[i + 2 * k] * inv, acc[i + 2 * k + 1] * inv);
-      wv[k] = *reinterpret_cast<uint32_t*>(&b);
-    }
-    *reinterpret_cast<uint4*>(dst + i) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 w;
+  w.x = *reinterpret_cast<uint32_t*>(&lo);
+  w.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(a.cu_q_rows[s]) * a.num_q_heads + h) * D + d4 * 4) = w;
 }
 
 }  // namespace
 
 cudaError_t launch_plan(const LocalArgs& a, int mode, int chunk, cudaStream_t st) {
-  plan_kernel<<<1, 1024, 0, st>>>(a, mode, chunk);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, a, mode, chunk);
 }
 
 cudaError_t launch_combine(const LocalArgs& a, int mode, int heads_per_unit, int head_dim, int chunk,
                            cudaStream_t st) {
-  const int64_t warps = static_cast<int64_t>(a.batch) * a.num_q_heads;
-  const int blocks = static_cast<int>((warps + 7) / 8);
-  if (head_dim == 256)
-    combine_kernel<256><<<blocks, 256, 0, st>>>(a, mode, heads_per_unit, chunk);
-  else
-    combine_kernel<512><<<blocks, 256, 0, st>>>(a, mode, heads_per_unit, chunk);
-  return cudaGetLastError();
+  const int threads = a.num_q_heads * head_dim / 4;
+  const dim3 grid((threads + 255) / 256, a.batch);
+  if (head_dim == 256) return launch_pdl(combine_kernel<256>, grid, dim3(256), 0, st, a, mode, heads_per_unit, chunk);
+  return launch_pdl(combine_kernel<512>, grid, dim3(256), 0, st, a, mode, heads_per_unit, chunk);
 }
 
 }  // namespace gw
