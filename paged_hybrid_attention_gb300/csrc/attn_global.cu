@@ -475,7 +475,7 @@ cudaError_t launch_layout(const LocalArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   auto kern = global_decode_kernel<LAYOUT, HQ>;
   const size_t smem = sizeof(GSmem<LAYOUT, HQ>);
-  e = set_smem_once(kern, smem);
+  e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_sms()), dim3(kThreads), smem, stream, a);
   if (e != cudaSuccess) return e;

@@ -289,7 +289,7 @@ cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(WarpSmem) * kWarps;
   auto kern = local_decode_kernel<DT, G>;
-  e = set_smem_once(kern, smem);
+  e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_sms()), dim3(kWarps * 32), smem, st, a);
   if (e != cudaSuccess) return e;

@@ -590,7 +590,7 @@ cudaError_t launch_local_g(const LocalArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   auto kern = local_prompt_kernel<G>;
   const size_t smem = sizeof(LocalPromptSmem);
-  e = set_smem_once(kern, smem);
+  e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(num_sms() * 2), dim3(kLocalThreads), smem, st, a);
 }
@@ -601,7 +601,7 @@ cudaError_t launch_global_hq(const LocalArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   auto kern = global_prompt_kernel<LAYOUT, HQ>;
   const size_t smem = sizeof(GlobalPromptSmem<LAYOUT>);
-  e = set_smem_once(kern, smem);
+  e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(num_sms()), dim3(kGlobalThreads), smem, st, a);
 }

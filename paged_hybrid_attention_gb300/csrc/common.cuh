@@ -6,6 +6,7 @@
 #pragma once
 
 #include <atomic>
+#include <mutex>
 #include <cstdint>
 #include <utility>
 #include <cuda_bf16.h>
@@ -156,18 +157,32 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Raise a kernel's dynamic shared-memory limit once per device.
-template <typename K>
-inline cudaError_t set_smem_once(K kern, size_t bytes) {
-  static std::atomic<uint64_t> done{0};
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device).
+inline cudaError_t set_smem_once(const void* kern, size_t bytes) {
+  struct Entry {
+    const void* fn;
+    uint64_t devices;
+  };
+  static std::mutex mu;
+  static Entry table[64];
+  static int used = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
-  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry* ent = nullptr;
+  for (int i = 0; i < used; ++i)
+    if (table[i].fn == kern) ent = &table[i];
+  if (ent && bit && (ent->devices & bit)) return cudaSuccess;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
-  return e;
+  if (e != cudaSuccess) return e;
+  if (!ent && used < 64) {
+    table[used] = Entry{kern, 0};
+    ent = &table[used++];
+  }
+  if (ent) ent->devices |= bit;
+  return cudaSuccess;
 }
 
 }  // namespace gw
