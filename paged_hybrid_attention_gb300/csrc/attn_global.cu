@@ -88,6 +88,12 @@ struct GSmem {
 
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Bounded wait whose outcome is the same for every lane of the warp (the
+// warp-uniform MMA issue must never diverge).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
 }
@@ -219,72 +225,76 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      const uint32_t id_qk = tc::idesc_bf16(64, HQ, false, false);
-      const uint32_t id_pv = tc::idesc_bf16(128, NP, true, true);
-      const uint32_t q_addr = smem_u32(sm.q);
-      uint32_t gi = 0;
-      int uidx = -1, prev_u = -1;
-      TileDesc prev{};
-      bool has_prev = false, ok = true;
+    // The whole warp runs this loop with warp-uniform values; elect.sync
+    // picks the issuing lane inside mma_bf16_warp / commit_warp.
+    const uint32_t id_qk = tc::idesc_bf16(64, HQ, false, false);
+    const uint32_t id_pv = tc::idesc_bf16(128, NP, true, true);
+    const uint32_t q_addr = smem_u32(sm.q);
+    // descriptor bases; the start-address field is addr >> 4 in the low bits,
+    // so a byte offset o is added as o >> 4 (all addresses stay below 256 KiB)
+    const uint64_t qk_a0 = tc::smem_desc(smem_u32(sm.tiles[0]), 128, T::kBlk * 128);
+    const uint64_t qk_b0 = tc::smem_desc(q_addr, 128, 64 * 128);
+    const uint64_t pv_a0 = tc::smem_desc(smem_u32(sm.tiles[0]), T::kBlk * 128, 128);
+    const uint64_t pv_b0 = tc::smem_desc(smem_u32(sm.p[0]), (NP / 8) * 128, 128);
+    constexpr uint32_t kTileBytes = kTilePages * T::kPageBytes;
+    uint32_t gi = 0;
+    int uidx = -1, prev_u = -1;
+    TileDesc prev{};
+    bool has_prev = false, ok = true;
 
-      auto pv = [&](const TileDesc& d, uint32_t i, int ui) -> bool {
-        if (!mbar_wait(&sm.p_ready[i & 1], (i >> 1) & 1, st)) return false;
-        const int ob = ui & 1;
-        if ((d.flags & kFirst) && ui >= 2 && !mbar_wait(&sm.o_free[ob], ((ui >> 1) - 1) & 1, st)) return false;
-        tc::fence_after();
-        const uint32_t tile = smem_u32(sm.tiles[i % NB]);
-        const uint32_t pb = smem_u32(sm.p[i & 1]);
+    auto pv = [&](const TileDesc& d, uint32_t i, int ui) -> bool {
+      if (!warp_wait(&sm.p_ready[i & 1], (i >> 1) & 1, st)) return false;
+      const int ob = ui & 1;
+      if ((d.flags & kFirst) && ui >= 2 && !warp_wait(&sm.o_free[ob], ((ui >> 1) - 1) & 1, st)) return false;
+      tc::fence_after();
+      const uint64_t a_tile = pv_a0 + (((i % NB) * kTileBytes) >> 4);
+      const uint64_t b_p = pv_b0 + (((i & 1) * sizeof(sm.p[0])) >> 4);
+#pragma unroll
+      for (int j = 0; j < kTilePages; ++j) {
+        const uint64_t bd = b_p + ((2 * j * (NP / 8) * 128) >> 4);
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll
-          for (int j = 0; j < kTilePages; ++j) {
-            const uint64_t ad = tc::smem_desc(tile + j * T::kPageBytes + (T::kVcb + 16 * blk) * 128,
-                                              T::kBlk * 128, 128);
-            const uint64_t bd = tc::smem_desc(pb + 2 * j * (NP / 8) * 128, (NP / 8) * 128, 128);
-            tc::mma_bf16(tmem + 64 + 128 * ob + 32 * blk, ad, bd, id_pv, !((d.flags & kFirst) && j == 0));
-          }
+          const uint64_t ad = a_tile + ((j * T::kPageBytes + (T::kVcb + 16 * blk) * 128) >> 4);
+          tc::mma_bf16_warp(tmem + 64 + 128 * ob + 32 * blk, ad, bd, id_pv, !((d.flags & kFirst) && j == 0));
         }
-        tc::commit(&sm.empty[i % NB]);
-        tc::commit(&sm.pfree[i & 1]);
-        if (d.flags & kLast) tc::commit(&sm.o_done[ob]);
-        return true;
-      };
-
-      while (true) {
-        const int b = gi % NB;
-        if (!mbar_wait(&sm.full[b], (gi / NB) & 1, st)) { ok = false; break; }
-        const TileDesc d = sm.ring[gi % kRing];
-        if (d.flags & kEnd) break;
-        if (d.flags & kFirst) {
-          ++uidx;
-          if (!mbar_wait(&sm.q_ready, uidx & 1, st)) { ok = false; break; }
-        }
-        tc::fence_after();
-        const uint32_t tile = smem_u32(sm.tiles[b]);
-        const uint32_t d_s = tmem + 32 * (gi & 1);
-#pragma unroll 8
-        for (int ks = 0; ks < 32; ++ks) {
-          const uint64_t ad = tc::smem_desc(tile + T::k_cb(ks) * 128, 128, T::kBlk * 128);
-          const uint64_t bd = tc::smem_desc(q_addr + 2 * ks * 128, 128, 64 * 128);
-          tc::mma_bf16(d_s, ad, bd, id_qk, ks > 0);
-        }
-        tc::commit(&sm.s_ready[gi & 1]);
-        if (d.flags & kLast) tc::commit(&sm.q_free);  // Q may be replaced once this completes
-        if constexpr (NB == 1) {
-          // one tile buffer: the next tile cannot load before this P.V is done
-          if (!pv(d, gi, uidx)) { ok = false; break; }
-        } else {
-          // two buffers: QK^T of this tile overlaps the softmax of the previous one
-          if (has_prev && !pv(prev, gi - 1, prev_u)) { ok = false; break; }
-          prev = d;
-          prev_u = uidx;
-          has_prev = true;
-        }
-        ++gi;
       }
-      if (NB > 1 && ok && has_prev) pv(prev, gi - 1, prev_u);
+      tc::commit_warp(&sm.empty[i % NB]);
+      tc::commit_warp(&sm.pfree[i & 1]);
+      if (d.flags & kLast) tc::commit_warp(&sm.o_done[ob]);
+      return true;
+    };
+
+    // Order per tile: P.V of the previous tile first (it frees that tile's
+    // buffer for the producer as early as possible, so the HBM load of the
+    // tile after next overlaps this tile's QK^T and softmax), then QK^T.
+    while (true) {
+      if (has_prev && !pv(prev, gi - 1, prev_u)) { ok = false; break; }
+      has_prev = false;
+      const int b = gi % NB;
+      if (!warp_wait(&sm.full[b], (gi / NB) & 1, st)) { ok = false; break; }
+      const TileDesc d = sm.ring[gi % kRing];
+      if (d.flags & kEnd) break;
+      if (d.flags & kFirst) {
+        ++uidx;
+        if (!warp_wait(&sm.q_ready, uidx & 1, st)) { ok = false; break; }
+      }
+      tc::fence_after();
+      const uint64_t a_tile = qk_a0 + ((b * kTileBytes) >> 4);
+      const uint32_t d_s = tmem + 32 * (gi & 1);
+#pragma unroll
+      for (int ks = 0; ks < 32; ++ks) {
+        const uint64_t ad = a_tile + ((T::k_cb(ks) * 128) >> 4);
+        const uint64_t bd = qk_b0 + ((2 * ks * 128) >> 4);
+        tc::mma_bf16_warp(d_s, ad, bd, id_qk, ks > 0);
+      }
+      tc::commit_warp(&sm.s_ready[gi & 1]);
+      if (d.flags & kLast) tc::commit_warp(&sm.q_free);  // Q may be replaced once this completes
+      prev = d;
+      prev_u = uidx;
+      has_prev = true;
+      ++gi;
     }
+    (void)ok;
   } else if (warp == 6) {
     // -------------------------------------------------------------- q loader
     // Ordering: wait until the last QK^T of the previous unit has completed

@@ -48,6 +48,27 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Warp-uniform issue: the whole warp executes the call with identical
+// operands and elect.sync picks the one lane that issues.  Keeping the
+// operands warp-uniform lets them stay in uniform registers, which makes the
+// issue several times cheaper than a single-lane divergent branch.
+__device__ __forceinline__ void mma_bf16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+
+// Warp-uniform commit by the elected (issuing) lane.
+__device__ __forceinline__ void commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
 // Arrive on `bar` once all previously issued tcgen05 operations of this
 // thread have completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
