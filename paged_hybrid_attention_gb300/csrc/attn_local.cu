@@ -9,7 +9,7 @@
 //
 // Design (split-KV flash decoding on CUDA cores; a GQA group of G <= 8 query
 // heads per KV head is too narrow for a tensor-core contraction):
-//   * Work unit = (sequence, KV head, chunk of up to 4 bf16 / 8 e4m3 pages of
+//   * Work unit = (sequence, KV head, chunk of up to 2 bf16 / 8 e4m3 pages of
 //     the window).  A plan kernel turns lengths into unit offsets; the split
 //     depends on the sequence's own length only.
 //   * Persistent CTAs, one per SM, of 8 independent warps.  Each warp takes
@@ -20,8 +20,10 @@
 //     across lanes with a transpose-reduction whose token order is permuted by
 //     lane bits, so every level is one shuffle + add per value (no selects).
 //   * Online softmax in base 2 (scale * log2 e folded into q), fp32 throughout.
-//   * Each unit writes an unnormalised partial (m, l, o); a combine kernel
-//     merges a sequence's partials in chunk order (log-sum-exp) into bf16.
+//   * Each unit writes an unnormalised partial (m, l, o); the warp that
+//     finishes the last unit of a (sequence, KV head) pair merges that pair's
+//     partials in chunk order (log-sum-exp, read back from L2) into bf16, so
+//     no separate combine launch is needed.
 #include "common.cuh"
 
 namespace gw {
@@ -33,7 +35,7 @@ constexpr int kStageBytes = 8192;
 constexpr int kRing = kStages + 2;
 
 struct Unit {
-  int32_t s, g, hp_lo, n, tok_lo, tok_hi, unit, row;
+  int32_t s, g, hp_lo, n, tok_lo, tok_hi, unit, row, nc, pad_[3];
 };
 
 struct __align__(128) WarpSmem {
@@ -78,6 +80,7 @@ __device__ __forceinline__ Unit decode_unit(const LocalArgs& a, int u) {
   d.n = (d.tok_hi - 1) / T::kTok + 1 - d.hp_lo;
   d.unit = u;
   d.row = a.cu_q_rows[lo];
+  d.nc = nc;
   return d;
 }
 
@@ -275,6 +278,46 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
         *reinterpret_cast<float4*>(po + h * 256 + 4) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
         if (lane == h) a.part_ml[static_cast<int64_t>(d.unit) * G + h] = make_float2(m[h], l);
       }
+      // ---- the warp that finishes a (sequence, KV head) pair's last unit
+      // merges the pair's partials in chunk order (from L2) and writes bf16
+      __threadfence();
+      __syncwarp();
+      const int pair = d.s * a.kv_heads + d.g;
+      int last = 0;
+      if (lane == 0) last = atomicAdd(&a.pair_cnt[pair], 1) == d.nc - 1;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+        const int64_t ub = static_cast<int64_t>(d.unit) - (d.unit - a.unit_base[d.s]) % d.nc;  // chunk 0 of the pair
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float M = -INFINITY;
+          for (int c = 0; c < d.nc; ++c) M = fmaxf(M, __ldcg(&a.part_ml[(ub + c) * G + h]).x);
+          float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          float den = 0.f;
+          if (M != -INFINITY) {
+            for (int c = 0; c < d.nc; ++c) {
+              const float2 ml = __ldcg(&a.part_ml[(ub + c) * G + h]);
+              const float wgt = ex2(ml.x - M);
+              den += wgt * ml.y;
+              const float* pp = a.part_o + ((ub + c) * G + h) * 256 + lane * 8;
+              const float4 u0 = __ldcg(reinterpret_cast<const float4*>(pp));
+              const float4 u1 = __ldcg(reinterpret_cast<const float4*>(pp + 4));
+              acc[0] += wgt * u0.x; acc[1] += wgt * u0.y; acc[2] += wgt * u0.z; acc[3] += wgt * u0.w;
+              acc[4] += wgt * u1.x; acc[5] += wgt * u1.y; acc[6] += wgt * u1.z; acc[7] += wgt * u1.w;
+            }
+          }
+          const float inv = den > 0.f ? 1.f / den : 0.f;
+          uint32_t wv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+            wv[i] = *reinterpret_cast<uint32_t*>(&b);
+          }
+          uint16_t* dst = a.out + (static_cast<int64_t>(d.row) * a.num_q_heads + d.g * G + h) * 256 + lane * 8;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+      }
       c_i = 0;
       c_slot = (c_slot + 1) % kRing;
     }
@@ -291,9 +334,7 @@ cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   auto kern = local_decode_kernel<DT, G>;
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(num_sms()), dim3(kWarps * 32), smem, st, a);
-  if (e != cudaSuccess) return e;
-  return launch_combine(a, kSplitLocal, G, 256, T::kChunk, st);
+  return launch_pdl(kern, dim3(num_sms()), dim3(kWarps * 32), smem, st, a);
 }
 
 template <int DT>
