@@ -9,7 +9,7 @@
 //
 // Design (split-KV flash decoding on CUDA cores; a GQA group of G <= 8 query
 // heads per KV head is too narrow for a tensor-core contraction):
-//   * Work unit = (sequence, KV head, chunk of up to 2 bf16 / 8 e4m3 pages of
+//   * Work unit = (sequence, KV head, chunk of up to 4 bf16 / 8 e4m3 pages of
 //     the window).  A plan kernel turns lengths into unit offsets; the split
 //     depends on the sequence's own length only.
 //   * Persistent CTAs, one per SM, of 8 independent warps.  Each warp takes
@@ -108,6 +108,70 @@ __device__ __forceinline__ void xreduce(float* x) {
       x[0] += __shfl_xor_sync(0xffffffffu, x[0], O);
       xreduce<1, O / 2>(x);
     }
+  }
+}
+
+// Log-sum-exp merge of one (sequence, KV head) pair's nc <= 64 partials, in
+// chunk order, by one warp; partials are read with ld.global.cg (other SMs
+// wrote them; L1 is not coherent).  Chunk weights are computed lane-parallel
+// and the o partials are loaded four chunks at a time to keep loads in flight.
+template <int G>
+__device__ __noinline__ void merge_pair(const LocalArgs& a, const Unit& d, int lane) {
+  const int nc = d.nc;
+  const int64_t ub = static_cast<int64_t>(d.unit) - (d.unit - a.unit_base[d.s]) % nc;  // chunk 0 of the pair
+#pragma unroll 1
+  for (int h = 0; h < G; ++h) {
+    float mc[2], lc[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int c = lane + 32 * k;
+      float2 ml = make_float2(-INFINITY, 0.f);
+      if (c < nc) ml = __ldcg(&a.part_ml[(ub + c) * G + h]);
+      mc[k] = ml.x;
+      lc[k] = ml.y;
+    }
+    float M = fmaxf(mc[0], mc[1]);
+#pragma unroll
+    for (int O = 16; O >= 1; O >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, O));
+    float wc[2], den = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      wc[k] = (M == -INFINITY || mc[k] == -INFINITY) ? 0.f : ex2(mc[k] - M);
+      den += wc[k] * lc[k];
+    }
+#pragma unroll
+    for (int O = 16; O >= 1; O >>= 1) den += __shfl_xor_sync(0xffffffffu, den, O);
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    const float* base = a.part_o + (ub * G + h) * 256 + lane * 8;
+#pragma unroll 1
+    for (int c0 = 0; c0 < nc; c0 += 4) {
+      float4 u[4][2];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = min(c0 + j, nc - 1);
+        const float* pp = base + static_cast<int64_t>(c) * G * 256;
+        u[j][0] = __ldcg(reinterpret_cast<const float4*>(pp));
+        u[j][1] = __ldcg(reinterpret_cast<const float4*>(pp + 4));
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + j;
+        const float w0 = __shfl_sync(0xffffffffu, wc[0], c & 31);
+        const float w1 = __shfl_sync(0xffffffffu, wc[1], c & 31);
+        const float w = c < nc ? (c < 32 ? w0 : w1) : 0.f;
+        acc[0] += w * u[j][0].x; acc[1] += w * u[j][0].y; acc[2] += w * u[j][0].z; acc[3] += w * u[j][0].w;
+        acc[4] += w * u[j][1].x; acc[5] += w * u[j][1].y; acc[6] += w * u[j][1].z; acc[7] += w * u[j][1].w;
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    uint32_t wv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+      wv[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    uint16_t* dst = a.out + (static_cast<int64_t>(d.row) * a.num_q_heads + d.g * G + h) * 256 + lane * 8;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
   }
 }
 
@@ -288,35 +352,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
         __threadfence();
-        const int64_t ub = static_cast<int64_t>(d.unit) - (d.unit - a.unit_base[d.s]) % d.nc;  // chunk 0 of the pair
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float M = -INFINITY;
-          for (int c = 0; c < d.nc; ++c) M = fmaxf(M, __ldcg(&a.part_ml[(ub + c) * G + h]).x);
-          float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          float den = 0.f;
-          if (M != -INFINITY) {
-            for (int c = 0; c < d.nc; ++c) {
-              const float2 ml = __ldcg(&a.part_ml[(ub + c) * G + h]);
-              const float wgt = ex2(ml.x - M);
-              den += wgt * ml.y;
-              const float* pp = a.part_o + ((ub + c) * G + h) * 256 + lane * 8;
-              const float4 u0 = __ldcg(reinterpret_cast<const float4*>(pp));
-              const float4 u1 = __ldcg(reinterpret_cast<const float4*>(pp + 4));
-              acc[0] += wgt * u0.x; acc[1] += wgt * u0.y; acc[2] += wgt * u0.z; acc[3] += wgt * u0.w;
-              acc[4] += wgt * u1.x; acc[5] += wgt * u1.y; acc[6] += wgt * u1.z; acc[7] += wgt * u1.w;
-            }
-          }
-          const float inv = den > 0.f ? 1.f / den : 0.f;
-          uint32_t wv[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-            wv[i] = *reinterpret_cast<uint32_t*>(&b);
-          }
-          uint16_t* dst = a.out + (static_cast<int64_t>(d.row) * a.num_q_heads + d.g * G + h) * 256 + lane * 8;
-          *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        }
+        merge_pair<G>(a, d, lane);
       }
       c_i = 0;
       c_slot = (c_slot + 1) % kRing;

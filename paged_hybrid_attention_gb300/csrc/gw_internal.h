@@ -14,7 +14,7 @@ namespace gw {
 // logical pages of that sequence's window); a global unit is (sequence, chunk
 // of global_chunk_pages(L) pages).  Chunks depend only on the sequence's own
 // length, so a row's arithmetic never depends on the rest of the batch.
-constexpr int kLocalChunkPagesBf16 = 2;
+constexpr int kLocalChunkPagesBf16 = 4;
 constexpr int kLocalChunkPagesE4m3 = 8;
 // Global chunks start at 16 pages and double until a sequence has at most
 // kGlobalMaxChunks of them (long contexts get long chunks, so the partials
