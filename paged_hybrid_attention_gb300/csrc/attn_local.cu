@@ -20,10 +20,8 @@
 //     across lanes with a transpose-reduction whose token order is permuted by
 //     lane bits, so every level is one shuffle + add per value (no selects).
 //   * Online softmax in base 2 (scale * log2 e folded into q), fp32 throughout.
-//   * Each unit writes an unnormalised partial (m, l, o); the warp that
-//     finishes the last unit of a (sequence, KV head) pair merges that pair's
-//     partials in chunk order (log-sum-exp, read back from L2) into bf16, so
-//     no separate combine launch is needed.
+//   * Each unit writes an unnormalised partial (m, l, o); a combine kernel
+//     merges a sequence's partials in chunk order (log-sum-exp) into bf16.
 #include "common.cuh"
 
 namespace gw {
@@ -35,7 +33,7 @@ constexpr int kStageBytes = 8192;
 constexpr int kRing = kStages + 2;
 
 struct Unit {
-  int32_t s, g, hp_lo, n, tok_lo, tok_hi, unit, row, nc, pad_[3];
+  int32_t s, g, hp_lo, n, tok_lo, tok_hi, unit, row;
 };
 
 struct __align__(128) WarpSmem {
@@ -80,7 +78,6 @@ __device__ __forceinline__ Unit decode_unit(const LocalArgs& a, int u) {
   d.n = (d.tok_hi - 1) / T::kTok + 1 - d.hp_lo;
   d.unit = u;
   d.row = a.cu_q_rows[lo];
-  d.nc = nc;
   return d;
 }
 
@@ -108,70 +105,6 @@ __device__ __forceinline__ void xreduce(float* x) {
       x[0] += __shfl_xor_sync(0xffffffffu, x[0], O);
       xreduce<1, O / 2>(x);
     }
-  }
-}
-
-// Log-sum-exp merge of one (sequence, KV head) pair's nc <= 64 partials, in
-// chunk order, by one warp; partials are read with ld.global.cg (other SMs
-// wrote them; L1 is not coherent).  Chunk weights are computed lane-parallel
-// and the o partials are loaded four chunks at a time to keep loads in flight.
-template <int G>
-__device__ __noinline__ void merge_pair(const LocalArgs& a, const Unit& d, int lane) {
-  const int nc = d.nc;
-  const int64_t ub = static_cast<int64_t>(d.unit) - (d.unit - a.unit_base[d.s]) % nc;  // chunk 0 of the pair
-#pragma unroll 1
-  for (int h = 0; h < G; ++h) {
-    float mc[2], lc[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int c = lane + 32 * k;
-      float2 ml = make_float2(-INFINITY, 0.f);
-      if (c < nc) ml = __ldcg(&a.part_ml[(ub + c) * G + h]);
-      mc[k] = ml.x;
-      lc[k] = ml.y;
-    }
-    float M = fmaxf(mc[0], mc[1]);
-#pragma unroll
-    for (int O = 16; O >= 1; O >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, O));
-    float wc[2], den = 0.f;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      wc[k] = (M == -INFINITY || mc[k] == -INFINITY) ? 0.f : ex2(mc[k] - M);
-      den += wc[k] * lc[k];
-    }
-#pragma unroll
-    for (int O = 16; O >= 1; O >>= 1) den += __shfl_xor_sync(0xffffffffu, den, O);
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    const float* base = a.part_o + (ub * G + h) * 256 + lane * 8;
-#pragma unroll 1
-    for (int c0 = 0; c0 < nc; c0 += 4) {
-      float4 u[4][2];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = min(c0 + j, nc - 1);
-        const float* pp = base + static_cast<int64_t>(c) * G * 256;
-        u[j][0] = __ldcg(reinterpret_cast<const float4*>(pp));
-        u[j][1] = __ldcg(reinterpret_cast<const float4*>(pp + 4));
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = c0 + j;
-        const float w0 = __shfl_sync(0xffffffffu, wc[0], c & 31);
-        const float w1 = __shfl_sync(0xffffffffu, wc[1], c & 31);
-        const float w = c < nc ? (c < 32 ? w0 : w1) : 0.f;
-        acc[0] += w * u[j][0].x; acc[1] += w * u[j][0].y; acc[2] += w * u[j][0].z; acc[3] += w * u[j][0].w;
-        acc[4] += w * u[j][1].x; acc[5] += w * u[j][1].y; acc[6] += w * u[j][1].z; acc[7] += w * u[j][1].w;
-      }
-    }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    uint32_t wv[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-      wv[i] = *reinterpret_cast<uint32_t*>(&b);
-    }
-    uint16_t* dst = a.out + (static_cast<int64_t>(d.row) * a.num_q_heads + d.g * G + h) * 256 + lane * 8;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
   }
 }
 
@@ -342,18 +275,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
         *reinterpret_cast<float4*>(po + h * 256 + 4) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
         if (lane == h) a.part_ml[static_cast<int64_t>(d.unit) * G + h] = make_float2(m[h], l);
       }
-      // ---- the warp that finishes a (sequence, KV head) pair's last unit
-      // merges the pair's partials in chunk order (from L2) and writes bf16
-      __threadfence();
-      __syncwarp();
-      const int pair = d.s * a.kv_heads + d.g;
-      int last = 0;
-      if (lane == 0) last = atomicAdd(&a.pair_cnt[pair], 1) == d.nc - 1;
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence();
-        merge_pair<G>(a, d, lane);
-      }
       c_i = 0;
       c_slot = (c_slot + 1) % kRing;
     }
@@ -370,7 +291,9 @@ cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   auto kern = local_decode_kernel<DT, G>;
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(num_sms()), dim3(kWarps * 32), smem, st, a);
+  e = launch_pdl(kern, dim3(num_sms()), dim3(kWarps * 32), smem, st, a);
+  if (e != cudaSuccess) return e;
+  return launch_combine(a, kSplitLocal, G, 256, T::kChunk, st);
 }
 
 template <int DT>

@@ -114,9 +114,7 @@ WsLayout ws_layout(int layout, int dtype, int kv_heads, int num_q_heads, int bat
   w.ml = w.unit_base + round_up(static_cast<size_t>(batch + 1) * 4, 256);
   w.o = w.ml + round_up(static_cast<size_t>(units) * w.heads_per_unit * 8, 256);
   w.prompt_base = w.o + round_up(static_cast<size_t>(units) * w.heads_per_unit * D * 4, 256);
-  w.pair = w.prompt_base + round_up(static_cast<size_t>(batch + 1) * 4, 256);
-  const size_t pairs = layout == GW_LAYOUT_LOCAL ? static_cast<size_t>(batch) * kv_heads : 0;
-  w.total = w.pair + round_up(pairs * 4, 256);
+  w.total = w.prompt_base + round_up(static_cast<size_t>(batch + 1) * 4, 256);
   return w;
 }
 
@@ -234,7 +232,6 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
   a.part_ml = reinterpret_cast<float2*>(ws + w.ml);
   a.part_o = reinterpret_cast<float*>(ws + w.o);
   a.prompt_base = reinterpret_cast<int32_t*>(ws + w.prompt_base);
-  a.pair_cnt = reinterpret_cast<int32_t*>(ws + w.pair);
   a.max_units = w.max_units;
   a.status = dev_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

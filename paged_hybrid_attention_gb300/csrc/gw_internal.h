@@ -48,11 +48,9 @@ __host__ __device__ __forceinline__ int global_chunks(int L) {
 //   [256, ub_end)     int32 unit_base[batch + 1], rounded up to 256 bytes
 //   [ub_end, ml_end)  float2 (m, l) per (unit, head of the unit)
 //   [ml_end, o_end)   float  o[unit][head of the unit][head_dim]
-//   [o_end, pb_end)   int32 prompt_base[batch + 1] (prompt-row tile offsets)
-//   [pb_end, ...)     int32 pair_cnt[batch * kv_heads] (local: finished units
-//                     per (sequence, KV head), zeroed by the plan kernel)
+//   [o_end, ...)      int32 prompt_base[batch + 1] (prompt-row tile offsets)
 struct WsLayout {
-  size_t counter, unit_base, ml, o, prompt_base, pair, total;
+  size_t counter, unit_base, ml, o, prompt_base, total;
   int64_t max_units;
   int heads_per_unit;
 };
@@ -81,7 +79,6 @@ struct LocalArgs {
   int64_t max_units;
   int32_t* status;
   int32_t* prompt_base;  // tile offsets of the prompt-row kernels
-  int32_t* pair_cnt;     // local decode: finished units per (sequence, KV head)
 };
 
 struct AppendArgs {
@@ -105,8 +102,7 @@ int num_sms();
 gw_status set_error(gw_status code, const char* fn, const char* fmt, ...);
 
 // Split-KV plan: unit_base[s] = units of the decode-row sequences before s;
-// zeroes the work counter (and, local mode, the per-pair unit counters) and
-// writes zero rows for decode rows it refuses.  mode: kSplitLocal (units = kv_heads * chunks of
+// zeroes the work counter.  mode: kSplitLocal (units = kv_heads * chunks of
 // `chunk` pages of the window) or kSplitGlobal (units = global_chunks(L)).
 cudaError_t launch_plan(const LocalArgs& a, int mode, int chunk, cudaStream_t st);
 // Log-sum-exp merge of each decode row's partials into bf16 `out`.

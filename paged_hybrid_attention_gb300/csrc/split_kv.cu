@@ -33,15 +33,10 @@ __global__ void plan_kernel(const LocalArgs a, int mode, int chunk) {
       const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
       const int L = a.seq_lens[s];
       if (n == 1) {
-        if (len_ok(a, L, n)) {
+        if (len_ok(a, L, n))
           units = seq_units(a, mode, chunk, L);
-        } else {
+        else
           set_status(a.status, GW_DEV_LEN_RANGE);
-          if (mode == kSplitLocal) {  // no unit will write this row: zero it here
-            uint4* row = reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(a.cu_q_rows[s]) * a.num_q_heads * 256);
-            for (int i = 0; i < a.num_q_heads * 32; ++i) row[i] = make_uint4(0, 0, 0, 0);
-          }
-        }
       }
     }
     int x = units;  // inclusive warp scan
@@ -68,22 +63,10 @@ __global__ void plan_kernel(const LocalArgs a, int mode, int chunk) {
     if (threadIdx.x == blockDim.x - 1) carry = excl + units;
     __syncthreads();
   }
-  if (mode == kSplitLocal) {
-    const int pairs = a.batch * a.kv_heads;
-    for (int i = threadIdx.x; i < pairs; i += blockDim.x) a.pair_cnt[i] = 0;
-  }
   if (threadIdx.x == 0) {
     a.unit_base[a.batch] = carry;
     *a.counter = 0;
     if (carry > a.max_units) set_status(a.status, GW_DEV_WORKSPACE);
-  }
-  if (mode == kSplitLocal && carry > a.max_units) {
-    // nothing will be computed: zero every decode row
-    for (int s = 0; s < a.batch; ++s) {
-      if (a.cu_q_rows[s + 1] - a.cu_q_rows[s] != 1) continue;
-      uint4* row = reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(a.cu_q_rows[s]) * a.num_q_heads * 256);
-      for (int i = threadIdx.x; i < a.num_q_heads * 32; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
-    }
   }
 }
 
