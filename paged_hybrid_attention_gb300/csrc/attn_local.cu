@@ -19,7 +19,11 @@
 //   * Lane l owns head dims [8l, 8l+8).  q.K partial dot products are reduced
 //     across lanes with a transpose-reduction whose token order is permuted by
 //     lane bits, so every level is one shuffle + add per value (no selects).
-//   * Online softmax in base 2 (scale * log2 e folded into q), fp32 throughout.
+//   * Products use the mixed-precision fma.rn.f32.{bf16,f16} (16-bit operands
+//     read from packed registers, fp32 accumulate), so K and V are never
+//     widened: bf16 pages multiply as stored, e4m3 pages after one paired
+//     e4m3x2 -> f16x2 conversion.  Softmax is base 2 in fp32; P is rounded to
+//     the multiplicand format and l sums exactly the rounded weights.
 //   * Each unit writes an unnormalised partial (m, l, o); a combine kernel
 //     merges a sequence's partials in chunk order (log-sum-exp) into bf16.
 #include "common.cuh"
@@ -42,7 +46,7 @@ struct __align__(128) WarpSmem {
   int32_t valid[kStages];
   int32_t pad_;
   Unit ring[kRing];
-  float pbuf[16 * 8];
+  uint16_t pbuf[16 * 8];  // p of (token, head) in the 16-bit multiplicand format
 };
 
 template <int DT>
@@ -81,14 +85,58 @@ __device__ __forceinline__ Unit decode_unit(const LocalArgs& a, int u) {
   return d;
 }
 
+// Mixed-precision multiply-add with fp32 accumulation (sm_100+): d = a * b + c
+// with 16-bit a, b taken straight from the halves of packed registers.  The
+// product of two 16-bit floats is exact in fp32, so this equals an fp32 FMA on
+// the widened values, without spending an instruction on the widening.
+// bf16 pages multiply in bf16 (q is bf16 already); e4m3 pages are widened to
+// f16 by the paired e4m3x2 -> f16x2 conversion and multiply in f16 (q is
+// rounded to f16 once per unit, exact for |q| in the f16 normal range).
 template <int DT>
-__device__ __forceinline__ void load_row8(const uint8_t* row_base, int lane, float (&f)[8]) {
-  if constexpr (DT == GW_KV_BF16) {
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(row_base + lane * 16), f);
-  } else {
-    e4m3x8_to_f32(*reinterpret_cast<const uint2*>(row_base + lane * 8), f);
+struct Mix;
+template <>
+struct Mix<GW_KV_BF16> {
+  __device__ __forceinline__ static float fma(uint16_t a, uint16_t b, float c) {
+    float d;
+    asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
   }
-}
+  __device__ __forceinline__ static uint16_t from_f32(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+  __device__ __forceinline__ static float to_f32(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
+  __device__ __forceinline__ static uint16_t from_bf16(uint16_t x) { return x; }
+  // this lane's 8 elements of a row as 4 packed pairs
+  __device__ __forceinline__ static void row(const uint8_t* base, int lane, uint32_t (&w)[4]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(base + lane * 16);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  }
+};
+template <>
+struct Mix<GW_KV_E4M3> {
+  __device__ __forceinline__ static float fma(uint16_t a, uint16_t b, float c) {
+    float d;
+    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+  }
+  __device__ __forceinline__ static uint16_t from_f32(float x) { return __half_as_ushort(__float2half_rn(x)); }
+  __device__ __forceinline__ static float to_f32(uint16_t x) { return __half2float(__ushort_as_half(x)); }
+  __device__ __forceinline__ static uint16_t from_bf16(uint16_t x) {
+    return __half_as_ushort(__float2half_rn(__uint_as_float(static_cast<uint32_t>(x) << 16)));
+  }
+  __device__ __forceinline__ static void row(const uint8_t* base, int lane, uint32_t (&w)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2*>(base + lane * 8);
+    const uint32_t u[2] = {v.x, v.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[i] & 0xFFFFu), __NV_E4M3);
+      __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[i] >> 16), __NV_E4M3);
+      w[2 * i] = *reinterpret_cast<uint32_t*>(&lo);
+      w[2 * i + 1] = *reinterpret_cast<uint32_t*>(&hi);
+    }
+  }
+};
+
+__device__ __forceinline__ uint16_t lo16(uint32_t w) { return static_cast<uint16_t>(w & 0xFFFFu); }
+__device__ __forceinline__ uint16_t hi16(uint32_t w) { return static_cast<uint16_t>(w >> 16); }
 
 // Transpose-reduction over the 32 lanes of x[N] (N = tokens per stage) whose
 // entry j holds token j ^ perm(lane).  Each halving level keeps the lower half
@@ -176,7 +224,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
   f_done = !grab(0);
   while (!f_done && issued - consumed < kStages) issue();
 
-  float qf[G][8], o[G][8], m[G], lsum[G];
+  using X = Mix<DT>;
+  uint32_t q16[G][4];  // this lane's 8 q dims per head, packed 16-bit pairs
+  float o[G][8], m[G], lsum[G];
   int c_slot = 0, c_i = 0;
   while (consumed < issued) {
     const Unit d = sm.ring[c_slot];
@@ -184,13 +234,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
       const uint16_t* qrow = a.q + (static_cast<int64_t>(d.row) * a.num_q_heads + d.g * G) * 256 + lane * 8;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float t[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(qrow + h * 256), t);
+        const uint4 qv = *reinterpret_cast<const uint4*>(qrow + h * 256);
+        const uint32_t u[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          qf[h][i] = t[i] * a.scale_log2;
-          o[h][i] = 0.f;
-        }
+        for (int i = 0; i < 4; ++i)
+          q16[h][i] = static_cast<uint32_t>(X::from_bf16(lo16(u[i]))) | (static_cast<uint32_t>(X::from_bf16(hi16(u[i]))) << 16);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
         m[h] = -INFINITY;
         lsum[h] = 0.f;
       }
@@ -209,13 +259,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
     float x[G][kTok];
 #pragma unroll
     for (int j = 0; j < kTok; ++j) {
-      float kf[8];
-      load_row8<DT>(Ks + (j ^ perm) * 256 * T::kEs, lane, kf);
+      uint32_t w[4];
+      X::row(Ks + (j ^ perm) * 256 * T::kEs, lane, w);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float acc = qf[h][0] * kf[0];
+        float acc = 0.f;
 #pragma unroll
-        for (int i = 1; i < 8; ++i) acc = fmaf(qf[h][i], kf[i], acc);
+        for (int i = 0; i < 4; ++i) {
+          acc = X::fma(lo16(q16[h][i]), lo16(w[i]), acc);
+          acc = X::fma(hi16(q16[h][i]), hi16(w[i]), acc);
+        }
         x[h][j] = acc;
       }
     }
@@ -224,24 +277,25 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
 
     const int tabs = t0 + perm;
     const bool valid = sm.valid[st] && tabs >= d.tok_lo && tabs < d.tok_hi;
-    float p[G];
+    uint16_t p16[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float s = valid ? x[h][0] : -INFINITY;
+      const float s = valid ? x[h][0] * a.scale_log2 : -INFINITY;
       float mx = s;
 #pragma unroll
       for (int O = 1 << (5 - T::kLevels); O < 32; O <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, O));
       const float mnew = fmaxf(m[h], mx);
       const float alpha = mnew == -INFINITY ? 1.f : ex2(m[h] - mnew);
-      p[h] = valid ? ex2(s - mnew) : 0.f;
+      p16[h] = X::from_f32(valid ? ex2(s - mnew) : 0.f);
       m[h] = mnew;
-      lsum[h] = lsum[h] * alpha + (canon ? p[h] : 0.f);
+      // l sums the rounded weights P.V multiplies by
+      lsum[h] = lsum[h] * alpha + (canon ? X::to_f32(p16[h]) : 0.f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[h][i] *= alpha;
     }
     if (canon) {
 #pragma unroll
-      for (int h = 0; h < G; ++h) sm.pbuf[perm * G + h] = p[h];
+      for (int h = 0; h < G; ++h) sm.pbuf[perm * G + h] = p16[h];
     }
     __syncwarp();
 
@@ -251,15 +305,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
 #pragma unroll
     for (int t = 0; t < kTok; ++t) {
       if (!stage_ok || t0 + t < d.tok_lo || t0 + t >= d.tok_hi) continue;
-      float vf[8];
-      load_row8<DT>(Vs + t * 256 * T::kEs, lane, vf);
-      float pt[G];
+      uint32_t w[4];
+      X::row(Vs + t * 256 * T::kEs, lane, w);
 #pragma unroll
-      for (int h = 0; h < G; ++h) pt[h] = sm.pbuf[t * G + h];
+      for (int h = 0; h < G; ++h) {
+        const uint16_t ph = sm.pbuf[t * G + h];
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[h][i] = fmaf(pt[h], vf[i], o[h][i]);
+        for (int i = 0; i < 4; ++i) {
+          o[h][2 * i] = X::fma(ph, lo16(w[i]), o[h][2 * i]);
+          o[h][2 * i + 1] = X::fma(ph, hi16(w[i]), o[h][2 * i + 1]);
+        }
+      }
     }
     __syncwarp();
     ++consumed;
