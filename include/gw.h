@@ -173,18 +173,9 @@ gw_status gw_kv_append(const gw_kv_pool* pool, const void* k, const void* v, int
  *   max_q_rows   host bound on n_b (1 for a pure decode step).
  *   window       >= 1 (1024 for the served model).
  *   workspace    device scratch of at least gw_attn_workspace_bytes(...),
- *                256-byte aligned, zero-filled once before its first use.
- *                Every call leaves its counter words zero again, so one
- *                workspace can serve any later local or global call on the
- *                same stream; two calls that may run concurrently need two.
- * The decode rows run as one persistent kernel of one CTA per SM whose CTAs
- * meet at a grid-wide barrier before merging the split-KV partials; it
- * assumes every SM of the device is available to it (a kernel that occupies
- * SMs for the whole call on another stream makes the barrier time out after
- * two seconds and GW_DEV_TIMEOUT is reported).
+ *                16-byte aligned; contents need no initialisation.
  * Errors: GW_ERR_INVALID_ARG, GW_ERR_WORKSPACE, GW_ERR_UNSUPPORTED
- * (num_q_heads / kv_heads not in {1,2,4,8}; batch > 4096; prompt rows on an
- * e4m3 pool), GW_ERR_CUDA.
+ * (num_q_heads / kv_heads not in {1,2,4,8}), GW_ERR_CUDA.
  */
 gw_status gw_decode_attn_local(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,
                                int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,

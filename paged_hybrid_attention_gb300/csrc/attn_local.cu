@@ -24,13 +24,8 @@
 //     widened: bf16 pages multiply as stored, e4m3 pages after one paired
 //     e4m3x2 -> f16x2 conversion.  Softmax is base 2 in fp32; P is rounded to
 //     the multiplicand format and l sums exactly the rounded weights.
-//   * Each unit writes an unnormalised partial (m, l, o).  One launch does
-//     the whole call: every CTA computes the split plan of the batch in shared
-//     memory, streams units, meets the other CTAs at a bounded grid-wide
-//     barrier (one CTA per SM, all resident), and then the CTAs merge the
-//     (sequence, KV head) pairs' partials in chunk order (log-sum-exp) from
-//     L2 into bf16.  The claim / barrier / exit counters in the workspace are
-//     zero on entry and the last CTA out returns them to zero.
+//   * Each unit writes an unnormalised partial (m, l, o); a combine kernel
+//     merges a sequence's partials in chunk order (log-sum-exp) into bf16.
 #include "common.cuh"
 
 namespace gw {
@@ -54,15 +49,6 @@ struct __align__(128) WarpSmem {
   uint16_t pbuf[16 * 8];  // p of (token, head) in the 16-bit multiplicand format
 };
 
-// Whole-call shared state of a CTA: the per-warp pipelines plus the split
-// plan (unit offset of every sequence), computed by each CTA for itself.
-constexpr int kMaxBatch = kLocalMaxBatch;
-struct CtaSmem {
-  WarpSmem warp[kWarps];
-  int32_t ubase[kMaxBatch + 1];
-  int32_t scan[kWarps];
-};
-
 template <int DT>
 struct Traits {
   static constexpr int kEs = DT == GW_KV_BF16 ? 2 : 1;
@@ -73,11 +59,11 @@ struct Traits {
 };
 
 template <class T>
-__device__ __forceinline__ Unit decode_unit(const LocalArgs& a, const int32_t* ubase, int u) {
+__device__ __forceinline__ Unit decode_unit(const LocalArgs& a, int u) {
   int lo = 0, hi = a.batch;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (ubase[mid] <= u) lo = mid; else hi = mid - 1;
+    if (a.unit_base[mid] <= u) lo = mid; else hi = mid - 1;
   }
   Unit d;
   d.s = lo;
@@ -85,7 +71,7 @@ __device__ __forceinline__ Unit decode_unit(const LocalArgs& a, const int32_t* u
   const int first = L > a.window ? L - a.window : 0;
   const int p0 = first / kPage, p1 = (L - 1) / kPage;
   const int nc = (p1 - p0 + T::kChunk) / T::kChunk;
-  const int r = u - ubase[lo];
+  const int r = u - a.unit_base[lo];
   d.g = r / nc;
   const int c = r % nc;
   const int lpa = p0 + c * T::kChunk;
@@ -97,113 +83,6 @@ __device__ __forceinline__ Unit decode_unit(const LocalArgs& a, const int32_t* u
   d.unit = u;
   d.row = a.cu_q_rows[lo];
   return d;
-}
-
-__device__ __forceinline__ bool len_ok(const LocalArgs& a, int L) {
-  return L >= 1 && static_cast<int64_t>(L) <= static_cast<int64_t>(a.max_pages) * kPage;
-}
-
-// Split plan of the whole batch, computed by one CTA into shared memory:
-// ubase[s] = units of the decode-row sequences before s.  Sequences this CTA
-// owns (s % gridDim.x == blockIdx.x) with a refused length get status bits and
-// zero output rows here, since no unit will write them.
-template <class T>
-__device__ void plan_in_smem(const LocalArgs& a, CtaSmem& sm) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  int carry = 0;
-  for (int base = 0; base < a.batch; base += kWarps * 32) {
-    const int s = base + tid;
-    int units = 0;
-    if (s < a.batch && a.cu_q_rows[s + 1] - a.cu_q_rows[s] == 1) {
-      const int L = a.seq_lens[s];
-      if (len_ok(a, L)) {
-        units = a.kv_heads * local_chunks(L, a.window, T::kChunk);
-      } else if (s % gridDim.x == blockIdx.x) {
-        set_status(a.status, GW_DEV_LEN_RANGE);
-        uint4* row = reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(a.cu_q_rows[s]) * a.num_q_heads * 256);
-        for (int i = 0; i < a.num_q_heads * 32; ++i) row[i] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    int x = units;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) sm.scan[w] = x;
-    __syncthreads();
-    int before = carry;
-    for (int k = 0; k < w; ++k) before += sm.scan[k];
-    int tot = carry;
-    for (int k = 0; k < kWarps; ++k) tot += sm.scan[k];
-    if (s < a.batch) sm.ubase[s] = before + x - units;
-    carry = tot;
-    __syncthreads();
-  }
-  if (tid == 0) sm.ubase[a.batch] = carry;
-  __syncthreads();
-}
-
-// Log-sum-exp merge of one (sequence, KV head) pair's nc <= 64 partials in
-// chunk order, by one warp; partials come from other SMs, so they are read
-// with ld.global.cg (L1 is not coherent).  Chunk weights are lane-parallel and
-// the o partials are loaded four chunks at a time.
-template <int G>
-__device__ void merge_pair(const LocalArgs& a, int64_t ub, int nc, int row, int g, int lane) {
-#pragma unroll 1
-  for (int h = 0; h < G; ++h) {
-    float mc[2], lc[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int c = lane + 32 * k;
-      float2 ml = make_float2(-INFINITY, 0.f);
-      if (c < nc) ml = __ldcg(&a.part_ml[(ub + c) * G + h]);
-      mc[k] = ml.x;
-      lc[k] = ml.y;
-    }
-    float M = fmaxf(mc[0], mc[1]);
-#pragma unroll
-    for (int O = 16; O >= 1; O >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, O));
-    float wc[2], den = 0.f;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      wc[k] = (M == -INFINITY || mc[k] == -INFINITY) ? 0.f : ex2(mc[k] - M);
-      den += wc[k] * lc[k];
-    }
-#pragma unroll
-    for (int O = 16; O >= 1; O >>= 1) den += __shfl_xor_sync(0xffffffffu, den, O);
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    const float* base = a.part_o + (ub * G + h) * 256 + lane * 8;
-#pragma unroll 1
-    for (int c0 = 0; c0 < nc; c0 += 4) {
-      float4 u[4][2];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = min(c0 + j, nc - 1);
-        const float* pp = base + static_cast<int64_t>(c) * G * 256;
-        u[j][0] = __ldcg(reinterpret_cast<const float4*>(pp));
-        u[j][1] = __ldcg(reinterpret_cast<const float4*>(pp + 4));
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = c0 + j;
-        const float w0 = __shfl_sync(0xffffffffu, wc[0], c & 31);
-        const float w1 = __shfl_sync(0xffffffffu, wc[1], c & 31);
-        const float wt = c < nc ? (c < 32 ? w0 : w1) : 0.f;
-        acc[0] += wt * u[j][0].x; acc[1] += wt * u[j][0].y; acc[2] += wt * u[j][0].z; acc[3] += wt * u[j][0].w;
-        acc[4] += wt * u[j][1].x; acc[5] += wt * u[j][1].y; acc[6] += wt * u[j][1].z; acc[7] += wt * u[j][1].w;
-      }
-    }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    uint32_t wv[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-      wv[i] = *reinterpret_cast<uint32_t*>(&b);
-    }
-    uint16_t* dst = a.out + (static_cast<int64_t>(row) * a.num_q_heads + g * G + h) * 256 + lane * 8;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-  }
 }
 
 // Mixed-precision multiply-add with fp32 accumulation (sm_100+): d = a * b + c
@@ -283,8 +162,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
   constexpr int kTok = T::kTok;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  CtaSmem& cta = *reinterpret_cast<CtaSmem*>(smem_raw);
-  WarpSmem& sm = cta.warp[warp];
+  WarpSmem& sm = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
   if (lane == 0) {
 #pragma unroll
     for (int i = 0; i < kStages; ++i) mbar_init(&sm.bar[i], 1);
@@ -293,20 +171,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
   __syncwarp();
   pdl_wait();
   pdl_trigger();
-  plan_in_smem<T>(a, cta);
-  const int32_t* ubase = cta.ubase;
-  const int total_units = ubase[a.batch];
-  const bool run = total_units <= a.max_units;
-  if (!run) {
-    // nothing will be computed: status, and zero the decode rows this CTA owns
-    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.status, GW_DEV_WORKSPACE);
-    for (int s2 = blockIdx.x; s2 < a.batch; s2 += gridDim.x) {
-      if (a.cu_q_rows[s2 + 1] - a.cu_q_rows[s2] != 1) continue;
-      uint4* row = reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(a.cu_q_rows[s2]) * a.num_q_heads * 256);
-      for (int i = threadIdx.x; i < a.num_q_heads * 32; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
-    }
-  }
-  int32_t* counters = a.counter;  // [0] unit claims, [1] barrier arrivals, [2] exits
+  const int total_units = a.unit_base[a.batch];
+  if (total_units > a.max_units) return;
   const uint64_t pol = policy_evict_first();
   const int64_t head_bytes = 2LL * kPage * 256 * T::kEs;  // K + V of one KV head in one page
   const int perm = (lane >> (5 - T::kLevels)) & (kTok - 1);
@@ -317,12 +183,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
   uint32_t issued = 0, consumed = 0;
 
   auto grab = [&](int slot) -> bool {
-    if (!run) return false;
     int u = 0;
-    if (lane == 0) u = atomicAdd(&counters[0], 1);
+    if (lane == 0) u = atomicAdd(a.counter, 1);
     u = __shfl_sync(0xffffffffu, u, 0);
     if (u >= total_units) return false;
-    const Unit d = decode_unit<T>(a, ubase, u);
+    const Unit d = decode_unit<T>(a, u);
     if (lane == 0) sm.ring[slot] = d;
     __syncwarp();
     return true;
@@ -382,10 +247,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
     }
     const int st = consumed % kStages;
     if (!mbar_wait(&sm.bar[st], (consumed / kStages) & 1, a.status)) {
-      // abandon: drain whatever is still in flight (bounded), then join the
-      // grid barrier below like everyone else
+      // abandon: drain whatever is still in flight (bounded) and leave
       for (uint32_t k = consumed + 1; k < issued; ++k) mbar_wait(&sm.bar[k % kStages], (k / kStages) & 1, nullptr);
-      break;
+      return;
     }
     const uint8_t* Ks = sm.stage[st];
     const uint8_t* Vs = Ks + kStageBytes / 2;
@@ -472,59 +336,20 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
     }
     while (!f_done && issued - consumed < kStages) issue();
   }
-
-  // ---- grid-wide barrier: every unit's partial is written (all CTAs are
-  // resident: one per SM, grid = SM count), then the CTAs merge the
-  // (sequence, KV head) pairs in parallel, reading the partials from L2.
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&counters[1], 1);
-    const uint64_t t0 = global_ns();
-    while (true) {
-      int arrived;
-      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(arrived) : "l"(&counters[1]) : "memory");
-      if (arrived >= static_cast<int>(gridDim.x)) break;
-      if (global_ns() - t0 > kWaitNs) {
-        set_status(a.status, GW_DEV_TIMEOUT);
-        break;
-      }
-      __nanosleep(64);
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  if (run) {
-    const int pairs = a.batch * a.kv_heads;
-    for (int pr = blockIdx.x * kWarps + warp; pr < pairs; pr += gridDim.x * kWarps) {
-      const int s2 = pr / a.kv_heads, g = pr % a.kv_heads;
-      const int nu = ubase[s2 + 1] - ubase[s2];
-      if (nu == 0) continue;
-      const int nc = nu / a.kv_heads;
-      merge_pair<G>(a, static_cast<int64_t>(ubase[s2]) + static_cast<int64_t>(g) * nc, nc, a.cu_q_rows[s2], g, lane);
-    }
-  }
-  // ---- the last CTA out returns the counters to zero for the next call
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(&counters[2], 1) == static_cast<int>(gridDim.x) - 1) {
-      counters[0] = 0;
-      counters[1] = 0;
-      counters[2] = 0;
-      __threadfence();
-    }
-  }
 }
 
 template <int DT, int G>
 cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   using T = Traits<DT>;
-  const size_t smem = sizeof(CtaSmem);
-  auto kern = local_decode_kernel<DT, G>;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
+  cudaError_t e = launch_plan(a, kSplitLocal, T::kChunk, st);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(num_sms()), dim3(kWarps * 32), smem, st, a);
+  const size_t smem = sizeof(WarpSmem) * kWarps;
+  auto kern = local_decode_kernel<DT, G>;
+  e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(kern, dim3(num_sms()), dim3(kWarps * 32), smem, st, a);
+  if (e != cudaSuccess) return e;
+  return launch_combine(a, kSplitLocal, G, 256, T::kChunk, st);
 }
 
 template <int DT>

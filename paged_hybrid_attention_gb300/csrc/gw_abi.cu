@@ -193,10 +193,6 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
   const int group = num_q_heads / pool->kv_heads;
   if (local && group != 1 && group != 2 && group != 4 && group != 8)
     return fail(GW_ERR_UNSUPPORTED, fn, "query heads per KV head must be 1, 2, 4 or 8 (got %d)", group);
-  if (local && batch > kLocalMaxBatch)
-    return fail(GW_ERR_UNSUPPORTED, fn, "batch %d exceeds %d sequences per call", batch, kLocalMaxBatch);
-  if (local && max_q_rows > 1 && pool->dtype != GW_KV_BF16)
-    return fail(GW_ERR_UNSUPPORTED, fn, "prompt rows (max_q_rows > 1) need a bf16 pool");
   if (!local && num_q_heads != 8 && num_q_heads != 16 && num_q_heads != 32)
     return fail(GW_ERR_UNSUPPORTED, fn, "num_q_heads must be 8, 16 or 32 (got %d)", num_q_heads);
   if (local && window < 1) return fail(GW_ERR_INVALID_ARG, fn, "window must be >= 1");

@@ -22,9 +22,6 @@ constexpr int kLocalChunkPagesE4m3 = 8;
 constexpr int kGlobalChunkPagesMin = 16;
 constexpr int kGlobalMaxChunks = 128;
 
-// Sequences per local decode call (the split plan lives in shared memory).
-constexpr int kLocalMaxBatch = 4096;
-
 constexpr int kSplitLocal = 0;
 constexpr int kSplitGlobal = 1;
 
@@ -47,8 +44,7 @@ __host__ __device__ __forceinline__ int global_chunks(int L) {
 }
 
 // Workspace layout (offsets from the 256-byte aligned workspace base):
-//   [0, 256)          int32 counters: [0] unit claims, [1] grid-barrier
-//                     arrivals, [2] exits (zero between calls)
+//   [0, 256)          int32 work counter (+ padding)
 //   [256, ub_end)     int32 unit_base[batch + 1], rounded up to 256 bytes
 //   [ub_end, ml_end)  float2 (m, l) per (unit, head of the unit)
 //   [ml_end, o_end)   float  o[unit][head of the unit][head_dim]

@@ -81,9 +81,6 @@ __global__ void combine_kernel(const LocalArgs a, int mode, int G, int chunk) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= a.num_q_heads * kQ) return;
   const int h = idx / kQ, d4 = idx % kQ;
-  // every decode kernel has finished claiming units: return the shared claim
-  // counter to zero (the local kernel relies on it between calls)
-  if (s == 0 && idx == 0) *a.counter = 0;
   const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
   if (n != 1) return;
   const int L = a.seq_lens[s];

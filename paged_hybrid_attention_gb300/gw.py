@@ -151,9 +151,8 @@ def workspace_bytes(pool, num_q_heads, batch, max_pages_per_seq, max_q_rows=1, w
 
 
 def alloc_workspace(pool, num_q_heads, batch, max_pages_per_seq, max_q_rows=1, window=1024, device="cuda"):
-    """Zero-filled, 256-byte aligned workspace (the ABI requires zeros before first use)."""
     n = workspace_bytes(pool, num_q_heads, batch, max_pages_per_seq, max_q_rows, window)
-    buf = torch.zeros(n + 256, dtype=torch.uint8, device=device)
+    buf = torch.empty(n + 256, dtype=torch.uint8, device=device)
     off = (-buf.data_ptr()) % 256
     return buf[off:off + n]
 
