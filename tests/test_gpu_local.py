@@ -180,3 +180,37 @@ def test_local_garbage_outside_window_is_ignored():
     assert torch.isfinite(out.float()).all()
     ref = H.build_pool(layer, tab.numpy())
     _compare(layer, out, ref, range(layer.B))
+
+
+def test_workspace_shared_by_consecutive_calls_bitwise():
+    """One workspace serves local, global and local calls in turn."""
+    sp = synth.spec("serving")
+    sub = synth.custom("ws", sp.seed, sp.num_q_heads, sp.lens[:5], sp.n_rows[:5], sp.families)
+    loc = synth.Layer(sub, "local")
+    glo = synth.Layer(sub, "global", layer=7)
+    pools = []
+    for layer in (loc, glo):
+        fam = layer.fam
+        tab = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sub.lens)) + 1).cuda()
+        pool = G.new_pool(layer)
+        G.append(layer, pool, tab)
+        pools.append(pool)
+    ref_l = G.attend(loc, pools[0])
+    ref_g = G.attend(glo, pools[1])
+    nbytes = max(gw.workspace_bytes(pools[0], 32, 5, loc.block_table.shape[1], 1, 1024),
+                 gw.workspace_bytes(pools[1], 32, 5, glo.block_table.shape[1], 1, 1))
+    ws = torch.empty(nbytes + 256, dtype=torch.uint8, device="cuda").fill_(0x77)   # no zero-fill needed
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + nbytes]
+    qs = [G.bits_to_cuda_bf16(l.queries()) for l in (loc, glo)]
+    for it in range(3):
+        for k, (layer, pool) in enumerate(zip((loc, glo), pools)):
+            out = torch.empty_like(qs[k])
+            args = (pool, qs[k], out, G.i32(layer.cu_rows()), G.i32(sub.lens), G.i32(layer.block_table), ws)
+            if k == 0:
+                gw.decode_attn_local(*args, 1024)
+            else:
+                gw.decode_attn_global(*args)
+            torch.cuda.synchronize()
+            ref = ref_l if k == 0 else ref_g
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), (it, k)
