@@ -276,15 +276,57 @@ def oracle_sample(name, budget_s):
 
 
 # --------------------------------------------------------------------------- main
+class Ranks:
+    """The ranks of one run (torchrun environment: RANK, LOCAL_RANK,
+    WORLD_SIZE, MASTER_ADDR/PORT).  Weak scaling: every rank serves its own
+    independent batch of sequences, so the data path has no collective; the
+    process group only brackets the timed region (barrier) and reduces the
+    per-rank figures on the host side of the measurement."""
+
+    def __init__(self, backend):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.backend = backend
+        self.device = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend)
+
+    def barrier(self):
+        if self.world > 1:
+            torch.distributed.barrier()
+
+    def _reduce(self, x, op):
+        if self.world == 1:
+            return float(x)
+        dev = self.device if self.backend == "nccl" else torch.device("cpu")
+        t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=op)
+        return float(t.item())
+
+    def max(self, x):
+        return self._reduce(x, torch.distributed.ReduceOp.MAX if self.world > 1 else None)
+
+    def sum(self, x):
+        return self._reduce(x, torch.distributed.ReduceOp.SUM if self.world > 1 else None)
+
+    def throughput(self, step_bytes, ms):
+        """Whole-job GB/s: the bytes every rank's step read, over the slowest
+        rank's time per step."""
+        return self.sum(step_bytes) / (self.max(ms) * 1e-3) / 1e9
+
+    def close(self):
+        if self.world > 1:
+            torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse()
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     peak, peak_kind, _ = peaks()
 
     if args.impl == "reference":
-        if rank != 0:
+        if int(os.environ.get("RANK", "0")) != 0:
             return
         ref_steps = []
         desc = ""
@@ -301,12 +343,11 @@ def main():
         print(json.dumps(line))
         return
 
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-        torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    ranks = Ranks("nccl")
+    world, rank = ranks.world, ranks.rank
+    dev = torch.device("cuda", ranks.local_rank if world > 1 else 0)
     torch.cuda.set_device(dev)
+    ranks.device = dev
     from paged_hybrid_attention_gb300 import gw
 
     sp, layers = workload_layers(args.workload, rank)
@@ -320,10 +361,6 @@ def main():
     dom_name = "local decode attention call (plan + split-KV decode + combine)" if locals_ else \
         "global decode attention call (plan + tcgen05 decode + combine)"
     dom_bytes = statistics.mean(g.kv_bytes for g in dom)
-
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
 
     def step():
         for g in glayers:
@@ -353,7 +390,7 @@ def main():
     # ---- device-timed region: K steps (CUDA-graph replays unless --eager)
     K = args.steps
     clocks = ClockSampler(dev.index)
-    barrier()
+    ranks.barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
@@ -368,12 +405,10 @@ def main():
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    barrier()
-    ms = t0.elapsed_time(t1) / K
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ranks.barrier()
+    ms_rank = t0.elapsed_time(t1) / K
+    ms = ranks.max(ms_rank)
+    value = ranks.throughput(step_bytes, ms_rank)
     status = int(sum(int(g.status.item()) for g in glayers))
 
     # ---- dominant call: CUDA events around each call over eager steps
@@ -397,7 +432,7 @@ def main():
                 g.run(gw, stream)
                 g.download()
         torch.cuda.synchronize()
-        barrier()
+        ranks.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -408,17 +443,14 @@ def main():
                 g.download()
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / K
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e_rank = e0.elapsed_time(e1) / K
+        e2e_ms = ranks.max(e2e_rank)
+        e2e = {"value": ranks.throughput(step_bytes, e2e_rank), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     if rank != 0:
+        ranks.close()
         return
-    value = world * step_bytes / (ms * 1e-3) / 1e9
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     src = os.path.join(ROOT, "paged_hybrid_attention_gb300", "csrc", "attn_local.cu")
     traffic = None
@@ -453,6 +485,7 @@ def main():
         "device_status": status,
     }
     print(json.dumps(line))
+    ranks.close()
 
 
 if __name__ == "__main__":
