@@ -173,9 +173,10 @@ gw_status gw_kv_append(const gw_kv_pool* pool, const void* k, const void* v, int
  *   max_q_rows   host bound on n_b (1 for a pure decode step).
  *   window       >= 1 (1024 for the served model).
  *   workspace    device scratch of at least gw_attn_workspace_bytes(...),
- *                16-byte aligned; contents need no initialisation.
+ *                256-byte aligned; contents need no initialisation.
  * Errors: GW_ERR_INVALID_ARG, GW_ERR_WORKSPACE, GW_ERR_UNSUPPORTED
- * (num_q_heads / kv_heads not in {1,2,4,8}), GW_ERR_CUDA.
+ * (num_q_heads / kv_heads not in {1,2,4,8}, or batch > 4096: the decode
+ * kernel keeps the batch's split plan in shared memory), GW_ERR_CUDA.
  */
 gw_status gw_decode_attn_local(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,
                                int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,

@@ -8,14 +8,18 @@
 // e4m3 at scale 1.0; here it is widened to fp32 on the load path.
 //
 // Design (split-KV flash decoding on CUDA cores; a GQA group of G <= 8 query
-// heads per KV head is too narrow for a tensor-core contraction):
+// heads per KV head is too narrow for a tensor-core contraction, and the
+// kernel is bound by HBM, not by arithmetic):
 //   * Work unit = (sequence, KV head, chunk of up to 4 bf16 / 8 e4m3 pages of
-//     the window).  A plan kernel turns lengths into unit offsets; the split
-//     depends on the sequence's own length only.
-//   * Persistent CTAs, one per SM, of 8 independent warps.  Each warp takes
-//     units from an atomic counter and streams 8 KiB stages (8 tokens of K and
-//     V for bf16, 16 for e4m3) with cp.async.bulk into a private 3-stage ring,
-//     prefetching across unit boundaries.
+//     the window).  The split depends on the sequence's own length only.
+//   * Persistent CTAs, one per SM, of 8 independent warps.  Every CTA
+//     computes the batch's split plan (unit offsets) into its own shared
+//     memory, so no plan kernel and no work counter sit in front of the
+//     decode; units are dealt round-robin over the warps, SM-minor, so each
+//     round spreads evenly over the SMs.
+//   * Each warp streams 8 KiB stages (8 tokens of K and V for bf16, 16 for
+//     e4m3) with cp.async.bulk into a private 2-stage ring, prefetching
+//     across unit boundaries.
 //   * Lane l owns head dims [8l, 8l+8).  q.K partial dot products are reduced
 //     across lanes with a transpose-reduction whose token order is permuted by
 //     lane bits, so every level is one shuffle + add per value (no selects).
@@ -32,7 +36,7 @@ namespace gw {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kStageBytes = 8192;
 constexpr int kRing = kStages + 2;
 
@@ -59,11 +63,11 @@ struct Traits {
 };
 
 template <class T>
-__device__ __forceinline__ Unit decode_unit(const LocalArgs& a, int u) {
+__device__ __forceinline__ Unit decode_unit(const LocalArgs& a, const int32_t* ub, int u) {
   int lo = 0, hi = a.batch;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (a.unit_base[mid] <= u) lo = mid; else hi = mid - 1;
+    if (ub[mid] <= u) lo = mid; else hi = mid - 1;
   }
   Unit d;
   d.s = lo;
@@ -71,7 +75,7 @@ __device__ __forceinline__ Unit decode_unit(const LocalArgs& a, int u) {
   const int first = L > a.window ? L - a.window : 0;
   const int p0 = first / kPage, p1 = (L - 1) / kPage;
   const int nc = (p1 - p0 + T::kChunk) / T::kChunk;
-  const int r = u - a.unit_base[lo];
+  const int r = u - ub[lo];
   d.g = r / nc;
   const int c = r % nc;
   const int lpa = p0 + c * T::kChunk;
@@ -156,6 +160,60 @@ __device__ __forceinline__ void xreduce(float* x) {
   }
 }
 
+// The split plan of the batch, computed by every CTA into its own shared
+// memory: ub[s] = units of the decode-row sequences before s (ub[batch] =
+// total).  CTA 0 also stores it to the workspace for the combine kernel.
+template <int kChunk>
+__device__ void plan_in_smem(const LocalArgs& a, int32_t* ub, int32_t* scratch) {
+  const int nt = blockDim.x, t = threadIdx.x;
+  const int per = (a.batch + nt - 1) / nt;
+  const int s0 = min(a.batch, t * per), s1 = min(a.batch, s0 + per);
+  int mine = 0;
+  for (int s = s0; s < s1; ++s) {
+    const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
+    const int L = a.seq_lens[s];
+    int units = 0;
+    if (n == 1) {
+      if (L >= 1 && static_cast<int64_t>(L) <= static_cast<int64_t>(a.max_pages) * kPage)
+        units = a.kv_heads * local_chunks(L, a.window, kChunk);
+      else if (blockIdx.x == 0)
+        set_status(a.status, GW_DEV_LEN_RANGE);
+    }
+    ub[s] = units;  // per-sequence count for now
+    mine += units;
+  }
+  // exclusive scan of the per-thread sums
+  const int lane = t & 31, w = t >> 5;
+  int x = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int v = lane < (nt >> 5) ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane < (nt >> 5)) scratch[lane] = v;
+  }
+  __syncthreads();
+  int run = (w > 0 ? scratch[w - 1] : 0) + x - mine;
+  for (int s = s0; s < s1; ++s) {
+    const int c = ub[s];
+    ub[s] = run;
+    run += c;
+  }
+  if (t == nt - 1) ub[a.batch] = run;
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int s = t; s <= a.batch; s += nt) a.unit_base[s] = ub[s];
+}
+
 template <int DT, int G>
 __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const LocalArgs a) {
   using T = Traits<DT>;
@@ -168,12 +226,20 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
     for (int i = 0; i < kStages; ++i) mbar_init(&sm.bar[i], 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  int32_t* ub = reinterpret_cast<int32_t*>(smem_raw + sizeof(WarpSmem) * kWarps);
   pdl_wait();
   pdl_trigger();
-  const int total_units = a.unit_base[a.batch];
-  if (total_units > a.max_units) return;
+  plan_in_smem<T::kChunk>(a, ub, ub + kLocalMaxBatch + 1);
+  const int total_units = ub[a.batch];
+  if (total_units > a.max_units) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.status, GW_DEV_WORKSPACE);
+    return;
+  }
   const uint64_t pol = policy_evict_first();
+  // units are dealt round-robin over the warps, SM-minor, so every SM gets
+  // an equal share of each round
+  const int n_warps = gridDim.x * kWarps;
+  int next_u = warp * gridDim.x + blockIdx.x;
   const int64_t head_bytes = 2LL * kPage * 256 * T::kEs;  // K + V of one KV head in one page
   const int perm = (lane >> (5 - T::kLevels)) & (kTok - 1);
   const bool canon = (lane & ((1 << (5 - T::kLevels)) - 1)) == 0;
@@ -183,11 +249,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
   uint32_t issued = 0, consumed = 0;
 
   auto grab = [&](int slot) -> bool {
-    int u = 0;
-    if (lane == 0) u = atomicAdd(a.counter, 1);
-    u = __shfl_sync(0xffffffffu, u, 0);
+    const int u = next_u;
+    next_u += n_warps;
     if (u >= total_units) return false;
-    const Unit d = decode_unit<T>(a, u);
+    const Unit d = decode_unit<T>(a, ub, u);
     if (lane == 0) sm.ring[slot] = d;
     __syncwarp();
     return true;
@@ -341,9 +406,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const Loca
 template <int DT, int G>
 cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   using T = Traits<DT>;
-  cudaError_t e = launch_plan(a, kSplitLocal, T::kChunk, st);
-  if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(WarpSmem) * kWarps;
+  cudaError_t e;
+  const size_t smem = sizeof(WarpSmem) * kWarps + sizeof(int32_t) * (kLocalMaxBatch + 1 + 32);
   auto kern = local_decode_kernel<DT, G>;
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;

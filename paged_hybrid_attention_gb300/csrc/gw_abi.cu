@@ -196,6 +196,8 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
   if (!local && num_q_heads != 8 && num_q_heads != 16 && num_q_heads != 32)
     return fail(GW_ERR_UNSUPPORTED, fn, "num_q_heads must be 8, 16 or 32 (got %d)", num_q_heads);
   if (local && window < 1) return fail(GW_ERR_INVALID_ARG, fn, "window must be >= 1");
+  if (local && batch > kLocalMaxBatch)
+    return fail(GW_ERR_UNSUPPORTED, fn, "batch (%d) exceeds %d sequences per call", batch, kLocalMaxBatch);
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(GW_ERR_INVALID_ARG, fn, "scale must be finite and > 0");
   if (max_pages_per_seq < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_pages_per_seq must be >= 1");
   if (max_q_rows < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_q_rows must be >= 1");

@@ -22,6 +22,9 @@ constexpr int kLocalChunkPagesE4m3 = 8;
 constexpr int kGlobalChunkPagesMin = 16;
 constexpr int kGlobalMaxChunks = 128;
 
+// Local decode keeps the batch's split plan in shared memory.
+constexpr int kLocalMaxBatch = 4096;
+
 constexpr int kSplitLocal = 0;
 constexpr int kSplitGlobal = 1;
 

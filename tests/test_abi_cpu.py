@@ -84,6 +84,8 @@ def test_attention_host_validation():
     assert _local_call(d, ws_bytes=100) == gw.GW_ERR_WORKSPACE
     assert "workspace_bytes" in gw.last_error()
     assert _local_call(d, batch=0) == gw.GW_OK                        # empty batch: nothing to do
+    assert _local_call(d, batch=4097) == gw.GW_ERR_UNSUPPORTED        # split plan lives in shared memory
+    assert "4096" in gw.last_error()
     g = _desc(gw.LAYOUT_GLOBAL_FOLDED, kvh=1, hd=512, rd=128)
     assert _local_call(g) == gw.GW_ERR_INVALID_ARG                    # global pool on the local entry
     L = gw.lib()
