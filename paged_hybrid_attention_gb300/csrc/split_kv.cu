@@ -70,39 +70,64 @@ __global__ void plan_kernel(const LocalArgs a, int mode, int chunk) {
   }
 }
 
-// One thread per (sequence, q head, 4 dims): merges that head's partials of
-// the sequence in chunk order (log-sum-exp, base 2) and writes bf16.
+// One warp per (sequence, q head, 128-dim slice); lane l owns 4 dims of the
+// slice.  The (m, l) of chunks lane, lane + 32, ... give the warp maximum M
+// while the first batch of kB chunks' partials is already being fetched; then
+// every lane sums w_c * o_c over its dims in chunk order, kB chunks' loads in
+// flight at a time.  The result is written as bf16.
 template <int D>
 __global__ void combine_kernel(const LocalArgs a, int mode, int G, int chunk) {
+  constexpr int kSlices = D / 128;
+  constexpr int kB = 16;  // chunks per batch
   pdl_wait();
   pdl_trigger();
-  constexpr int kQ = D / 4;
-  const int s = blockIdx.y;
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= a.num_q_heads * kQ) return;
-  const int h = idx / kQ, d4 = idx % kQ;
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (wid >= static_cast<int64_t>(a.batch) * a.num_q_heads * kSlices) return;
+  const int slice = static_cast<int>(wid % kSlices);
+  const int64_t sh = wid / kSlices;
+  const int s = static_cast<int>(sh / a.num_q_heads), h = static_cast<int>(sh % a.num_q_heads);
   const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
   if (n != 1) return;
   const int L = a.seq_lens[s];
+  const int dim0 = slice * 128 + lane * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
   if (len_ok(a, L, 1) && a.unit_base[a.batch] <= a.max_units) {
     const int nc = mode == kSplitLocal ? local_chunks(L, a.window, chunk) : global_chunks(L);
     const int g = h / G, hh = h % G;
     const int64_t ub = a.unit_base[s] + static_cast<int64_t>(g) * nc;
+    float4 u[kB];
+    float2 ml[kB];
+    auto fetch = [&](int c0) {
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        if (c0 + b < nc) {
+          const int64_t row = (ub + c0 + b) * G + hh;
+          ml[b] = a.part_ml[row];
+          u[b] = *reinterpret_cast<const float4*>(a.part_o + row * D + dim0);
+        }
+      }
+    };
+    fetch(0);
     float M = -INFINITY;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, a.part_ml[(ub + c) * G + hh].x);
+    for (int c = lane; c < nc; c += 32) M = fmaxf(M, a.part_ml[(ub + c) * G + hh].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     if (M != -INFINITY) {
-#pragma unroll 4
-      for (int c = 0; c < nc; ++c) {
-        const float2 ml = a.part_ml[(ub + c) * G + hh];
-        const float wgt = ex2(ml.x - M);
-        den += wgt * ml.y;
-        const float4 u = *reinterpret_cast<const float4*>(a.part_o + ((ub + c) * G + hh) * D + d4 * 4);
-        acc.x += wgt * u.x;
-        acc.y += wgt * u.y;
-        acc.z += wgt * u.z;
-        acc.w += wgt * u.w;
+      for (int c0 = 0; c0 < nc; c0 += kB) {
+        if (c0 > 0) fetch(c0);
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+          if (c0 + b < nc) {
+            const float wgt = ex2(ml[b].x - M);
+            den += wgt * ml[b].y;
+            acc.x += wgt * u[b].x;
+            acc.y += wgt * u[b].y;
+            acc.z += wgt * u[b].z;
+            acc.w += wgt * u[b].w;
+          }
+        }
       }
     }
   }
@@ -112,7 +137,7 @@ __global__ void combine_kernel(const LocalArgs a, int mode, int G, int chunk) {
   uint2 w;
   w.x = *reinterpret_cast<uint32_t*>(&lo);
   w.y = *reinterpret_cast<uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(a.cu_q_rows[s]) * a.num_q_heads + h) * D + d4 * 4) = w;
+  *reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(a.cu_q_rows[s]) * a.num_q_heads + h) * D + dim0) = w;
 }
 
 }  // namespace
@@ -123,8 +148,8 @@ cudaError_t launch_plan(const LocalArgs& a, int mode, int chunk, cudaStream_t st
 
 cudaError_t launch_combine(const LocalArgs& a, int mode, int heads_per_unit, int head_dim, int chunk,
                            cudaStream_t st) {
-  const int threads = a.num_q_heads * head_dim / 4;
-  const dim3 grid((threads + 255) / 256, a.batch);
+  const int64_t warps = static_cast<int64_t>(a.batch) * a.num_q_heads * (head_dim / 128);
+  const dim3 grid(static_cast<unsigned>((warps + 7) / 8));
   if (head_dim == 256) return launch_pdl(combine_kernel<256>, grid, dim3(256), 0, st, a, mode, heads_per_unit, chunk);
   return launch_pdl(combine_kernel<512>, grid, dim3(256), 0, st, a, mode, heads_per_unit, chunk);
 }
