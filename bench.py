@@ -12,8 +12,10 @@ KV heads hd256, window 1024, bf16; global one KV head hd512, folded V + k_rot.
 Printed: ONE JSON line (rank 0) with value = algorithmic KV GB/s of the whole
 step (KV bytes the method must read / device time), steps/s, a roofline
 object for the dominant call (the local attention call), an e2e number through
-the C ABI with host buffers, the oracle timed on host cores (cpu_baseline),
-clock samples and kernel launch counts.
+the C ABI with host buffers (every step uploads its inputs from one pinned
+host buffer and downloads its outputs into another, one copy each), the
+oracle timed on host cores (cpu_baseline), clock samples and kernel launch
+counts.
 
 --impl reference times the float64 CPU oracle (the reference arm) on a
 bounded sample of the same workload.
@@ -61,6 +63,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch every step eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-probe", action="store_true", help="skip the gw_bw_probe read-ceiling measurement")
     return ap.parse_args()
 
 
@@ -139,10 +142,6 @@ class GpuLayer:
         self.ws = gw.alloc_workspace(self.pool, sp.num_q_heads, len(sp.lens), self.bt.shape[1], self.max_q_rows,
                                      max(1, fam.window), device=dev)
         self.kv_bytes = kv_bytes(layer)
-        # pinned host copies for the end-to-end leg
-        self.host_in = {k: getattr(self, k).cpu().pin_memory() for k in
-                        ("q", "k_new", "v_new", "slot_new", "pos_new", "cu", "lens", "bt")}
-        self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
 
     def _append_random(self, gw, gen, dev, slot, pos, sig, chunk=1 << 18):
         fam = self.fam
@@ -155,9 +154,6 @@ class GpuLayer:
             k = (torch.randn(*shape, generator=gen, device=dev) * sig).to(torch.bfloat16) \
                 if fam.kind == "local" else v
             gw.kv_append(self.pool, k, v, s_, p_, self.table, self.status)
-
-    def in_bytes(self):
-        return sum(t.numel() * t.element_size() for t in self.host_in.values())
 
     def run(self, gw, stream, ev=None):
         gw.kv_append(self.pool, self.k_new, self.v_new, self.slot_new, self.pos_new, self.table, self.status, stream)
@@ -172,12 +168,34 @@ class GpuLayer:
         if ev is not None:
             ev[1].record(stream)
 
-    def upload(self, stream):
-        for k, h in self.host_in.items():
-            getattr(self, k).copy_(h, non_blocking=True)
+    INPUTS = ("q", "k_new", "v_new", "slot_new", "pos_new", "cu", "lens", "bt")
+
+
+class Arena:
+    """One device buffer holding the named tensors of every layer (256-byte
+    aligned views), mirrored by one pinned host buffer: a step's inputs go up
+    in one copy and its outputs come back in one."""
+
+    def __init__(self, glayers, names, dev):
+        items, off = [], 0
+        for g in glayers:
+            for n in names:
+                t = getattr(g, n)
+                items.append((g, n, t, off))
+                off += -(-t.numel() * t.element_size() // 256) * 256
+        self.nbytes = off
+        self.dev = torch.empty(off, dtype=torch.uint8, device=dev)
+        for g, n, t, o in items:
+            view = self.dev[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            setattr(g, n, view)
+        self.host = self.dev.cpu().pin_memory()
+
+    def upload(self):
+        self.dev.copy_(self.host, non_blocking=True)
 
     def download(self):
-        self.host_out.copy_(self.out, non_blocking=True)
+        self.host.copy_(self.dev, non_blocking=True)
 
 
 # --------------------------------------------------------------------------- clocks
@@ -353,12 +371,14 @@ def main():
     sp, layers = workload_layers(args.workload, rank)
     gen = torch.Generator(device=dev).manual_seed(sp.seed + 17 * rank)
     glayers = [GpuLayer(l, gw, gen, dev) for l in layers]
+    arena_in = Arena(glayers, GpuLayer.INPUTS, dev)   # the step's inputs, one upload
+    arena_out = Arena(glayers, ("out",), dev)         # the step's outputs, one download
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     step_bytes = sum(g.kv_bytes for g in glayers)
     locals_ = [g for g in glayers if g.fam.kind == "local"]
     dom = locals_ if locals_ else glayers
-    dom_name = "local decode attention call (plan + split-KV decode + combine)" if locals_ else \
+    dom_name = "local decode attention call (split-KV decode + combine)" if locals_ else \
         "global decode attention call (plan + tcgen05 decode + combine)"
     dom_bytes = statistics.mean(g.kv_bytes for g in dom)
 
@@ -421,26 +441,42 @@ def main():
     torch.cuda.synchronize()
     dom_ms = statistics.mean(e0.elapsed_time(e1) for g in dom for e0, e1 in evs[id(g)])
 
+    # ---- read ceiling of the decode kernels' copy pipeline (gw_bw_probe, 4 GiB)
+    read_gbs = None
+    if not args.no_probe:
+        probe_buf = torch.ones(4 << 30, dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            gw.bw_probe(probe_buf, stream=stream)
+        probe_ms = []
+        for _ in range(5):
+            p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            p0.record(stream)
+            gw.bw_probe(probe_buf, stream=stream)
+            p1.record(stream)
+            torch.cuda.synchronize()
+            probe_ms.append(p0.elapsed_time(p1))
+        read_gbs = probe_buf.numel() / (min(probe_ms) * 1e-3) / 1e9
+        del probe_buf
+
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        h2d = sum(g.in_bytes() for g in glayers)
-        d2h = sum(g.host_out.numel() * g.host_out.element_size() for g in glayers)
+        h2d, d2h = arena_in.nbytes, arena_out.nbytes
         for _ in range(2):
+            arena_in.upload()
             for g in glayers:
-                g.upload(stream)
                 g.run(gw, stream)
-                g.download()
+            arena_out.download()
         torch.cuda.synchronize()
         ranks.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(K):
+            arena_in.upload()
             for g in glayers:
-                g.upload(stream)
                 g.run(gw, stream)
-                g.download()
+            arena_out.download()
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_rank = e0.elapsed_time(e1) / K
@@ -463,7 +499,10 @@ def main():
     if not args.no_cpu:
         gbs, desc, _ = oracle_sample(args.workload, budget_s=12.0)
         cpu = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
-    launches_per_step = sum(1 + 3 + (1 if g.max_q_rows > 1 else 0) for g in glayers)
+    # gw kernels per layer: append; local = decode + combine, global = plan + decode
+    # + combine; prompt rows add a tile plan and the prompt kernel
+    launches_per_step = sum(1 + (2 if g.fam.kind == "local" else 3) + (2 if g.max_q_rows > 1 else 0)
+                            for g in glayers)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms, "steps_per_s": 1000.0 / ms, "higher_is_better": True, "scaling": "weak",
@@ -477,7 +516,12 @@ def main():
         "roofline": {"kernel": dom_name + ", CUDA events around each call, %d eager steps" % K2,
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                     "frac_of_read_probe": achieved / read_gbs if read_gbs else None,
+                     "frac_of_nominal_8000": achieved / 8000.0,
                      "algorithmic_bytes_per_launch": dom_bytes, "ms_per_launch": dom_ms},
+        "bw_probe": None if read_gbs is None else {"read_gbs": read_gbs, "bytes": 4 << 30,
+                     "what": "gw_bw_probe: 4 GiB streamed through the local decode copy pipeline "
+                             "(8 warps x 2-stage 8 KiB rings per SM), no arithmetic; best of 5"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,

@@ -227,8 +227,8 @@ size_t gw_attn_workspace_bytes(const gw_kv_pool* pool, int32_t num_q_heads, int3
  * before any stream capture.  All calls share the one array and it keeps the
  * last call's contents (each call re-initialises what it needs), so calls
  * whose executions overlap on the GPU (different streams without ordering)
- * race on it.  Sequences with more than one query row are not supported here
- * any more than on gw_decode_attn_local today.
+ * race on it.  Sequences with more than one query row (prompt rows of a mixed
+ * step) are served as by gw_decode_attn_local, within the same 32 MiB.
  */
 gw_status gw_decode_attn_local_noalloc(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,
                                        int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,
@@ -237,6 +237,22 @@ gw_status gw_decode_attn_local_noalloc(const gw_kv_pool* pool, const void* q, vo
 
 /* Bytes of the static scratch behind gw_decode_attn_local_noalloc. */
 size_t gw_noalloc_scratch_bytes(void);
+
+/*
+ * gw_bw_probe - a measurement aid, not part of the method: streams the first
+ * floor(bytes / 8192) * 8192 bytes of the device buffer `buf` through the
+ * copy pipeline of the local decode kernel (one CTA per SM, 8 warps, each
+ * with a 2-stage ring of 8 KiB shared-memory stages filled by two 4 KiB
+ * cp.async.bulk copies) and discards them, so that its rate is the read
+ * bandwidth that pipeline can reach on the GPU.  The pages this library
+ * follows have no counterpart of this entry point.
+ *   buf          device memory, 16-byte aligned, caller-owned, only read.
+ *   bytes        >= 8192.
+ *   dev_status   optional; GW_DEV_TIMEOUT if a copy never lands.
+ * Errors: GW_ERR_INVALID_ARG (NULL or misaligned buf, bytes < 8192),
+ * GW_ERR_CUDA.  Asynchronous on `stream`.
+ */
+gw_status gw_bw_probe(const void* buf, size_t bytes, int32_t* dev_status, void* stream);
 
 /* Message of the calling thread's last failed call ("" if none). */
 const char* gw_last_error(void);

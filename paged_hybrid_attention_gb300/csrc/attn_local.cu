@@ -12,7 +12,9 @@
 // kernel is bound by HBM, not by arithmetic):
 //   * Work unit = (sequence, KV head, chunk of up to 4 bf16 / 8 e4m3 pages of
 //     the window).  The split depends on the sequence's own length only.
-//   * Persistent CTAs, one per SM, of 8 independent warps.  Every CTA
+//   * Persistent CTAs, one per SM, of independent warps: 8 for bf16, 12 for
+//     e4m3 (which spends twice the instructions per byte on conversions and
+//     is bound by issue latency, so more warps hide more of it).  Every CTA
 //     computes the batch's split plan (unit offsets) into its own shared
 //     memory, so no plan kernel and no work counter sit in front of the
 //     decode; units are dealt round-robin over the warps, SM-minor, so each
@@ -35,16 +37,20 @@
 namespace gw {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kStages = 2;
+// warps per CTA: 8 for bf16; e4m3 spends twice the instructions per byte and
+// is issue-latency bound, so it runs 12 (with 2-stage rings) where the
+// register budget allows (G <= 4)
+template <int DT, int G>
+constexpr int warps_for() { return DT == GW_KV_E4M3 && G <= 4 ? 12 : 8; }
 constexpr int kStageBytes = 8192;
-constexpr int kRing = kStages + 2;
 
 struct Unit {
   int32_t s, g, hp_lo, n, tok_lo, tok_hi, unit, row;
 };
 
+template <int kStages>
 struct __align__(128) WarpSmem {
+  static constexpr int kRing = kStages + 2;
   uint8_t stage[kStages][kStageBytes];
   uint64_t bar[kStages];
   int32_t valid[kStages];
@@ -60,6 +66,8 @@ struct Traits {
   static constexpr int kSpp = kPage / kTok;                   // stages per page: 2 / 1
   static constexpr int kLevels = kTok == 16 ? 4 : 3;          // halving levels of the reduction
   static constexpr int kChunk = DT == GW_KV_BF16 ? kLocalChunkPagesBf16 : kLocalChunkPagesE4m3;
+  static constexpr int kStages = 2;  // copy-ring depth per warp
+  using Smem = WarpSmem<kStages>;
 };
 
 template <class T>
@@ -215,18 +223,20 @@ __device__ void plan_in_smem(const LocalArgs& a, int32_t* ub, int32_t* scratch) 
 }
 
 template <int DT, int G>
-__global__ void __launch_bounds__(kWarps * 32, 1) local_decode_kernel(const LocalArgs a) {
+__global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kernel(const LocalArgs a) {
+  constexpr int kWarps = warps_for<DT, G>();
   using T = Traits<DT>;
   constexpr int kTok = T::kTok;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  WarpSmem& sm = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
+  constexpr int kStages = T::kStages, kRing = T::Smem::kRing;
+  typename T::Smem& sm = reinterpret_cast<typename T::Smem*>(smem_raw)[warp];
   if (lane == 0) {
 #pragma unroll
     for (int i = 0; i < kStages; ++i) mbar_init(&sm.bar[i], 1);
     fence_mbar_init();
   }
-  int32_t* ub = reinterpret_cast<int32_t*>(smem_raw + sizeof(WarpSmem) * kWarps);
+  int32_t* ub = reinterpret_cast<int32_t*>(smem_raw + sizeof(typename T::Smem) * kWarps);
   pdl_wait();
   pdl_trigger();
   plan_in_smem<T::kChunk>(a, ub, ub + kLocalMaxBatch + 1);
@@ -407,7 +417,8 @@ template <int DT, int G>
 cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   using T = Traits<DT>;
   cudaError_t e;
-  const size_t smem = sizeof(WarpSmem) * kWarps + sizeof(int32_t) * (kLocalMaxBatch + 1 + 32);
+  constexpr int kWarps = warps_for<DT, G>();
+  const size_t smem = sizeof(typename T::Smem) * kWarps + sizeof(int32_t) * (kLocalMaxBatch + 1 + 32);
   auto kern = local_decode_kernel<DT, G>;
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;

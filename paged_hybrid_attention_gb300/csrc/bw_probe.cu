@@ -1,0 +1,77 @@
+// gw_bw_probe: the read bandwidth the decode kernels' copy pipeline can reach.
+//
+// Not part of the method: a measurement aid for the roofline.  It streams a
+// buffer through exactly the pipeline shape of the local decode kernel - one
+// persistent CTA per SM, 8 warps, each with a private 2-stage ring of 8 KiB
+// stages filled by two 4 KiB cp.async.bulk copies - and does no arithmetic,
+// so its rate is the ceiling that pipeline can reach on this GPU.
+#include "common.cuh"
+
+namespace gw {
+namespace {
+
+constexpr int kProbeWarps = 8;
+constexpr int kProbeStages = 2;
+constexpr int kProbeStage = 8192;
+
+struct __align__(128) ProbeWarp {
+  uint8_t stage[kProbeStages][kProbeStage];
+  uint64_t bar[kProbeStages];
+};
+
+__global__ void __launch_bounds__(kProbeWarps * 32, 1) bw_probe_kernel(const uint8_t* buf, int64_t chunks,
+                                                                          int32_t* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ProbeWarp& sm = reinterpret_cast<ProbeWarp*>(smem_raw)[warp];
+  if (lane == 0) {
+    for (int i = 0; i < kProbeStages; ++i) mbar_init(&sm.bar[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  pdl_wait();
+  pdl_trigger();
+  const uint64_t pol = policy_evict_first();
+  const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kProbeWarps;
+  int64_t next = static_cast<int64_t>(warp) * gridDim.x + blockIdx.x;  // SM-minor, as the decode kernel
+  uint32_t issued = 0, consumed = 0;
+  auto issue = [&]() {
+    const int st = issued % kProbeStages;
+    if (lane == 0) {
+      const uint8_t* src = buf + next * kProbeStage;
+      mbar_arrive_expect_tx(&sm.bar[st], kProbeStage);
+      bulk_g2s(sm.stage[st], src, kProbeStage / 2, &sm.bar[st], pol);
+      bulk_g2s(sm.stage[st] + kProbeStage / 2, src + kProbeStage / 2, kProbeStage / 2, &sm.bar[st], pol);
+    }
+    ++issued;
+    next += n_warps;
+  };
+  while (next < chunks && issued - consumed < kProbeStages) issue();
+  uint32_t acc = 0;
+  while (consumed < issued) {
+    const int st = consumed % kProbeStages;
+    if (!mbar_wait(&sm.bar[st], (consumed / kProbeStages) & 1, status)) {
+      for (uint32_t k = consumed + 1; k < issued; ++k)
+        mbar_wait(&sm.bar[k % kProbeStages], (k / kProbeStages) & 1, nullptr);
+      return;
+    }
+    acc ^= *reinterpret_cast<const uint32_t*>(sm.stage[st] + lane * 16);
+    __syncwarp();
+    ++consumed;
+    while (next < chunks && issued - consumed < kProbeStages) issue();
+  }
+  // never true for a pool of finite bf16 data; keeps the reads observable
+  if (acc == 0x7FC00001u && status) atomicOr(status, 0);
+}
+
+}  // namespace
+
+cudaError_t launch_bw_probe(const void* buf, int64_t chunks, int32_t* status, cudaStream_t st) {
+  const size_t smem = sizeof(ProbeWarp) * kProbeWarps;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(bw_probe_kernel), smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(bw_probe_kernel, dim3(num_sms()), dim3(kProbeWarps * 32), smem, st,
+                    static_cast<const uint8_t*>(buf), chunks, status);
+}
+
+}  // namespace gw

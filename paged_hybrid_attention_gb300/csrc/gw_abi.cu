@@ -265,4 +265,15 @@ gw_status gw_decode_attn_global(const gw_kv_pool* pool, const void* q, void* out
                      stream);
 }
 
+gw_status gw_bw_probe(const void* buf, size_t bytes, int32_t* dev_status, void* stream) {
+  const char* fn = "gw_bw_probe";
+  g_err[0] = 0;
+  if (!buf || !aligned(buf, 16)) return fail(GW_ERR_INVALID_ARG, fn, "buf NULL or not 16-byte aligned");
+  if (bytes < 8192) return fail(GW_ERR_INVALID_ARG, fn, "bytes (%zu) < 8192", bytes);
+  if (dev_status && !aligned(dev_status, 4)) return fail(GW_ERR_INVALID_ARG, fn, "dev_status misaligned");
+  return cuda_status(launch_bw_probe(buf, static_cast<int64_t>(bytes / 8192), dev_status,
+                                     static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
 }  // extern "C"

@@ -113,6 +113,7 @@ cudaError_t launch_combine(const LocalArgs& a, int mode, int heads_per_unit, int
                            cudaStream_t st);
 
 cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream_t st);
+cudaError_t launch_bw_probe(const void* buf, int64_t chunks, int32_t* status, cudaStream_t st);
 cudaError_t launch_local_decode(int dtype, int group, const LocalArgs& a, cudaStream_t st);
 cudaError_t launch_global_decode(int layout, const LocalArgs& a, cudaStream_t st);
 cudaError_t launch_local_prompt(int dtype, int group, const LocalArgs& a, int max_q_rows, cudaStream_t st);

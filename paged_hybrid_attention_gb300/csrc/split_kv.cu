@@ -87,16 +87,18 @@ __global__ void combine_kernel(const LocalArgs a, int mode, int G, int chunk) {
   const int slice = static_cast<int>(wid % kSlices);
   const int64_t sh = wid / kSlices;
   const int s = static_cast<int>(sh / a.num_q_heads), h = static_cast<int>(sh % a.num_q_heads);
-  const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
-  if (n != 1) return;
+  // independent loads, issued together (one round trip before the partials)
+  const int row0 = a.cu_q_rows[s], row1 = a.cu_q_rows[s + 1];
   const int L = a.seq_lens[s];
+  const int ub_s = a.unit_base[s], ub_total = a.unit_base[a.batch];
+  if (row1 - row0 != 1) return;
   const int dim0 = slice * 128 + lane * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
-  if (len_ok(a, L, 1) && a.unit_base[a.batch] <= a.max_units) {
+  if (len_ok(a, L, 1) && ub_total <= a.max_units) {
     const int nc = mode == kSplitLocal ? local_chunks(L, a.window, chunk) : global_chunks(L);
     const int g = h / G, hh = h % G;
-    const int64_t ub = a.unit_base[s] + static_cast<int64_t>(g) * nc;
+    const int64_t ub = ub_s + static_cast<int64_t>(g) * nc;
     float4 u[kB];
     float2 ml[kB];
     auto fetch = [&](int c0) {
@@ -137,7 +139,7 @@ __global__ void combine_kernel(const LocalArgs a, int mode, int G, int chunk) {
   uint2 w;
   w.x = *reinterpret_cast<uint32_t*>(&lo);
   w.y = *reinterpret_cast<uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(a.cu_q_rows[s]) * a.num_q_heads + h) * D + dim0) = w;
+  *reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(row0) * a.num_q_heads + h) * D + dim0) = w;
 }
 
 }  // namespace

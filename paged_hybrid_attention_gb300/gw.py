@@ -29,7 +29,7 @@ LAYOUTS = {"local": LAYOUT_LOCAL, "folded": LAYOUT_GLOBAL_FOLDED, "full": LAYOUT
 DTYPES = {"bf16": KV_BF16, "e4m3": KV_E4M3}
 EXPORTS = ["gw_pool_page_bytes", "gw_kv_append", "gw_decode_attn_local", "gw_decode_attn_global",
            "gw_attn_workspace_bytes", "gw_last_error", "gw_version", "gw_decode_attn_local_noalloc",
-           "gw_noalloc_scratch_bytes"]
+           "gw_noalloc_scratch_bytes", "gw_bw_probe"]
 
 
 class GwError(RuntimeError):
@@ -63,6 +63,8 @@ _lib.gw_decode_attn_local_noalloc.argtypes = [_P, _vp, _vp, _i32, _i32, _vp, _vp
 _lib.gw_decode_attn_local_noalloc.restype = _i32
 _lib.gw_noalloc_scratch_bytes.argtypes = []
 _lib.gw_noalloc_scratch_bytes.restype = _sz
+_lib.gw_bw_probe.argtypes = [_vp, _sz, _vp, _vp]
+_lib.gw_bw_probe.restype = _i32
 _lib.gw_last_error.argtypes = []
 _lib.gw_last_error.restype = ctypes.c_char_p
 _lib.gw_version.argtypes = []
@@ -186,3 +188,8 @@ def decode_attn_local_noalloc(pool, q, out, cu_q_rows, seq_lens, block_table, wi
                                              int(seq_lens.numel()), _ptr(cu_q_rows), _ptr(seq_lens),
                                              _ptr(block_table), int(block_table.shape[1]), int(max_q_rows),
                                              int(window), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def bw_probe(buf, dev_status=None, stream=None):
+    """gw_bw_probe: stream `buf` (a CUDA tensor) through the decode kernels' copy pipeline."""
+    _check(_lib.gw_bw_probe(_ptr(buf), int(buf.numel() * buf.element_size()), _ptr(dev_status), _stream(stream)))

@@ -119,3 +119,12 @@ def test_rope_table_matches_oracle(theta, R, D):
     tol = np.maximum(np.spacing(np.abs(ref)).astype(np.float64), 1e-10)
     assert np.all(np.abs(mine.astype(np.float64) - ref) <= tol)
     assert np.count_nonzero(mine.view(np.uint32) != ref.view(np.uint32)) < 1e-4 * ref.size
+
+
+def test_bw_probe_host_validation():
+    L = gw.lib()
+    assert L.gw_bw_probe(None, 1 << 20, None, None) == gw.GW_ERR_INVALID_ARG
+    assert gw.last_error().startswith("gw_bw_probe:")
+    assert L.gw_bw_probe(_fake((1 << 24) + 8), 1 << 20, None, None) == gw.GW_ERR_INVALID_ARG   # misaligned
+    assert L.gw_bw_probe(_fake(), 4096, None, None) == gw.GW_ERR_INVALID_ARG                   # < one stage
+    assert "8192" in gw.last_error()
