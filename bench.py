@@ -46,10 +46,14 @@ from paged_hybrid_attention_gb300 import synth  # noqa: E402
 METRIC = "decode-attn KV GB/s (frac of HBM peak) & batched decode steps/s, 1×GB300"
 UNIT = "GB/s"
 
-# ncu DRAM traffic (read + write bytes) per launch of the dominant kernel, with
-# the SHA-256 of the kernel source it was taken from; reported as null once the
-# source no longer matches.  (bytes, sha256 of csrc/attn_local.cu)
-NCU_TRAFFIC = {"local_decode": None}
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
+# of the dominant kernel per workload, with the SHA-256 of the kernel source it
+# was captured from; reported as null once the source no longer matches.
+# workload: (bytes, source file under csrc/, sha256)
+NCU_TRAFFIC = {
+    "serving": (275160832, "attn_local.cu", "50e1e8a57f56e5db08acb6b0a79fe4b6f9d92f3921e2fb30ebe1c2a9e9b5cd0f"),
+    "fp8_local": (552877568, "attn_local.cu", "50e1e8a57f56e5db08acb6b0a79fe4b6f9d92f3921e2fb30ebe1c2a9e9b5cd0f"),
+}
 
 
 def parse():
@@ -69,12 +73,13 @@ def parse():
 
 # --------------------------------------------------------------------------- setup
 def peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, 'measured' | 'fallback')."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured", float(d.get("sm_max_mhz", 2070.0))
-    return 6800.0, "fallback", 2070.0
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
 
 
 def workload_layers(name, rank):
@@ -111,6 +116,20 @@ def kv_bytes(layer):
     return tot
 
 
+def prompt_flops(layer):
+    """Tensor FLOPs of the prompt rows (sequences with n > 1 query rows) of one
+    attention call: 2 contractions (q.K, p.V) x 2 flops x heads x dim x keys."""
+    fam, sp = layer.fam, layer.spec
+    tot = 0
+    for L, n in zip(sp.lens.astype(np.int64), sp.n_rows.astype(np.int64)):
+        if n <= 1:
+            continue
+        p = np.arange(L - n, L, dtype=np.int64)
+        keys = np.minimum(p + 1, fam.window) if fam.kind == "local" else p + 1
+        tot += int(keys.sum())
+    return 4 * sp.num_q_heads * fam.head_dim * tot
+
+
 class GpuLayer:
     def __init__(self, layer, gw, gen, dev):
         fam, sp = layer.fam, layer.spec
@@ -142,6 +161,7 @@ class GpuLayer:
         self.ws = gw.alloc_workspace(self.pool, sp.num_q_heads, len(sp.lens), self.bt.shape[1], self.max_q_rows,
                                      max(1, fam.window), device=dev)
         self.kv_bytes = kv_bytes(layer)
+        self.prompt_flops = prompt_flops(layer)
 
     def _append_random(self, gw, gen, dev, slot, pos, sig, chunk=1 << 18):
         fam = self.fam
@@ -155,16 +175,19 @@ class GpuLayer:
                 if fam.kind == "local" else v
             gw.kv_append(self.pool, k, v, s_, p_, self.table, self.status)
 
-    def run(self, gw, stream, ev=None):
-        gw.kv_append(self.pool, self.k_new, self.v_new, self.slot_new, self.pos_new, self.table, self.status, stream)
-        if ev is not None:
-            ev[0].record(stream)
+    def attend(self, gw, stream):
         if self.fam.kind == "local":
             gw.decode_attn_local(self.pool, self.q, self.out, self.cu, self.lens, self.bt, self.ws, self.fam.window,
                                  max_q_rows=self.max_q_rows, dev_status=self.status, stream=stream)
         else:
             gw.decode_attn_global(self.pool, self.q, self.out, self.cu, self.lens, self.bt, self.ws,
                                   max_q_rows=self.max_q_rows, dev_status=self.status, stream=stream)
+
+    def run(self, gw, stream, ev=None):
+        gw.kv_append(self.pool, self.k_new, self.v_new, self.slot_new, self.pos_new, self.table, self.status, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        self.attend(gw, stream)
         if ev is not None:
             ev[1].record(stream)
 
@@ -341,7 +364,7 @@ class Ranks:
 
 def main():
     args = parse()
-    peak, peak_kind, _ = peaks()
+    peak, peak_tf, peak_kind = peaks()
 
     if args.impl == "reference":
         if int(os.environ.get("RANK", "0")) != 0:
@@ -431,15 +454,43 @@ def main():
     value = ranks.throughput(step_bytes, ms_rank)
     status = int(sum(int(g.status.item()) for g in glayers))
 
-    # ---- dominant call: CUDA events around each call over eager steps
-    K2 = min(K, 200)
+    # ---- dominant call, steady state: a CUDA graph of consecutive calls over
+    # the dominant layers (each its own pool, so every call reads its KV from
+    # HBM), replayed R times between CUDA events on the launching stream
+    reps_in_graph = max(1, 20 // len(dom))
+    n_calls = reps_in_graph * len(dom)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for g in dom:
+            g.attend(gw, side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    gdom = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gdom):
+        for _ in range(reps_in_graph):
+            for g in dom:
+                g.attend(gw, torch.cuda.current_stream())
+    for _ in range(3):
+        gdom.replay()
+    torch.cuda.synchronize()
+    R = 20
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for _ in range(R):
+        gdom.replay()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dom_ms = d0.elapsed_time(d1) / (R * n_calls)
+    # the same call timed eagerly (events around each call of 50 eager steps)
+    K2 = min(K, 50)
     evs = {id(g): [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
            for g in dom}
     for k in range(K2):
         for g in glayers:
             g.run(gw, stream, evs[id(g)][k] if id(g) in evs else None)
     torch.cuda.synchronize()
-    dom_ms = statistics.mean(e0.elapsed_time(e1) for g in dom for e0, e1 in evs[id(g)])
+    dom_ms_eager = statistics.mean(e0.elapsed_time(e1) for g in dom for e0, e1 in evs[id(g)])
 
     # ---- read ceiling of the decode kernels' copy pipeline (gw_bw_probe, 4 GiB)
     read_gbs = None
@@ -488,13 +539,28 @@ def main():
         ranks.close()
         return
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    src = os.path.join(ROOT, "paged_hybrid_attention_gb300", "csrc", "attn_local.cu")
+    dom_flops = statistics.mean(g.prompt_flops for g in dom)
     traffic = None
-    if NCU_TRAFFIC.get("local_decode"):
-        tb, sha = NCU_TRAFFIC["local_decode"]
-        with open(src, "rb") as f:
+    if args.workload in NCU_TRAFFIC:
+        tb, fname, sha = NCU_TRAFFIC[args.workload]
+        with open(os.path.join(ROOT, "paged_hybrid_attention_gb300", "csrc", fname), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest() == sha:
                 traffic = tb
+    how = dom_name + ", CUDA-graph replay of %d consecutive calls x %d, events on the launching stream" % (n_calls, R)
+    if dom_flops > 0:
+        # prompt rows make the call a dense contraction: tensor roofline
+        tflops = dom_flops / (dom_ms * 1e-3) / 1e12
+        roofline = {"kernel": how + " (decode rows + causal prompt rows)", "bound": "tensor", "achieved": tflops,
+                    "peak": peak_tf, "unit": "TFLOP/s", "frac": tflops / peak_tf, "peak_kind": peak_kind,
+                    "traffic": None, "algorithmic_flops_per_launch": dom_flops, "kv_gbs": achieved,
+                    "ms_per_launch": dom_ms, "ms_per_launch_eager": dom_ms_eager}
+    else:
+        roofline = {"kernel": how, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                    "frac_of_read_probe": achieved / read_gbs if read_gbs else None,
+                    "frac_of_nominal_8000": achieved / 8000.0,
+                    "algorithmic_bytes_per_launch": dom_bytes, "ms_per_launch": dom_ms,
+                    "ms_per_launch_eager": dom_ms_eager}
     cpu = None
     if not args.no_cpu:
         gbs, desc, _ = oracle_sample(args.workload, budget_s=12.0)
@@ -513,12 +579,7 @@ def main():
                    "batch": int(len(sp.lens)), "kv_bytes_per_step": step_bytes, "q_heads": sp.num_q_heads,
                    "l2": "inputs larger than L2: %.2f GB of KV read per step" % (step_bytes / 1e9),
                    "parallelism": "dp%d (sequences sharded, no collective)" % world},
-        "roofline": {"kernel": dom_name + ", CUDA events around each call, %d eager steps" % K2,
-                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
-                     "frac_of_read_probe": achieved / read_gbs if read_gbs else None,
-                     "frac_of_nominal_8000": achieved / 8000.0,
-                     "algorithmic_bytes_per_launch": dom_bytes, "ms_per_launch": dom_ms},
+        "roofline": roofline,
         "bw_probe": None if read_gbs is None else {"read_gbs": read_gbs, "bytes": 4 << 30,
                      "what": "gw_bw_probe: 4 GiB streamed through the local decode copy pipeline "
                              "(8 warps x 2-stage 8 KiB rings per SM), no arithmetic; best of 5"},
