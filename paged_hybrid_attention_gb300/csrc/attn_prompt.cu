@@ -6,21 +6,17 @@
 // appended first in the same step) and attends causally: keys
 // [max(0, p - W + 1), p] on local layers, [0, p] on global layers.
 //
-// Unlike decode rows, these are real dense contractions (many query rows
-// against the same keys), computed here FlashAttention-2 style with
+// This file holds the tile plan shared by both families and the global-layer
+// kernel; the local-layer kernel (tcgen05, tensor memory) is in
+// attn_prompt_tc.cu.  The global kernel is FlashAttention-2 style with
 // warp-level mma.sync (m16n8k16, bf16 in, fp32 accumulate) and an online
-// base-2 softmax:
-//   * local  (head dim 256): a CTA owns 64 rows = (64/G queries) x (the G q
-//     heads of one KV head), so every K/V tile is shared by the GQA group;
-//     K/V tiles of 32 keys are gathered from the pages with cp.async into
-//     XOR-swizzled shared memory (conflict-free ldmatrix).
-//   * global (head dim 512, one KV head): a CTA owns 64 rows = (64/HQ
-//     queries) x HQ heads; pairs of warps split the head dim, exchange their
-//     partial logits through shared memory and each accumulate half of O.
-//     Pages are copied whole with cp.async.bulk; the folded page's 8x8 blocks
-//     are read directly by ldmatrix, K = k_rot || V[128:512] by addressing.
-// Tiles of (sequence, KV head, query block) are enumerated by a small plan
-// kernel and processed by persistent CTAs.
+// base-2 softmax: a CTA owns 64 rows = (64/HQ queries) x HQ heads; pairs of
+// warps split the head dim, exchange their partial logits through shared
+// memory and each accumulate half of O.  Pages are copied whole with
+// cp.async.bulk; the folded page's 8x8 blocks are read directly by ldmatrix,
+// K = k_rot || V[128:512] by addressing.  Tiles of (sequence, KV head, query
+// block) are enumerated by a small plan kernel and processed by persistent
+// CTAs.
 #include "common.cuh"
 
 namespace gw {
@@ -126,217 +122,9 @@ __global__ void plan_prompt_kernel(const LocalArgs a, int heads_factor, int quer
   if (threadIdx.x == 0) a.prompt_base[a.batch] = carry;
 }
 
-// ============================================================ local (hd 256)
+// =========================================================== global (hd 512)
 constexpr int kRows = 64;     // query rows x heads per CTA
 constexpr int kKeys = 32;     // keys per K/V tile
-constexpr int kLocalThreads = 128;
-
-struct LocalPromptSmem {
-  uint8_t q[kRows * 512];          // [64 rows][256] bf16, swizzled
-  uint8_t k[2][kKeys * 512];       // [32 keys][256] bf16, swizzled
-  uint8_t v[2][kKeys * 512];
-};
-
-template <int G>
-__global__ void __launch_bounds__(kLocalThreads, 2) local_prompt_kernel(const LocalArgs a) {
-  constexpr int BQ = kRows / G;  // queries per tile
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  LocalPromptSmem& sm = *reinterpret_cast<LocalPromptSmem*>(smem_raw);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g8 = lane >> 2, c4 = lane & 3;
-  pdl_wait();
-  pdl_trigger();
-  const int total = a.prompt_base[a.batch];
-  const uint32_t q_s = smem_u32(sm.q);
-  const int64_t head_elems = 2LL * kPage * 256;  // K + V of one KV head in one page
-
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    const int s = find_seq(a.prompt_base, a.batch, tile);
-    const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
-    const int nqb = (n + BQ - 1) / BQ;
-    const int r0 = tile - a.prompt_base[s];
-    const int g = r0 / nqb, qb = r0 % nqb;
-    const int L = a.seq_lens[s];
-    const int P0 = L - n;
-    const int q0 = qb * BQ;
-    const int nq = min(BQ, n - q0);
-    const int lo = max(0, P0 + q0 - a.window + 1);
-    const int hi = P0 + q0 + nq - 1;
-    const int t_lo = lo / kKeys, t_hi = hi / kKeys;
-    const int32_t* bt = a.block_table + static_cast<int64_t>(s) * a.max_pages;
-    const uint16_t* pool = reinterpret_cast<const uint16_t*>(a.pool);
-
-    __syncthreads();  // previous tile's smem readers are done
-    // ---- Q rows (zero rows past nq)
-    for (int i = tid; i < kRows * 32; i += kLocalThreads) {
-      const int r = i >> 5, c = i & 31;
-      const int hh = r / BQ, qi = r % BQ;
-      const uint32_t dst = q_s + swz<32>(r, c);
-      if (qi < nq) {
-        const int64_t row = static_cast<int64_t>(a.cu_q_rows[s] + q0 + qi) * a.num_q_heads + g * G + hh;
-        cp_async16(dst, a.q + row * 256 + c * 8);
-      } else {
-        st_zero16(dst);
-      }
-    }
-    auto load_kv = [&](int t, int buf) {
-      const uint32_t ks = smem_u32(sm.k[buf]), vs = smem_u32(sm.v[buf]);
-      for (int i = tid; i < kKeys * 32; i += kLocalThreads) {
-        const int j = i >> 5, c = i & 31;
-        const int key = t * kKeys + j;
-        const uint32_t off = swz<32>(j, c);
-        int32_t page = -1;
-        if (key >= lo && key <= hi) {
-          page = bt[key / kPage];
-          if (page < 0 || page >= a.num_pages) {
-            if (c == 0) set_status(a.status, GW_DEV_PAGE_RANGE);
-            page = -1;
-          }
-        }
-        if (page >= 0) {
-          const uint16_t* kb = pool + (static_cast<int64_t>(page) * a.kv_heads + g) * head_elems + (key % kPage) * 256;
-          cp_async16(ks + off, kb + c * 8);
-          cp_async16(vs + off, kb + kPage * 256 + c * 8);
-        } else {
-          st_zero16(ks + off);
-          st_zero16(vs + off);
-        }
-      }
-    };
-    load_kv(t_lo, 0);
-    cp_commit();
-
-    // row positions of this thread's two rows (g8 and g8 + 8 of the warp's 16)
-    int pos[2];
-    bool rv[2];
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int r = warp * 16 + g8 + 8 * h2;
-      const int qi = r % BQ;
-      rv[h2] = qi < nq;
-      pos[h2] = P0 + q0 + qi;
-    }
-    float o[32][4];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-
-    for (int t = t_lo; t <= t_hi; ++t) {
-      const int buf = (t - t_lo) & 1;
-      if (t < t_hi) load_kv(t + 1, buf ^ 1);
-      cp_commit();
-      cp_wait<1>();
-      __syncthreads();
-      const uint32_t ks = smem_u32(sm.k[buf]), vs = smem_u32(sm.v[buf]);
-      // ---- S = Q K^T (16 rows x 32 keys per warp)
-      float sacc[4][4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 16; ++kk) {
-        uint32_t af[4];
-        {
-          const int r = warp * 16 + (lane & 15);
-          ldsm_x4(q_s + swz<32>(r, 2 * kk + (lane >> 4)), af);
-        }
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          uint32_t bf[4];
-          const int mi = lane >> 3;
-          const int key = np * 16 + (lane & 7) + 8 * (mi >> 1);
-          ldsm_x4(ks + swz<32>(key, 2 * kk + (mi & 1)), bf);
-          mma16816(sacc[2 * np], af, bf[0], bf[1]);
-          mma16816(sacc[2 * np + 1], af, bf[2], bf[3]);
-        }
-      }
-      // ---- mask, online softmax (base 2)
-      float rmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h2 = e >> 1;
-          const int key = t * kKeys + nt * 8 + 2 * c4 + (e & 1);
-          const bool ok = rv[h2] && key <= pos[h2] && key > pos[h2] - a.window && key >= lo;
-          const float sv = ok ? sacc[nt][e] * a.scale_log2 : -INFINITY;
-          sacc[nt][e] = sv;
-          rmax[h2] = fmaxf(rmax[h2], sv);
-        }
-      }
-      float alpha[2];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        rmax[h2] = fmaxf(rmax[h2], __shfl_xor_sync(0xffffffffu, rmax[h2], 1));
-        rmax[h2] = fmaxf(rmax[h2], __shfl_xor_sync(0xffffffffu, rmax[h2], 2));
-        const float mn = fmaxf(m[h2], rmax[h2]);
-        alpha[h2] = mn == -INFINITY ? 1.f : ex2(m[h2] - mn);
-        m[h2] = mn;
-      }
-      uint32_t pf[2][4];
-      float rs[2] = {0.f, 0.f};
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        float p[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h2 = e >> 1;
-          p[e] = sacc[nt][e] == -INFINITY ? 0.f : ex2(sacc[nt][e] - m[h2]);
-        }
-        const uint32_t lo2 = pack_bf16(p[0], p[1]), hi2 = pack_bf16(p[2], p[3]);
-        const __nv_bfloat162 bl = *reinterpret_cast<const __nv_bfloat162*>(&lo2);
-        const __nv_bfloat162 bh = *reinterpret_cast<const __nv_bfloat162*>(&hi2);
-        rs[0] += __low2float(bl) + __high2float(bl);
-        rs[1] += __low2float(bh) + __high2float(bh);
-        // A fragment of P for k-step nt/2: regs {row g, k lo}, {row g+8, k lo}, {row g, k hi}, {row g+8, k hi}
-        pf[nt >> 1][(nt & 1) * 2 + 0] = lo2;
-        pf[nt >> 1][(nt & 1) * 2 + 1] = hi2;
-      }
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) l[h2] = l[h2] * alpha[h2] + rs[h2];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        o[i][0] *= alpha[0];
-        o[i][1] *= alpha[0];
-        o[i][2] *= alpha[1];
-        o[i][3] *= alpha[1];
-      }
-      // ---- O += P V
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-#pragma unroll
-        for (int np = 0; np < 16; ++np) {
-          uint32_t bf[4];
-          const int mi = lane >> 3;
-          const int key = kk * 16 + (lane & 7) + 8 * (mi & 1);
-          ldsm_x4_t(vs + swz<32>(key, 2 * np + (mi >> 1)), bf);
-          mma16816(o[2 * np], pf[kk], bf[0], bf[1]);
-          mma16816(o[2 * np + 1], pf[kk], bf[2], bf[3]);
-        }
-      }
-      __syncthreads();
-    }
-    cp_wait<0>();
-    // ---- epilogue
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      l[h2] += __shfl_xor_sync(0xffffffffu, l[h2], 1);
-      l[h2] += __shfl_xor_sync(0xffffffffu, l[h2], 2);
-    }
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      if (!rv[h2]) continue;
-      const int r = warp * 16 + g8 + 8 * h2;
-      const int hh = r / BQ, qi = r % BQ;
-      const float inv = l[h2] > 0.f ? 1.f / l[h2] : 0.f;
-      uint16_t* dst = a.out + (static_cast<int64_t>(a.cu_q_rows[s] + q0 + qi) * a.num_q_heads + g * G + hh) * 256;
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        *reinterpret_cast<uint32_t*>(dst + i * 8 + 2 * c4) = pack_bf16(o[i][2 * h2] * inv, o[i][2 * h2 + 1] * inv);
-    }
-  }
-}
-
-// =========================================================== global (hd 512)
 constexpr int kGlobalThreads = 256;
 
 template <int LAYOUT>
@@ -586,13 +374,9 @@ __global__ void __launch_bounds__(kGlobalThreads, 1) global_prompt_kernel(const 
 
 template <int G>
 cudaError_t launch_local_g(const LocalArgs& a, cudaStream_t st) {
-  cudaError_t e = launch_pdl(plan_prompt_kernel, dim3(1), dim3(1024), 0, st, a, a.kv_heads, kRows / G);
+  cudaError_t e = launch_pdl(plan_prompt_kernel, dim3(1), dim3(1024), 0, st, a, a.kv_heads, 128 / G);
   if (e != cudaSuccess) return e;
-  auto kern = local_prompt_kernel<G>;
-  const size_t smem = sizeof(LocalPromptSmem);
-  e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(num_sms() * 2), dim3(kLocalThreads), smem, st, a);
+  return launch_local_prompt_tc(G, a, st);
 }
 
 template <int LAYOUT, int HQ>

@@ -1,0 +1,487 @@
+// Prompt rows of a mixed step on LOCAL layers, on the tensor cores (tcgen05).
+//
+// "Gemma 4" (pegainfer model page), "Scheduling": a new prompt's rows are
+// computed in the same batched step as the live streams' next token;
+// "Chunked walk": a prompt may continue over pages cached earlier.  Row r of
+// a sequence with n > 1 query rows sits at position p = L - n + r and attends
+// causally within the window: keys [max(0, p - W + 1), p].
+//
+// These rows are a dense contraction, so they run on UMMA with fp32
+// accumulators in tensor memory:
+//   * a work tile is (sequence, KV head, block of 128/G queries); its 128
+//     rows are (G heads x 128/G queries), so every K/V tile feeds the whole
+//     GQA group;
+//   * per 64-key tile:  S[128 x 64]  = Q[128 x 256] . K^T      (M=128, N=64)
+//                       O[128 x 256] += P[128 x 64] . V         (M=128, N=256)
+//     S (two buffers) and O live in TMEM; TMEM lane i is row i, so each
+//     softmax thread owns one row and needs no cross-thread reduction;
+//   * softmax is base 2 with a lazily raised reference max per row (O is
+//     rescaled only when a logit exceeds it by more than 8); P is rounded to
+//     bf16 and l sums the rounded weights;
+//   * K and V tiles arrive by TMA (cp.async.bulk.tensor): one 2 KB copy per
+//     (page, 64-dim chunk) lands 16 key rows x 128 B in the 128-byte-swizzled
+//     UMMA layout, so a 64-key tile is 16 copies for K and 16 for V, issued
+//     together by 16 lanes of a producer warp.  K feeds Q.K^T as a K-major
+//     operand, V feeds P.V as an MN-major operand, three stages each.
+//   * Q and P never touch shared memory: the softmax threads write their Q
+//     rows (once per work tile) and their bf16 P rows (over the S columns
+//     just read) into tensor memory, and both contractions take A from there.
+//     TMEM: S at columns 0 and 64 (P over their first 32), Q at 128..255,
+//     O at 256..511.
+//     V rows of keys outside the tile's range are cleared before P.V (0 *
+//     anything must stay 0), K rows of pages not loaded before Q.K^T.
+// Warp roles (224 threads, persistent CTAs):
+//   warps 0-3  load Q rows, softmax, epilogue (warp w owns TMEM lanes 32w..)
+//   warps 4, 6 TMA producers of K and of V tiles (16 lanes issue a tile's copies)
+//   warp 5     MMA issue (elect.sync) and TMEM owner
+// Every wait is bounded; a timeout raises GW_DEV_TIMEOUT and the CTA stops.
+#include <cuda.h>
+
+#include "tcgen05.cuh"
+namespace gw {
+namespace {
+
+constexpr int kTM = 128;              // rows per work tile (UMMA M)
+constexpr int kTN = 64;               // keys per key tile (UMMA N of S)
+constexpr int kTcThreads = 224;
+constexpr float kTcLazy = 8.f;
+// TMEM columns: S buffers at 0 and 64, Q at 128..255, O at 256..511
+constexpr uint32_t kColS = 0, kColQ = 128, kColO = 256;
+constexpr uint32_t kPlane = kTN * 128;  // one 64-dim chunk of a K/V tile: 64 rows x 128 B
+constexpr int kKS = 3, kVS = 3;         // K and V stages
+
+struct TcSmem {
+  uint8_t k[kKS][4 * kPlane];    // [dim chunk 4][64 keys][128 B], 128-byte swizzled
+  uint8_t v[kVS][4 * kPlane];    // same layout
+  uint64_t kfull[kKS], kempty[kKS], vfull[kVS], vempty[kVS];
+  uint64_t s_ready[2], p_ready[2], pfree[2];
+  uint64_t q_full, q_free, o_done, o_free;
+  int32_t kmask[kKS], vmask[kVS];  // pages of the K / V tile that were loaded (bits 0-3)
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ void zero16(uint32_t dst) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0) : "memory");
+}
+
+// TMA: box {64 elements, 1 chunk, 16 rows} of the KV map -> 2 KB at dst.
+__device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap* map, int chunk, int row, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(chunk), "r"(row), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Shared-memory descriptor of a 128-byte-swizzled operand (atoms of 8 rows x
+// 128 B, 1024 B apart along the 8-row direction).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ int prompt_seq(const int32_t* base, int batch, int t) {
+  int lo = 0, hi = batch;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (base[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct WorkTile {
+  int s, g, q0, nq, P0, lo, hi, t_lo, t_hi, row0;
+};
+
+template <int G>
+__device__ __forceinline__ WorkTile work_tile(const LocalArgs& a, int tile) {
+  constexpr int BQ = kTM / G;
+  WorkTile w;
+  w.s = prompt_seq(a.prompt_base, a.batch, tile);
+  const int n = a.cu_q_rows[w.s + 1] - a.cu_q_rows[w.s];
+  const int nqb = (n + BQ - 1) / BQ;
+  const int r0 = tile - a.prompt_base[w.s];
+  w.g = r0 / nqb;
+  const int qb = r0 % nqb;
+  const int L = a.seq_lens[w.s];
+  w.P0 = L - n;
+  w.q0 = qb * BQ;
+  w.nq = min(BQ, n - w.q0);
+  w.lo = max(0, w.P0 + w.q0 - a.window + 1);
+  w.hi = w.P0 + w.q0 + w.nq - 1;
+  w.t_lo = w.lo / kTN;
+  w.t_hi = w.hi / kTN;
+  w.row0 = a.cu_q_rows[w.s];
+  return w;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    local_prompt_tc_kernel(const LocalArgs a, const __grid_constant__ CUtensorMap kv_map) {
+  constexpr int BQ = kTM / G;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  int32_t* st = a.status;
+
+  if (tid == 0) {
+    for (int b = 0; b < kKS; ++b) {
+      mbar_init(&sm.kfull[b], 1);
+      mbar_init(&sm.kempty[b], 1);
+    }
+    for (int b = 0; b < kVS; ++b) {
+      mbar_init(&sm.vfull[b], 1);
+      mbar_init(&sm.vempty[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.s_ready[b], 1);
+      mbar_init(&sm.p_ready[b], kTM);
+      mbar_init(&sm.pfree[b], 1);
+    }
+    mbar_init(&sm.q_full, kTM);
+    mbar_init(&sm.q_free, 1);
+    mbar_init(&sm.o_done, 1);
+    mbar_init(&sm.o_free, kTM);
+    fence_mbar_init();
+  }
+  pdl_wait();
+  pdl_trigger();
+  const int total = a.prompt_base[a.batch];
+  if (warp == 5) {
+    tc::alloc(&sm.tmem_base, 512);
+    tc::relinquish();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 4 || warp == 6) {
+    // ------------------------------------------------------ TMA producers
+    // warp 4 loads K tiles, warp 6 V tiles; lane l < 16 issues the copy of
+    // page l / 4, 64-dim chunk l % 4 (the 16 copies of a tile go out together)
+    const bool is_v = warp == 6;
+    const uint64_t pol = policy_evict_first();
+    const int j = lane >> 2, c = lane & 3;
+    uint32_t gi = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const WorkTile w = work_tile<G>(a, tile);
+      const int32_t* bt = a.block_table + static_cast<int64_t>(w.s) * a.max_pages;
+      for (int t = w.t_lo; t <= w.t_hi; ++t, ++gi) {
+        const int ns = is_v ? kVS : kKS;
+        const int b = static_cast<int>(gi % ns);
+        const uint32_t ph = gi / ns;  // use of this stage
+        // page j of the tile: loaded if it overlaps [lo, hi] and is valid
+        int32_t row = -1;
+        if (lane < 16) {
+          const int k0 = t * kTN + j * kPage;
+          if (k0 + kPage - 1 >= w.lo && k0 <= w.hi) {
+            const int32_t pg = bt[k0 / kPage];
+            if (pg >= 0 && pg < a.num_pages) {
+              row = (pg * a.kv_heads + w.g) * 2 * kPage + (is_v ? kPage : 0);
+            } else if (c == 0) {
+              set_status(st, GW_DEV_PAGE_RANGE);
+            }
+          }
+        }
+        const uint32_t loaded = __ballot_sync(0xffffffffu, row >= 0 && c == 0);  // bit 4j: page j
+        int mask = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mask |= ((loaded >> (4 * q)) & 1) << q;
+        uint64_t* full = is_v ? &sm.vfull[b] : &sm.kfull[b];
+        uint64_t* empty = is_v ? &sm.vempty[b] : &sm.kempty[b];
+        if (ph >= 1 && !__all_sync(0xffffffffu, mbar_wait(empty, (ph - 1) & 1, st))) { ok = false; break; }
+        if (lane == 0) {
+          if (is_v) sm.vmask[b] = mask; else sm.kmask[b] = mask;
+          mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(mask)) * 4 * 2048);
+        }
+        __syncwarp();
+        if (row >= 0)
+          tma_rows(smem_u32(is_v ? sm.v[b] : sm.k[b]) + c * kPlane + j * 2048, &kv_map, c, row, full, pol);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issue
+    const uint32_t id_s = tc::idesc_bf16(kTM, kTN, false, false);
+    const uint32_t id_o = tc::idesc_bf16(kTM, 256, false, true);
+    uint32_t gi = 0;
+    int wt = 0;
+    bool ok = true;
+    auto pv = [&](uint32_t i, int key0, const WorkTile& w, bool first_of_tile, bool last_of_tile) -> bool {
+      const int b = static_cast<int>(i % kVS);
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.vfull[b], (i / kVS) & 1, st))) return false;
+      // V rows of keys outside [lo, hi] or of pages not loaded: clear them
+      const int mask = sm.vmask[b];
+      if (mask != 0xF || key0 < w.lo || key0 + kTN - 1 > w.hi) {
+        const uint32_t vb = smem_u32(sm.v[b]);
+        for (int kr = 0; kr < kTN; ++kr) {
+          const int key = key0 + kr;
+          if (((mask >> (kr >> 4)) & 1) && key >= w.lo && key <= w.hi) continue;
+          zero16(vb + (lane >> 3) * kPlane + kr * 128 + (lane & 7) * 16);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      const int sb = i & 1;  // S / P buffer in tensor memory
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_ready[sb], (i >> 1) & 1, st))) return false;
+      tc::fence_after();
+      const uint32_t va = smem_u32(sm.v[b]);
+#pragma unroll
+      for (int kk = 0; kk < kTN / 16; ++kk)
+        tc::mma_bf16_ts_warp(tmem + kColO, tmem + kColS + 64 * sb + 8 * kk, sw128_desc(va + kk * 2048, kPlane), id_o,
+                             !(first_of_tile && kk == 0));
+      tc::commit_warp(&sm.vempty[b]);
+      tc::commit_warp(&sm.pfree[sb]);
+      if (last_of_tile) tc::commit_warp(&sm.o_done);
+      return true;
+    };
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++wt) {
+      const WorkTile w = work_tile<G>(a, tile);
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.q_full, wt & 1, st))) break;
+      const int nt = w.t_hi - w.t_lo + 1;
+      for (int j = 0; j < nt; ++j, ++gi) {
+        const int b = static_cast<int>(gi % kKS), sb = gi & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.kfull[b], (gi / kKS) & 1, st))) { ok = false; break; }
+        const uint32_t ka = smem_u32(sm.k[b]);
+        const int kmask = sm.kmask[b];
+        if (kmask != 0xF) {
+          // pages not loaded (outside the range or invalid): finite zeros, so no
+          // stale bytes can turn into NaN logits
+          for (int pg = 0; pg < 4; ++pg) {
+            if ((kmask >> pg) & 1) continue;
+            for (int kr = 0; kr < kPage; ++kr)
+              zero16(ka + (lane >> 3) * kPlane + (pg * kPage + kr) * 128 + (lane & 7) * 16);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        tc::fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks)
+          tc::mma_bf16_ts_warp(tmem + kColS + 64 * sb, tmem + kColQ + 8 * ks,
+                               sw128_desc(ka + (ks >> 2) * kPlane + (ks & 3) * 32, 16), id_s, ks > 0);
+        tc::commit_warp(&sm.kempty[b]);
+        tc::commit_warp(&sm.s_ready[sb]);
+        if (j == nt - 1) tc::commit_warp(&sm.q_free);
+        if (j == 0 && wt >= 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.o_free, (wt - 1) & 1, st))) {
+          ok = false;
+          break;
+        }
+        if (j >= 1 && !pv(gi - 1, (w.t_lo + j - 1) * kTN, w, j == 1, false)) { ok = false; break; }
+      }
+      if (!ok) break;
+      if (!pv(gi - 1, w.t_hi * kTN, w, nt == 1, true)) break;
+    }
+  } else {
+    // ---------------------------------------- Q rows, softmax, epilogue
+    const int r = tid;  // row of the work tile = TMEM lane
+    const int hh = r / BQ, qi = r % BQ;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    // Q row of a work tile -> tensor memory (128 columns of bf16 pairs), then
+    // signal the MMA warp; rows past the prompt are zeros
+    auto load_q = [&](const WorkTile& w) {
+      const bool ok_row = qi < w.nq;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + (static_cast<int64_t>(w.row0 + w.q0 + (ok_row ? qi : 0)) * a.num_q_heads + w.g * G + hh) * 256);
+      uint32_t qv[128];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const uint4 x = ok_row ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        qv[4 * c] = x.x;
+        qv[4 * c + 1] = x.y;
+        qv[4 * c + 2] = x.z;
+        qv[4 * c + 3] = x.w;
+      }
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk)
+        tc::st32(tmem + lane_base + kColQ + 32 * blk, *reinterpret_cast<uint32_t(*)[32]>(&qv[32 * blk]));
+      tc::wait_st();
+      tc::fence_before();
+      mbar_arrive(&sm.q_full);
+    };
+    uint32_t gi = 0;
+    int wt = 0;
+    if (static_cast<int>(blockIdx.x) < total) load_q(work_tile<G>(a, blockIdx.x));
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++wt) {
+      const WorkTile w = work_tile<G>(a, tile);
+      const bool row_ok = qi < w.nq;
+      const int pos = w.P0 + w.q0 + qi;
+      // this row's keys: [kmin, kmax] (empty for rows past the prompt)
+      const int kmin = max(w.lo, pos - a.window + 1), kmax = row_ok ? pos : -1;
+      float m_ref = -INFINITY;            // reference max, scaled log2 units
+      float lp[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums of the rounded weights
+      const int nt = w.t_hi - w.t_lo + 1;
+      bool ok = true;
+      for (int j = 0; j < nt; ++j, ++gi) {
+        const int b = gi & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_ready[b], (gi >> 1) & 1, st))) { ok = false; break; }
+        tc::fence_after();
+        uint32_t sv[64];
+        tc::ld32(tmem + lane_base + kColS + 64 * b, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tc::ld32(tmem + lane_base + kColS + 64 * b + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tc::wait_ld();
+        const int key0 = (w.t_lo + j) * kTN;
+        if (!(key0 >= kmin && key0 + kTN - 1 <= kmax)) {
+          // edge tile for this row: keys outside [kmin, kmax] get -inf
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (key0 + c < kmin || key0 + c > kmax) sv[c] = __float_as_uint(-INFINITY);
+        }
+        float mg[8];
+#pragma unroll
+        for (int g8 = 0; g8 < 8; ++g8) {
+          const float* x = reinterpret_cast<const float*>(&sv[g8 * 8]);
+          mg[g8] = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+        }
+        const float mraw = fmaxf(fmaxf(fmaxf(mg[0], mg[1]), fmaxf(mg[2], mg[3])), fmaxf(fmaxf(mg[4], mg[5]), fmaxf(mg[6], mg[7])));
+        const float mx = mraw * a.scale_log2;  // -inf stays -inf (scale > 0)
+        const bool raise = mx > m_ref + kTcLazy;  // false while the row has no key
+        if (__any_sync(0xffffffffu, raise)) {
+          const float m_new = raise ? mx : m_ref;
+          const float alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - m_new);
+          if (__any_sync(0xffffffffu, raise && m_ref != -INFINITY)) {
+            // O *= alpha for this warp's rows once P.V of the previous tile is done
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.pfree[(gi - 1) & 1], ((gi - 1) >> 1) & 1, st))) {
+              ok = false;
+              break;
+            }
+            tc::fence_after();
+#pragma unroll 1
+            for (int blk = 0; blk < 8; ++blk) {
+              uint32_t o[32];
+              const uint32_t ad = tmem + lane_base + kColO + 32 * blk;
+              tc::ld32(ad, o);
+              tc::wait_ld();
+              if (raise && m_ref != -INFINITY) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              }
+              tc::st32(ad, o);
+            }
+            tc::wait_st();
+          }
+          if (raise) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) lp[i] *= alpha;
+            m_ref = m_new;
+          }
+        }
+        // ---- P row (bf16 pairs) over the S columns just read: s_ready of this
+        // tile means every earlier MMA, P.V two tiles back included, is done.
+        // p = 2^(s * scale - m): masked keys (s = -inf) give 0; a row with no
+        // key yet uses m = 0 so that no inf - inf arises
+        const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+        uint32_t pw[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const float p0 = ex2(fmaf(__uint_as_float(sv[2 * u]), a.scale_log2, neg_m));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[2 * u + 1]), a.scale_log2, neg_m));
+          __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+          lp[u & 3] += __low2float(pb) + __high2float(pb);
+          pw[u] = *reinterpret_cast<uint32_t*>(&pb);
+        }
+        tc::st32(tmem + lane_base + kColS + 64 * b, pw);
+        tc::wait_st();
+        tc::fence_before();
+        mbar_arrive(&sm.p_ready[b]);
+      }
+      if (!ok) break;
+      // ---- next work tile's Q: the last QK^T of this one is done (its S was
+      // read above); the next work tile's first QK^T then overlaps this epilogue
+      const int next = tile + gridDim.x;
+      if (next < total) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.q_free, wt & 1, st))) break;
+        tc::fence_after();
+        load_q(work_tile<G>(a, next));
+      }
+      // ---- epilogue: O / l -> bf16
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_done, wt & 1, st))) break;
+      tc::fence_after();
+      const float l = (lp[0] + lp[1]) + (lp[2] + lp[3]);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint16_t* dst = a.out + (static_cast<int64_t>(w.row0 + w.q0 + qi) * a.num_q_heads + w.g * G + hh) * 256;
+#pragma unroll 1
+      for (int blk = 0; blk < 8; blk += 2) {
+        uint32_t o[64];
+        tc::ld32(tmem + lane_base + kColO + 32 * blk, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+        tc::ld32(tmem + lane_base + kColO + 32 * blk + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+        tc::wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[c + 2 * e]) * inv,
+                                                        __uint_as_float(o[c + 2 * e + 1]) * inv);
+              pk[e] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(dst + blk * 32 + c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+      }
+      tc::fence_before();
+      mbar_arrive(&sm.o_free);
+    }
+  }
+
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc::fence_after();
+    tc::dealloc(tmem, 512);
+  }
+}
+
+// The LOCAL pool as a 3-d tensor for TMA: rows of 256 bf16 (one token of K
+// or of V of one KV head), each split into 4 chunks of 64 elements.  Row
+// index = ((page * kv_heads + head) * 2 + {0: K, 1: V}) * 16 + token.
+cudaError_t make_kv_map(const LocalArgs& a, CUtensorMap* map) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+    encode = reinterpret_cast<EncodeFn>(fn);
+  }
+  const cuuint64_t dims[3] = {64, 4, static_cast<cuuint64_t>(a.num_pages) * a.kv_heads * 2 * kPage};
+  const cuuint64_t strides[2] = {128, 512};  // bytes, dims 1 and 2
+  const cuuint32_t box[3] = {64, 1, 16};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint8_t*>(a.pool), dims, strides,
+                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int G>
+cudaError_t launch_g(const LocalArgs& a, cudaStream_t st) {
+  CUtensorMap map;
+  cudaError_t e = make_kv_map(a, &map);
+  if (e != cudaSuccess) return e;
+  auto kern = local_prompt_tc_kernel<G>;
+  const size_t smem = sizeof(TcSmem);
+  e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(num_sms()), dim3(kTcThreads), smem, st, a, map);
+}
+
+}  // namespace
+
+cudaError_t launch_local_prompt_tc(int group, const LocalArgs& a, cudaStream_t st) {
+  switch (group) {
+    case 1: return launch_g<1>(a, st);
+    case 2: return launch_g<2>(a, st);
+    case 4: return launch_g<4>(a, st);
+    case 8: return launch_g<8>(a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gw

@@ -61,6 +61,18 @@ __device__ __forceinline__ void mma_bf16_warp(uint32_t d_tmem, uint64_t adesc, u
       : "memory");
 }
 
+// As mma_bf16_warp with the A operand in tensor memory: lane i of `a_tmem`
+// holds row i, 32-bit column c holds elements 2c (low half) and 2c + 1, so
+// a K-step of 16 elements spans 8 columns.
+__device__ __forceinline__ void mma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+
 // Warp-uniform commit by the elected (issuing) lane.
 __device__ __forceinline__ void commit_warp(uint64_t* bar) {
   asm volatile(

@@ -130,3 +130,27 @@ def test_mixed_full_size_sampled(key):
               51: sorted(rng.choice(2048, 6, replace=False).tolist() + [2047])}
     mx, rl = _check(layer, out, tab, sample)
     print("mixed %s sampled worst max-abs %.3g rel-l2 %.3g" % (key, mx, rl))
+
+
+@pytest.mark.parametrize("key", ["local", "global"])
+def test_prompt_rows_with_a_bad_page_are_reported_and_stay_finite(key):
+    """A page id out of range inside a prompt's key range is reported and never
+    read; rows of that prompt stay finite (the kernel substitutes zeros), the
+    other sequences are bit-identical to a run with a valid table."""
+    sp = synth.spec("mixed")
+    lens = np.concatenate([sp.lens[:3], [200, 300]]).astype(np.int32)
+    rows = np.array([1, 1, 1, 200, 150], np.int32)
+    layer = synth.Layer(synth.custom("badp", sp.seed, 32, lens, rows, sp.families), key,
+                        layer=0 if key == "local" else 100)
+    pool, tab, status = _build(layer)
+    good = G.attend(layer, pool)
+    bt = layer.block_table.copy()
+    bt[4, 5] = layer.num_pages + 7          # inside the continuation's key range
+    layer.block_table = bt
+    status.zero_()
+    out = G.attend(layer, pool, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & gw.GW_DEV_PAGE_RANGE
+    cu = layer.cu_rows()
+    assert torch.isfinite(out[cu[4]:cu[5]].float()).all()
+    assert torch.equal(out[:cu[4]].view(torch.int16), good[:cu[4]].view(torch.int16))
