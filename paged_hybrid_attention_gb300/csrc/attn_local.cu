@@ -7,41 +7,42 @@
 // family serves an opt in fp8 KV pool", "Description": the pool may hold
 // e4m3 at scale 1.0; here it is widened to fp32 on the load path.
 //
-// Design (split-KV flash decoding on CUDA cores; a GQA group of G <= 8 query
-// heads per KV head is too narrow for a tensor-core contraction, and the
-// kernel is bound by HBM, not by arithmetic):
-//   * Work unit = (sequence, KV head, chunk of up to 4 bf16 / 8 e4m3 pages of
-//     the window).  The split depends on the sequence's own length only.
-//   * Persistent CTAs, one per SM, of independent warps: 8 for bf16, 12 for
-//     e4m3 (which spends twice the instructions per byte on conversions and
-//     is bound by issue latency, so more warps hide more of it).  Every CTA
-//     computes the batch's split plan (unit offsets) into its own shared
-//     memory, so no plan kernel and no work counter sit in front of the
-//     decode; units are dealt round-robin over the warps, SM-minor, so each
-//     round spreads evenly over the SMs.
-//   * Each warp streams 8 KiB stages (8 tokens of K and V for bf16, 16 for
-//     e4m3) with cp.async.bulk into a private 2-stage ring, prefetching
-//     across unit boundaries.
-//   * Lane l owns head dims [8l, 8l+8).  q.K partial dot products are reduced
-//     across lanes with a transpose-reduction whose token order is permuted by
-//     lane bits, so every level is one shuffle + add per value (no selects).
-//   * Products use the mixed-precision fma.rn.f32.{bf16,f16} (16-bit operands
-//     read from packed registers, fp32 accumulate), so K and V are never
-//     widened: bf16 pages multiply as stored, e4m3 pages after one paired
-//     e4m3x2 -> f16x2 conversion.  Softmax is base 2 in fp32; P is rounded to
-//     the multiplicand format and l sums exactly the rounded weights.
-//   * Each unit writes an unnormalised partial (m, l, o); a combine kernel
-//     merges a sequence's partials in chunk order (log-sum-exp) into bf16.
-#include "common.cuh"
+// Split-KV flash decoding, common to both pool types:
+//   * Work unit = (sequence, KV head, chunk of up to 8 pages of the window).
+//     The split depends on the sequence's own length only.
+//   * Persistent CTAs, one per SM, of independent warps.  Every CTA computes
+//     the batch's split plan (unit offsets) into its own shared memory, so no
+//     plan kernel and no work counter sit in front of the decode; units are
+//     dealt round-robin over the warps, SM-minor, so each round spreads evenly
+//     over the SMs.
+//   * Each warp streams its units' pages through a private 2-stage ring,
+//     prefetching across unit boundaries, and writes an unnormalised partial
+//     (m, l, o) per unit; a combine kernel merges a sequence's partials in
+//     chunk order (log-sum-exp) into bf16.
+//   * Softmax is base 2 in fp32 against a reference max; P is rounded to the
+//     multiplicand format and l sums exactly the rounded weights.
+//
+// bf16 pools (local_decode_tc_kernel, 6 warps): a stage is one 16-token page
+// head (K and V, 16 KB) brought by 8 TMA tensor copies into 128-byte-swizzled
+// shared memory; q.K^T and P.V run on warp-level tensor cores (mma.sync
+// m16n8k16, the G heads of the group as rows) with P kept in registers.
+//
+// e4m3 pools (local_decode_kernel, 12 warps for G <= 4): 8 KiB stages of 16
+// tokens with cp.async.bulk; lane l owns head dims [8l, 8l+8); products use
+// the mixed-precision fma.rn.f32.f16 after one paired e4m3x2 -> f16x2
+// conversion (no widening to fp32); q.K partial dot products are reduced
+// across lanes with a transpose-reduction whose token order is permuted by
+// lane bits (one shuffle + add per value and level).  The conversions double
+// the instructions per byte, so the kernel is bound by issue latency and runs
+// more warps than the HBM stream alone would need.
+#include "tma.cuh"
 
 namespace gw {
 namespace {
 
-// warps per CTA: 8 for bf16; e4m3 spends twice the instructions per byte and
-// is issue-latency bound, so it runs 12 (with 2-stage rings) where the
-// register budget allows (G <= 4)
+// warps per CTA of the e4m3 kernel: 12 where the register budget allows
 template <int DT, int G>
-constexpr int warps_for() { return DT == GW_KV_E4M3 && G <= 4 ? 12 : 8; }
+constexpr int warps_for() { return G <= 4 ? 12 : 8; }
 constexpr int kStageBytes = 8192;
 
 struct Unit {
@@ -101,27 +102,11 @@ __device__ __forceinline__ Unit decode_unit(const LocalArgs& a, const int32_t* u
 // with 16-bit a, b taken straight from the halves of packed registers.  The
 // product of two 16-bit floats is exact in fp32, so this equals an fp32 FMA on
 // the widened values, without spending an instruction on the widening.
-// bf16 pages multiply in bf16 (q is bf16 already); e4m3 pages are widened to
-// f16 by the paired e4m3x2 -> f16x2 conversion and multiply in f16 (q is
-// rounded to f16 once per unit, exact for |q| in the f16 normal range).
+// e4m3 pages are widened to f16 by the paired e4m3x2 -> f16x2 conversion and
+// multiply in f16 (q is rounded to f16 once per unit, exact for |q| in the
+// f16 normal range).
 template <int DT>
 struct Mix;
-template <>
-struct Mix<GW_KV_BF16> {
-  __device__ __forceinline__ static float fma(uint16_t a, uint16_t b, float c) {
-    float d;
-    asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
-    return d;
-  }
-  __device__ __forceinline__ static uint16_t from_f32(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
-  __device__ __forceinline__ static float to_f32(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
-  __device__ __forceinline__ static uint16_t from_bf16(uint16_t x) { return x; }
-  // this lane's 8 elements of a row as 4 packed pairs
-  __device__ __forceinline__ static void row(const uint8_t* base, int lane, uint32_t (&w)[4]) {
-    const uint4 v = *reinterpret_cast<const uint4*>(base + lane * 16);
-    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-  }
-};
 template <>
 struct Mix<GW_KV_E4M3> {
   __device__ __forceinline__ static float fma(uint16_t a, uint16_t b, float c) {
@@ -413,6 +398,289 @@ __global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kerne
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// bf16 pages on warp-level tensor cores (mma.sync), fed by TMA.  A stage is
+// one 16-token page head: K (4 chunks x 16 rows x 128 B) and V (same), 16 KB
+// copied as 8 tensor boxes of 2 KB issued by 8 lanes, landing 128-byte
+// swizzled so that every ldmatrix below reads 8 distinct bank groups.
+//   S[16 x 16]   = Q[16 x 256] . K^T      (m16n8k16 x 2 token halves; rows
+//                                          = the G heads of the KV head)
+//   O^T[256 x 8] += V^T[256 x 16] . P^T   (m16n8k16; columns = heads)
+// The accumulator layout of S (lane: head lane/4, tokens 2(lane%4)+{0,1} of
+// each half) is the B-operand layout of P^T, so the weights stay in
+// registers; about 60 warp instructions per 16 tokens instead of ~700.
+constexpr int kTcWarps = 6;
+constexpr int kTcStages = 2;
+constexpr int kTcStage = 16384;  // K 8 KB then V 8 KB
+
+struct __align__(1024) TcWarpSmem {
+  uint8_t stage[kTcStages][kTcStage];
+  uint64_t bar[kTcStages];
+  int32_t valid[kTcStages];
+  Unit ring[kTcStages + 2];
+};
+
+struct TcTraits {
+  static constexpr int kTok = 16;  // tokens per stage
+  static constexpr int kChunk = kLocalChunkPagesBf16;
+};
+
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// d += a . b with a 16 x 16 (rows 8..15 zero: a1 = a3 = 0), b 16 x 8
+__device__ __forceinline__ void hmma_q(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void hmma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kTcWarps * 32, 1)
+    local_decode_tc_kernel(const LocalArgs a, const __grid_constant__ CUtensorMap kv_map) {
+  using T = TcTraits;
+  constexpr int kTok = T::kTok;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  TcWarpSmem& sm = reinterpret_cast<TcWarpSmem*>(smem_raw)[warp];
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < kTcStages; ++i) mbar_init(&sm.bar[i], 1);
+    fence_mbar_init();
+  }
+  int32_t* ub = reinterpret_cast<int32_t*>(smem_raw + sizeof(TcWarpSmem) * kTcWarps);
+  pdl_wait();
+  pdl_trigger();
+  plan_in_smem<T::kChunk>(a, ub, ub + kLocalMaxBatch + 1);
+  const int total_units = ub[a.batch];
+  if (total_units > a.max_units) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.status, GW_DEV_WORKSPACE);
+    return;
+  }
+  const uint64_t pol = policy_evict_first();
+  const int n_warps = gridDim.x * kTcWarps;
+  int next_u = warp * gridDim.x + blockIdx.x;
+  constexpr int kRing = kTcStages + 2;
+
+  int f_slot = 0, f_i = 0;
+  bool f_done = false;
+  uint32_t issued = 0, consumed = 0;
+
+  auto grab = [&](int slot) -> bool {
+    const int u = next_u;
+    next_u += n_warps;
+    if (u >= total_units) return false;
+    const Unit d = decode_unit<T>(a, ub, u);
+    if (lane == 0) sm.ring[slot] = d;
+    __syncwarp();
+    return true;
+  };
+
+  auto issue = [&]() {
+    const Unit d = sm.ring[f_slot];
+    const int st = issued % kTcStages;
+    const int lp = d.hp_lo + f_i;  // one page per stage
+    int32_t phys = 0;
+    if (lane == 0) phys = a.block_table[static_cast<int64_t>(d.s) * a.max_pages + lp];
+    phys = __shfl_sync(0xffffffffu, phys, 0);
+    if (phys < 0 || phys >= a.num_pages) {
+      if (lane == 0) {
+        sm.valid[st] = 0;
+        set_status(a.status, GW_DEV_PAGE_RANGE);
+        mbar_arrive(&sm.bar[st]);
+      }
+    } else {
+      if (lane == 0) {
+        sm.valid[st] = 1;
+        mbar_arrive_expect_tx(&sm.bar[st], kTcStage);
+      }
+      __syncwarp();
+      if (lane < 8) {
+        // lane: K (0-3) or V (4-7), 64-dim chunk lane % 4
+        const int kv = lane >> 2, c = lane & 3;
+        tma_rows(smem_u32(sm.stage[st]) + kv * 8192 + c * 2048, &kv_map, c,
+                 ((phys * a.kv_heads + d.g) * 2 + kv) * kPage, &sm.bar[st], pol);
+      }
+    }
+    ++issued;
+    if (++f_i == d.n) {
+      f_i = 0;
+      f_slot = (f_slot + 1) % kRing;
+      f_done = !grab(f_slot);
+    }
+  };
+
+  f_done = !grab(0);
+  while (!f_done && issued - consumed < kTcStages) issue();
+
+  const int hq = lane >> 2;        // S row (q head of the group) this lane holds
+  const int kq = (lane & 3) * 2;   // first of its two S columns in each token half
+  uint32_t qa[16][2];              // A fragments of Q: dims 16s + kq + {0,1} and 16s + 8 + kq + {0,1}
+  float o[16][4];                  // O^T: dims 16j + lane/4 (+8) x heads kq, kq + 1
+  float m_ref = -INFINITY, lsum = 0.f;
+  int c_slot = 0, c_i = 0;
+  while (consumed < issued) {
+    const Unit d = sm.ring[c_slot];
+    if (c_i == 0) {
+      if (hq < G) {
+        const uint32_t* qrow =
+            reinterpret_cast<const uint32_t*>(a.q + (static_cast<int64_t>(d.row) * a.num_q_heads + d.g * G + hq) * 256);
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+          qa[s][0] = qrow[(16 * s + kq) >> 1];
+          qa[s][1] = qrow[(16 * s + 8 + kq) >> 1];
+        }
+      } else {
+#pragma unroll
+        for (int s = 0; s < 16; ++s) qa[s][0] = qa[s][1] = 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+      m_ref = -INFINITY;
+      lsum = 0.f;
+    }
+    const int st = consumed % kTcStages;
+    if (!mbar_wait(&sm.bar[st], (consumed / kTcStages) & 1, a.status)) {
+      for (uint32_t k = consumed + 1; k < issued; ++k) mbar_wait(&sm.bar[k % kTcStages], (k / kTcStages) & 1, nullptr);
+      return;
+    }
+    const uint32_t kb = smem_u32(sm.stage[st]), vb = kb + 8192;
+    const int t0 = (d.hp_lo + c_i) * kTok;
+    const bool stage_ok = sm.valid[st] != 0;
+
+    // ---- S = Q . K^T for the two 8-token halves
+    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2) {  // 32 dims: chunk s2 / 2, units (s2 % 2) * 4 + 0..3
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t b[4];
+        const int row = h * 8 + (lane & 7);
+        ldsm4(kb + (s2 >> 1) * 2048 + sw128(row, (s2 & 1) * 4 + (lane >> 3)), b);
+        hmma_q(sacc[h], qa[2 * s2][0], qa[2 * s2][1], b[0], b[1]);
+        hmma_q(sacc[h], qa[2 * s2 + 1][0], qa[2 * s2 + 1][1], b[2], b[3]);
+      }
+    }
+
+    // ---- online softmax (base 2) against a lazily raised reference max
+    float sv[2][2];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tk = t0 + h * 8 + kq + e;
+        const bool ok = stage_ok && hq < G && tk >= d.tok_lo && tk < d.tok_hi;
+        sv[h][e] = ok ? sacc[h][e] * a.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sv[h][e]);
+      }
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const bool raise = mx > m_ref + 8.f;
+    if (__any_sync(0xffffffffu, raise)) {
+      const float m_new = raise ? mx : m_ref;
+      const float alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - m_new);
+      m_ref = m_new;
+      lsum *= alpha;
+      const float aa = __shfl_sync(0xffffffffu, alpha, (lane & 3) * 8);
+      const float ab = __shfl_sync(0xffffffffu, alpha, (lane & 3) * 8 + 4);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        o[j][0] *= aa;
+        o[j][1] *= ab;
+        o[j][2] *= aa;
+        o[j][3] *= ab;
+      }
+    }
+    uint32_t pb[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      pb[h] = pack2_bf16(sv[h][0] == -INFINITY ? 0.f : ex2(sv[h][0] - m_ref),
+                         sv[h][1] == -INFINITY ? 0.f : ex2(sv[h][1] - m_ref));
+      lsum += __uint_as_float(pb[h] << 16) + __uint_as_float(pb[h] & 0xFFFF0000u);
+    }
+
+    // ---- O^T += V^T . P^T; V rows of tokens outside the unit are cleared
+    // first (their bytes may be anything, even NaN patterns)
+    if (stage_ok) {
+      if (t0 < d.tok_lo || t0 + kTok > d.tok_hi) {
+        for (int r = 0; r < kTok; ++r) {
+          if (t0 + r >= d.tok_lo && t0 + r < d.tok_hi) continue;
+          *reinterpret_cast<uint4*>(sm.stage[st] + 8192 + (lane >> 3) * 2048 + r * 128 + (lane & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // ordered before the next TMA into this stage
+        __syncwarp();
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {  // dims 16j..16j+15: chunk j / 4, units (j % 4) * 2 + {0, 1}
+        uint32_t v[4];
+        const int m = lane >> 3;
+        const int row = (m >> 1) * 8 + (lane & 7);
+        ldsm4_t(vb + (j >> 2) * 2048 + sw128(row, (j & 3) * 2 + (m & 1)), v);
+        hmma(o[j], v, pb[0], pb[1]);
+      }
+    }
+    __syncwarp();
+    ++consumed;
+    if (++c_i == d.n) {
+      // ---- unit done: write the unnormalised partial (m, l, o)
+      float l = lsum + __shfl_xor_sync(0xffffffffu, lsum, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      if ((lane & 3) == 0 && hq < G) a.part_ml[static_cast<int64_t>(d.unit) * G + hq] = make_float2(m_ref, l);
+      float* po = a.part_o + static_cast<int64_t>(d.unit) * G * 256 + (lane >> 2);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (kq < G) {
+          po[kq * 256 + 16 * j] = o[j][0];
+          po[kq * 256 + 16 * j + 8] = o[j][2];
+        }
+        if (kq + 1 < G) {
+          po[(kq + 1) * 256 + 16 * j] = o[j][1];
+          po[(kq + 1) * 256 + 16 * j + 8] = o[j][3];
+        }
+      }
+      c_i = 0;
+      c_slot = (c_slot + 1) % kRing;
+    }
+    while (!f_done && issued - consumed < kTcStages) issue();
+  }
+}
+
+template <int G>
+cudaError_t launch_tc(const LocalArgs& a, cudaStream_t st) {
+  CUtensorMap map;
+  cudaError_t e = make_local_kv_map(a, &map);
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(TcWarpSmem) * kTcWarps + sizeof(int32_t) * (kLocalMaxBatch + 1 + 32);
+  auto kern = local_decode_tc_kernel<G>;
+  e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(kern, dim3(num_sms()), dim3(kTcWarps * 32), smem, st, a, map);
+  if (e != cudaSuccess) return e;
+  return launch_combine(a, kSplitLocal, G, 256, TcTraits::kChunk, st);
+}
+
 template <int DT, int G>
 cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   using T = Traits<DT>;
@@ -429,13 +697,23 @@ cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
 
 template <int DT>
 cudaError_t launch_dt(int group, const LocalArgs& a, cudaStream_t st) {
-  switch (group) {
-    case 1: return launch_typed<DT, 1>(a, st);
-    case 2: return launch_typed<DT, 2>(a, st);
-    case 4: return launch_typed<DT, 4>(a, st);
-    case 8: return launch_typed<DT, 8>(a, st);
+  if constexpr (DT == GW_KV_BF16) {
+    switch (group) {
+      case 1: return launch_tc<1>(a, st);
+      case 2: return launch_tc<2>(a, st);
+      case 4: return launch_tc<4>(a, st);
+      case 8: return launch_tc<8>(a, st);
+    }
+    return cudaErrorInvalidValue;
+  } else {
+    switch (group) {
+      case 1: return launch_typed<DT, 1>(a, st);
+      case 2: return launch_typed<DT, 2>(a, st);
+      case 4: return launch_typed<DT, 4>(a, st);
+      case 8: return launch_typed<DT, 8>(a, st);
+    }
+    return cudaErrorInvalidValue;
   }
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace

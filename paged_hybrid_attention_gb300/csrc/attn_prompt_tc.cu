@@ -35,9 +35,8 @@
 //   warps 4, 6 TMA producers of K and of V tiles (16 lanes issue a tile's copies)
 //   warp 5     MMA issue (elect.sync) and TMEM owner
 // Every wait is bounded; a timeout raises GW_DEV_TIMEOUT and the CTA stops.
-#include <cuda.h>
-
 #include "tcgen05.cuh"
+#include "tma.cuh"
 namespace gw {
 namespace {
 
@@ -62,16 +61,6 @@ struct TcSmem {
 
 __device__ __forceinline__ void zero16(uint32_t dst) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0) : "memory");
-}
-
-// TMA: box {64 elements, 1 chunk, 16 rows} of the KV map -> 2 KB at dst.
-__device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap* map, int chunk, int row, uint64_t* bar,
-                                         uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(chunk), "r"(row), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
 }
 
 // Shared-memory descriptor of a 128-byte-swizzled operand (atoms of 8 rows x
@@ -162,7 +151,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // warp 4 loads K tiles, warp 6 V tiles; lane l < 16 issues the copy of
     // page l / 4, 64-dim chunk l % 4 (the 16 copies of a tile go out together)
     const bool is_v = warp == 6;
-    const uint64_t pol = policy_evict_first();
+    // every K/V tile is read again by the neighbouring query blocks (a window
+    // of W keys is shared by W / 64 of them): keep it in L2 (evict last)
+    const uint64_t pol = policy_evict_last();
     const int j = lane >> 2, c = lane & 3;
     uint32_t gi = 0;
     bool ok = true;
@@ -435,35 +426,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// The LOCAL pool as a 3-d tensor for TMA: rows of 256 bf16 (one token of K
-// or of V of one KV head), each split into 4 chunks of 64 elements.  Row
-// index = ((page * kv_heads + head) * 2 + {0: K, 1: V}) * 16 + token.
-cudaError_t make_kv_map(const LocalArgs& a, CUtensorMap* map) {
-  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-  static EncodeFn encode = nullptr;
-  if (!encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
-    encode = reinterpret_cast<EncodeFn>(fn);
-  }
-  const cuuint64_t dims[3] = {64, 4, static_cast<cuuint64_t>(a.num_pages) * a.kv_heads * 2 * kPage};
-  const cuuint64_t strides[2] = {128, 512};  // bytes, dims 1 and 2
-  const cuuint32_t box[3] = {64, 1, 16};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint8_t*>(a.pool), dims, strides,
-                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int G>
 cudaError_t launch_g(const LocalArgs& a, cudaStream_t st) {
   CUtensorMap map;
-  cudaError_t e = make_kv_map(a, &map);
+  cudaError_t e = make_local_kv_map(a, &map);
   if (e != cudaSuccess) return e;
   auto kern = local_prompt_tc_kernel<G>;
   const size_t smem = sizeof(TcSmem);

@@ -95,6 +95,13 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// L2 policy for data read many times in a short span (prompt-row K/V tiles).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // L2 policy for data read exactly once (KV pages): evict first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

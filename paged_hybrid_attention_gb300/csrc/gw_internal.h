@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/gw.h"
@@ -14,7 +15,7 @@ namespace gw {
 // logical pages of that sequence's window); a global unit is (sequence, chunk
 // of global_chunk_pages(L) pages).  Chunks depend only on the sequence's own
 // length, so a row's arithmetic never depends on the rest of the batch.
-constexpr int kLocalChunkPagesBf16 = 4;
+constexpr int kLocalChunkPagesBf16 = 8;
 constexpr int kLocalChunkPagesE4m3 = 8;
 // Global chunks start at 16 pages and double until a sequence has at most
 // kGlobalMaxChunks of them (long contexts get long chunks, so the partials
@@ -114,6 +115,11 @@ cudaError_t launch_combine(const LocalArgs& a, int mode, int heads_per_unit, int
 
 cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_bw_probe(const void* buf, int64_t chunks, int32_t* status, cudaStream_t st);
+// TMA descriptor of a bf16 LOCAL pool (rows of 256 elements in 4 chunks of 64;
+// row = ((page * kv_heads + head) * 2 + {K, V}) * 16 + token), box {64, 1, 16},
+// 128-byte swizzle.
+constexpr int kPageTokens = 16;
+cudaError_t make_local_kv_map(const LocalArgs& a, CUtensorMap* map);
 cudaError_t launch_local_decode(int dtype, int group, const LocalArgs& a, cudaStream_t st);
 cudaError_t launch_global_decode(int layout, const LocalArgs& a, cudaStream_t st);
 cudaError_t launch_local_prompt(int dtype, int group, const LocalArgs& a, int max_q_rows, cudaStream_t st);
