@@ -52,6 +52,7 @@ UNIT = "GB/s"
 # workload: (bytes, source file under csrc/, sha256)
 NCU_TRAFFIC = {
     "serving": (276518656, "attn_local.cu", "82c5752574d5b32d5d0c95830508037f3c14ebf9196eba63554f5dd163371e35"),
+    "fp8_local": (552995840, "attn_local.cu", "82c5752574d5b32d5d0c95830508037f3c14ebf9196eba63554f5dd163371e35"),
 }
 
 
