@@ -63,7 +63,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="serving",
-                    help="serving (default), fp8_local, long_global, long_global_full, mixed")
+                    help="serving (default), fp8_local, long_global, long_global_full, mixed, chunked, stack48")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch every step eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu", action="store_true")

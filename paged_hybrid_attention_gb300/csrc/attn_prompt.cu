@@ -172,7 +172,9 @@ __global__ void __launch_bounds__(kGlobalThreads, 1) global_prompt_kernel(const 
   fence_proxy_async_smem();
   __syncthreads();
   uint32_t uses[2] = {0, 0};  // completed phases per buffer
-  const uint64_t pol = policy_evict_first();
+  // a key's page is read again by every later query block of the prompt:
+  // keep the pages in L2 (evict last)
+  const uint64_t pol = policy_evict_last();
 
   for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
     const int s = find_seq(a.prompt_base, a.batch, tile);

@@ -18,6 +18,11 @@ layers per global layer):
   long_global 8 slots at L = 131072, global only, folded vs full control.
   mixed       48 decode streams, L ~ U[1024, 16384], plus 4 new prompts of 2048
               rows appended and attended in the same step; both families.
+  chunked     32 decode streams, L ~ U[1024, 16384], plus 4 prompts continuing
+              with a 1024-row chunk over U[4096, 16384] cached tokens (the
+              chunked walk); both families.
+  stack48     the serving shapes over a 48-layer stack (40 local + 8 global
+              layers, each with its own pools).
 
 Every sequence's tensors come from their own generator seed, so one sequence
 can be regenerated alone (the oracle checks samples of the big workloads).
@@ -95,6 +100,17 @@ def spec(name):
         loc = Family("local", "bf16", "local", 16, 256, 256, 1e4, 1024)
         glo = Family("global", "bf16", "folded", 1, 512, 128, 1e6, 0)
         return Spec(name, 1005, 32, lens, rows, {"local": loc, "global": glo}, 5, 1)
+    if name == "chunked":
+        dec = _draw_lens(1006, 32, 1024, 16384)
+        hist = _draw_lens(1106, 4, 4096, 16384)
+        lens = np.concatenate([dec, hist + 1024]).astype(np.int32)
+        rows = np.concatenate([np.ones(32, np.int32), np.full(4, 1024, np.int32)])
+        loc = Family("local", "bf16", "local", 16, 256, 256, 1e4, 1024)
+        glo = Family("global", "bf16", "folded", 1, 512, 128, 1e6, 0)
+        return Spec(name, 1006, 32, lens, rows, {"local": loc, "global": glo}, 5, 1)
+    if name == "stack48":
+        base = spec("serving")
+        return Spec(name, base.seed, base.num_q_heads, base.lens, base.n_rows, base.families, 40, 8)
     raise KeyError(name)
 
 

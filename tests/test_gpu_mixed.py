@@ -132,6 +132,24 @@ def test_mixed_full_size_sampled(key):
     print("mixed %s sampled worst max-abs %.3g rel-l2 %.3g" % (key, mx, rl))
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("key", ["local", "global"])
+def test_chunked_continuation_full_size_sampled(key):
+    """Prompt chunks of 1024 rows continuing over 4k-16k cached tokens (the
+    chunked walk), next to 32 decode streams, sampled against the oracle."""
+    layer = synth.Layer(synth.spec("chunked"), key)
+    pool, tab, status = _build(layer)
+    out = G.attend(layer, pool, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rng = np.random.Generator(np.random.PCG64(4))
+    sample = {0: [0], 31: [0],
+              32: sorted(rng.choice(1024, 6, replace=False).tolist() + [0, 1023]),
+              35: sorted(rng.choice(1024, 4, replace=False).tolist() + [511])}
+    mx, rl = _check(layer, out, tab, sample)
+    print("chunked %s sampled worst max-abs %.3g rel-l2 %.3g" % (key, mx, rl))
+
+
 @pytest.mark.parametrize("key", ["local", "global"])
 def test_prompt_rows_with_a_bad_page_are_reported_and_stay_finite(key):
     """A page id out of range inside a prompt's key range is reported and never
