@@ -30,10 +30,11 @@
 //     O at 256..511.
 //     V rows of keys outside the tile's range are cleared before P.V (0 *
 //     anything must stay 0), K rows of pages not loaded before Q.K^T.
-// Warp roles (224 threads, persistent CTAs):
+// Warp roles (256 threads, persistent CTAs):
 //   warps 0-3  load Q rows, softmax, epilogue (warp w owns TMEM lanes 32w..)
 //   warps 4, 6 TMA producers of K and of V tiles (16 lanes issue a tile's copies)
-//   warp 5     MMA issue (elect.sync) and TMEM owner
+//   warp 5     Q.K^T issue (elect.sync) and TMEM owner
+//   warp 7     P.V issue, so that neither contraction's issue waits on the other
 // Every wait is bounded; a timeout raises GW_DEV_TIMEOUT and the CTA stops.
 #include "tcgen05.cuh"
 #include "tma.cuh"
@@ -42,7 +43,7 @@ namespace {
 
 constexpr int kTM = 128;              // rows per work tile (UMMA M)
 constexpr int kTN = 64;               // keys per key tile (UMMA N of S)
-constexpr int kTcThreads = 224;
+constexpr int kTcThreads = 256;
 constexpr float kTcLazy = 8.f;
 // TMEM columns: S buffers at 0 and 64, Q at 128..255, O at 256..511
 constexpr uint32_t kColS = 0, kColQ = 128, kColO = 256;
@@ -194,40 +195,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issue
+    // ---------------------------------------------------- Q.K^T issue
     const uint32_t id_s = tc::idesc_bf16(kTM, kTN, false, false);
-    const uint32_t id_o = tc::idesc_bf16(kTM, 256, false, true);
     uint32_t gi = 0;
     int wt = 0;
     bool ok = true;
-    auto pv = [&](uint32_t i, int key0, const WorkTile& w, bool first_of_tile, bool last_of_tile) -> bool {
-      const int b = static_cast<int>(i % kVS);
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.vfull[b], (i / kVS) & 1, st))) return false;
-      // V rows of keys outside [lo, hi] or of pages not loaded: clear them
-      const int mask = sm.vmask[b];
-      if (mask != 0xF || key0 < w.lo || key0 + kTN - 1 > w.hi) {
-        const uint32_t vb = smem_u32(sm.v[b]);
-        for (int kr = 0; kr < kTN; ++kr) {
-          const int key = key0 + kr;
-          if (((mask >> (kr >> 4)) & 1) && key >= w.lo && key <= w.hi) continue;
-          zero16(vb + (lane >> 3) * kPlane + kr * 128 + (lane & 7) * 16);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      const int sb = i & 1;  // S / P buffer in tensor memory
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_ready[sb], (i >> 1) & 1, st))) return false;
-      tc::fence_after();
-      const uint32_t va = smem_u32(sm.v[b]);
-#pragma unroll
-      for (int kk = 0; kk < kTN / 16; ++kk)
-        tc::mma_bf16_ts_warp(tmem + kColO, tmem + kColS + 64 * sb + 8 * kk, sw128_desc(va + kk * 2048, kPlane), id_o,
-                             !(first_of_tile && kk == 0));
-      tc::commit_warp(&sm.vempty[b]);
-      tc::commit_warp(&sm.pfree[sb]);
-      if (last_of_tile) tc::commit_warp(&sm.o_done);
-      return true;
-    };
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++wt) {
       const WorkTile w = work_tile<G>(a, tile);
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.q_full, wt & 1, st))) break;
@@ -235,6 +207,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int j = 0; j < nt; ++j, ++gi) {
         const int b = static_cast<int>(gi % kKS), sb = gi & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(&sm.kfull[b], (gi / kKS) & 1, st))) { ok = false; break; }
+        // this S buffer holds P of tile gi - 2 until its P.V is done
+        if (gi >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sm.pfree[sb], ((gi >> 1) - 1) & 1, st))) {
+          ok = false;
+          break;
+        }
         const uint32_t ka = smem_u32(sm.k[b]);
         const int kmask = sm.kmask[b];
         if (kmask != 0xF) {
@@ -256,14 +233,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::commit_warp(&sm.kempty[b]);
         tc::commit_warp(&sm.s_ready[sb]);
         if (j == nt - 1) tc::commit_warp(&sm.q_free);
+      }
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------- P.V issue
+    const uint32_t id_o = tc::idesc_bf16(kTM, 256, false, true);
+    uint32_t gi = 0;
+    int wt = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++wt) {
+      const WorkTile w = work_tile<G>(a, tile);
+      const int nt = w.t_hi - w.t_lo + 1;
+      for (int j = 0; j < nt; ++j, ++gi) {
+        const int b = static_cast<int>(gi % kVS), sb = gi & 1;
         if (j == 0 && wt >= 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.o_free, (wt - 1) & 1, st))) {
           ok = false;
           break;
         }
-        if (j >= 1 && !pv(gi - 1, (w.t_lo + j - 1) * kTN, w, j == 1, false)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.vfull[b], (gi / kVS) & 1, st))) { ok = false; break; }
+        // V rows of keys outside [lo, hi] or of pages not loaded: clear them
+        const int key0 = (w.t_lo + j) * kTN;
+        const int mask = sm.vmask[b];
+        if (mask != 0xF || key0 < w.lo || key0 + kTN - 1 > w.hi) {
+          const uint32_t vb = smem_u32(sm.v[b]);
+          for (int kr = 0; kr < kTN; ++kr) {
+            const int key = key0 + kr;
+            if (((mask >> (kr >> 4)) & 1) && key >= w.lo && key <= w.hi) continue;
+            zero16(vb + (lane >> 3) * kPlane + kr * 128 + (lane & 7) * 16);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_ready[sb], (gi >> 1) & 1, st))) { ok = false; break; }
+        tc::fence_after();
+        const uint32_t va = smem_u32(sm.v[b]);
+#pragma unroll
+        for (int kk = 0; kk < kTN / 16; ++kk)
+          tc::mma_bf16_ts_warp(tmem + kColO, tmem + kColS + 64 * sb + 8 * kk, sw128_desc(va + kk * 2048, kPlane),
+                               id_o, !(j == 0 && kk == 0));
+        tc::commit_warp(&sm.vempty[b]);
+        tc::commit_warp(&sm.pfree[sb]);
+        if (j == nt - 1) tc::commit_warp(&sm.o_done);
       }
-      if (!ok) break;
-      if (!pv(gi - 1, w.t_hi * kTN, w, nt == 1, true)) break;
     }
   } else {
     // ---------------------------------------- Q rows, softmax, epilogue

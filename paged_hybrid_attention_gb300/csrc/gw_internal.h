@@ -126,6 +126,9 @@ cudaError_t launch_local_prompt(int dtype, int group, const LocalArgs& a, int ma
 // tcgen05 prompt-row kernel for local layers (bf16 pools); expects a.prompt_base
 // planned with 128 / group queries per tile
 cudaError_t launch_local_prompt_tc(int group, const LocalArgs& a, cudaStream_t st);
+// tcgen05 prompt-row kernel for global layers; expects a.prompt_base planned
+// with 2 tiles (output-dim halves) per block of 128 / num_q_heads queries
+cudaError_t launch_global_prompt_tc(int layout, const LocalArgs& a, cudaStream_t st);
 cudaError_t launch_global_prompt(int layout, const LocalArgs& a, int max_q_rows, cudaStream_t st);
 
 }  // namespace gw
