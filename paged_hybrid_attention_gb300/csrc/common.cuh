@@ -89,12 +89,6 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
-// Prefetch [src, src + bytes) into L2 (no completion tracking); 16-byte
-// aligned address, size a multiple of 16.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // L2 policy for data read many times in a short span (prompt-row K/V tiles).
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
@@ -122,21 +116,6 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& w, float (&f)[8]) {
   for (int i = 0; i < 4; ++i) {
     f[2 * i] = __uint_as_float(u[i] << 16);
     f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ void e4m3x8_to_f32(const uint2& w, float (&f)[8]) {
-  const uint32_t u[2] = {w.x, w.y};
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[i] & 0xFFFFu), __NV_E4M3);
-    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[i] >> 16), __NV_E4M3);
-    float2 a = __half22float2(*reinterpret_cast<__half2*>(&lo));
-    float2 b = __half22float2(*reinterpret_cast<__half2*>(&hi));
-    f[4 * i + 0] = a.x;
-    f[4 * i + 1] = a.y;
-    f[4 * i + 2] = b.x;
-    f[4 * i + 3] = b.y;
   }
 }
 
