@@ -190,8 +190,9 @@ gw_status gw_decode_attn_local(const gw_kv_pool* pool, const void* q, void* out,
  *
  * [pegainfer] "Architecture notes"; [Gewell] "the Why".  On a FOLDED pool the
  * kernel forms K_j = k_rot_j || V_j[128:512] on chip from the same page tile
- * that supplies V_j.  num_q_heads must be 8, 16 or 32.  Errors as above;
- * GW_ERR_UNSUPPORTED for an e4m3 pool ("supports only local").
+ * that supplies V_j.  num_q_heads must be 8, 16 or 32 and batch at most
+ * 4096.  Errors as above; GW_ERR_UNSUPPORTED for an e4m3 pool ("supports
+ * only local").
  */
 gw_status gw_decode_attn_global(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,
                                 int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,

@@ -17,20 +17,25 @@
 //   O^T[512 x HQ]   += V_tile^T[512 x 64] . P^T      (UMMA M=128 x4, N=HQ, K=16 per page)
 // with fp32 accumulators in tensor memory.
 //
-// Warp roles (224 threads, one persistent CTA per SM):
+// Warp roles (256 threads, one persistent CTA per SM):
 //   warps 0-3  softmax + epilogue: warp w owns TMEM lanes [32w, 32w+32), i.e.
 //              tokens [16w, 16w+16) of the tile (the M=64 accumulator uses
 //              lanes 0-15 of each 32-lane quadrant) and dims of O^T.
-//   warp 4     producer: takes split-KV units (sequence, chunk of pages) from
-//              an atomic counter and streams whole pages with cp.async.bulk
-//              into a double-buffered 4-page tile (single buffer for the full
-//              K+V control layout, whose pages are 1.6x larger).
-//   warp 5     MMA issuer (one thread) and TMEM owner.
-//   warp 6     loads each unit's q rows into the K-major Q operand.
-// Softmax is base 2 with a lazily updated reference max: a tile only
-// rescales the accumulators when some logit exceeds the reference by more
-// than 8 (p <= 256 otherwise), which after a unit's first tile is rare.
-// Each unit writes an unnormalised partial (m, l, o) for the shared combine.
+//   warp 4     producer: walks the CTA's split-KV units (sequence, chunk of
+//              pages; dealt round-robin from the in-kernel plan) and streams
+//              whole pages with cp.async.bulk into a double-buffered 4-page
+//              tile (single buffer for the full K+V control layout, whose
+//              pages are 1.6x larger).  Lanes 0-3 fetch the next tile's page
+//              numbers while the producer waits for a free buffer, and issue
+//              one page copy each.
+//   warp 5     QK^T issue and TMEM owner.
+//   warp 6     loads each unit's q rows into the K-major Q operand as soon as
+//              the previous unit's last QK^T has completed, and prefetches
+//              the next unit's rows into L2.
+//   warp 7     P.V issue.
+// QK^T and P.V are issued by different warps so that QK^T of the next tile
+// never waits behind the softmax of the current one.
+#include "plan.cuh"
 #include "tcgen05.cuh"
 
 namespace gw {
@@ -38,7 +43,7 @@ namespace {
 
 constexpr int kTilePages = 4;  // 64 tokens = UMMA M for QK^T
 constexpr int kRing = 4;       // tile descriptors in flight
-constexpr int kThreads = 224;
+constexpr int kThreads = 256;
 constexpr float kLazyThreshold = 8.f;
 
 template <int LAYOUT>
@@ -84,7 +89,10 @@ struct GSmem {
   uint64_t s_ready[2], p_ready[2], pfree[2], o_done[2], o_free[2], q_ready, q_free;
   uint32_t tmem_base;
   int32_t flag;
+  int32_t ub[kMaxBatch + 1 + 32];  // split plan (+ scan scratch)
 };
+static_assert(sizeof(GSmem<GW_LAYOUT_GLOBAL_FOLDED, 32>) <= 232448, "shared memory of one CTA");
+static_assert(sizeof(GSmem<GW_LAYOUT_GLOBAL_FULL, 32>) <= 232448, "shared memory of one CTA");
 
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -136,8 +144,12 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
   }
   pdl_wait();
   pdl_trigger();
-  const int total_units = a.unit_base[a.batch];
-  if (total_units > a.max_units) return;  // uniform; nothing allocated yet
+  plan_in_smem(a, sm.ub, sm.ub + kMaxBatch + 1, [](int L) { return global_chunks(L); });
+  const int total_units = sm.ub[a.batch];
+  if (total_units > a.max_units) {  // uniform; nothing allocated yet
+    if (blockIdx.x == 0 && tid == 0) set_status(st, GW_DEV_WORKSPACE);
+    return;
+  }
   if (warp == 5) {
     tc::alloc(&sm.tmem_base, 512);
     tc::relinquish();
@@ -151,101 +163,114 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
 
   if (warp == 4) {
     // ------------------------------------------------------------- producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      uint32_t fill = 0;
-      bool stop = false;
-      while (!stop) {
-        const int u = atomicAdd(a.counter, 1);
-        const bool end = u >= total_units;
-        int s = 0, L = 0, p0 = 0, p1 = 0, ntiles = 1, q_row = 0;
-        if (!end) {
-          int lo = 0, hi = a.batch;
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.unit_base[mid] <= u) lo = mid; else hi = mid - 1;
-          }
-          s = lo;
-          L = a.seq_lens[s];
-          const int cpg = global_chunk_pages(L);
-          p0 = (u - a.unit_base[s]) * cpg;
-          p1 = min(p0 + cpg, (L + kPage - 1) / kPage);
-          ntiles = (p1 - p0 + kTilePages - 1) / kTilePages;
-          q_row = a.cu_q_rows[s];
+    const uint64_t pol = policy_evict_first();
+    int u = blockIdx.x;
+    int s = 0, p0 = 0, p1 = 0, ntiles = 0, q_row = 0, L = 0, t = 0;
+    auto unit_info = [&]() {
+      s = plan_seq(sm.ub, a.batch, u);
+      L = a.seq_lens[s];
+      q_row = a.cu_q_rows[s];
+      const int cpg = global_chunk_pages(L);
+      p0 = (u - sm.ub[s]) * cpg;
+      p1 = min(p0 + cpg, (L + kPage - 1) / kPage);
+      ntiles = (p1 - p0 + kTilePages - 1) / kTilePages;
+    };
+    // lanes 0-3: physical page of page `lane` of tile t (raw; checked after
+    // the buffer wait so that the load's latency hides behind it)
+    auto fetch_page = [&](bool& in_unit) -> int32_t {
+      const int lp = p0 + t * kTilePages + lane;
+      in_unit = lane < kTilePages && lp < p1;
+      return in_unit ? a.block_table[static_cast<int64_t>(s) * a.max_pages + lp] : -1;
+    };
+    bool end = u >= total_units;
+    if (!end) unit_info();
+    bool in_unit = false;
+    int32_t pg = end ? -1 : fetch_page(in_unit);
+    for (uint32_t fill = 0;; ++fill) {
+      const int b = fill % NB;
+      if (fill >= NB && !warp_wait(&sm.empty[b], ((fill / NB) - 1) & 1, st)) break;
+      const bool ok = in_unit && pg >= 0 && pg < a.num_pages;
+      if (in_unit && !ok) set_status(st, GW_DEV_PAGE_RANGE);
+      const uint32_t mask = __ballot_sync(0xffffffffu, ok);
+      if (lane == 0) {
+        TileDesc d{};
+        if (end) {
+          d.flags = kEnd;
+        } else {
+          d.unit = u;
+          d.s = s;
+          d.q_row = q_row;
+          d.L = L;
+          d.tok0 = (p0 + t * kTilePages) * kPage;
+          d.ntiles = ntiles;
+          d.flags = (t == 0 ? kFirst : 0) | (t == ntiles - 1 ? kLast : 0) | static_cast<int>(mask << 8);
         }
-        for (int t = 0; t < ntiles; ++t) {
-          const int b = fill % NB;
-          if (fill >= NB && !mbar_wait(&sm.empty[b], ((fill / NB) - 1) & 1, st)) {
-            stop = true;
-            break;
-          }
-          TileDesc d{};
-          int phys[kTilePages];
-          uint32_t bytes = 0;
-          if (end) {
-            d.flags = kEnd;
-          } else {
-            d.unit = u;
-            d.s = s;
-            d.q_row = q_row;
-            d.L = L;
-            d.tok0 = (p0 + t * kTilePages) * kPage;
-            d.ntiles = ntiles;
-            d.flags = (t == 0 ? kFirst : 0) | (t == ntiles - 1 ? kLast : 0);
-            const int32_t* bt = a.block_table + static_cast<int64_t>(s) * a.max_pages;
-#pragma unroll
-            for (int j = 0; j < kTilePages; ++j) {
-              const int lp = p0 + t * kTilePages + j;
-              phys[j] = -1;
-              if (lp < p1) {
-                const int32_t pg = bt[lp];
-                if (pg >= 0 && pg < a.num_pages) {
-                  phys[j] = pg;
-                  d.flags |= 1 << (8 + j);
-                  bytes += T::kPageBytes;
-                } else {
-                  set_status(st, GW_DEV_PAGE_RANGE);
-                }
-              }
-            }
-          }
-          sm.ring[fill % kRing] = d;
-          mbar_arrive_expect_tx(&sm.full[b], bytes);
-          if (!end) {
-#pragma unroll
-            for (int j = 0; j < kTilePages; ++j)
-              if (phys[j] >= 0)
-                bulk_g2s(sm.tiles[b] + j * T::kPageBytes, a.pool + static_cast<int64_t>(phys[j]) * T::kPageBytes,
-                         T::kPageBytes, &sm.full[b], pol);
-          }
-          ++fill;
-        }
-        if (end) stop = true;
+        sm.ring[fill % kRing] = d;
+        mbar_arrive_expect_tx(&sm.full[b], __popc(mask) * T::kPageBytes);
       }
+      __syncwarp();
+      if (ok)
+        bulk_g2s(sm.tiles[b] + lane * T::kPageBytes, a.pool + static_cast<int64_t>(pg) * T::kPageBytes,
+                 T::kPageBytes, &sm.full[b], pol);
+      if (end) break;
+      if (++t == ntiles) {
+        t = 0;
+        u += gridDim.x;
+        end = u >= total_units;
+        if (!end) unit_info();
+      }
+      pg = end ? -1 : fetch_page(in_unit);
+      if (end) in_unit = false;
     }
   } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issue
+    // ----------------------------------------------------------- QK^T issue
     // The whole warp runs this loop with warp-uniform values; elect.sync
     // picks the issuing lane inside mma_bf16_warp / commit_warp.
     const uint32_t id_qk = tc::idesc_bf16(64, HQ, false, false);
-    const uint32_t id_pv = tc::idesc_bf16(128, NP, true, true);
-    const uint32_t q_addr = smem_u32(sm.q);
     // descriptor bases; the start-address field is addr >> 4 in the low bits,
     // so a byte offset o is added as o >> 4 (all addresses stay below 256 KiB)
     const uint64_t qk_a0 = tc::smem_desc(smem_u32(sm.tiles[0]), 128, T::kBlk * 128);
-    const uint64_t qk_b0 = tc::smem_desc(q_addr, 128, 64 * 128);
+    const uint64_t qk_b0 = tc::smem_desc(smem_u32(sm.q), 128, 64 * 128);
+    constexpr uint32_t kTileBytes = kTilePages * T::kPageBytes;
+    int uidx = -1;
+    for (uint32_t gi = 0;; ++gi) {
+      const int b = gi % NB;
+      if (!warp_wait(&sm.full[b], (gi / NB) & 1, st)) break;
+      const TileDesc d = sm.ring[gi % kRing];
+      if (d.flags & kEnd) break;
+      if (d.flags & kFirst) {
+        ++uidx;
+        if (!warp_wait(&sm.q_ready, uidx & 1, st)) break;
+      }
+      // S^T buffer gi & 1 is free once the softmax of tile gi - 2 has read it
+      if (gi >= 2 && !warp_wait(&sm.p_ready[gi & 1], ((gi >> 1) - 1) & 1, st)) break;
+      tc::fence_after();
+      const uint64_t a_tile = qk_a0 + ((b * kTileBytes) >> 4);
+      const uint32_t d_s = tmem + 32 * (gi & 1);
+#pragma unroll
+      for (int ks = 0; ks < 32; ++ks) {
+        const uint64_t ad = a_tile + ((T::k_cb(ks) * 128) >> 4);
+        const uint64_t bd = qk_b0 + ((2 * ks * 128) >> 4);
+        tc::mma_bf16_warp(d_s, ad, bd, id_qk, ks > 0);
+      }
+      tc::commit_warp(&sm.s_ready[gi & 1]);
+      if (d.flags & kLast) tc::commit_warp(&sm.q_free);  // Q may be replaced once this completes
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ P.V issue
+    const uint32_t id_pv = tc::idesc_bf16(128, NP, true, true);
     const uint64_t pv_a0 = tc::smem_desc(smem_u32(sm.tiles[0]), T::kBlk * 128, 128);
     const uint64_t pv_b0 = tc::smem_desc(smem_u32(sm.p[0]), (NP / 8) * 128, 128);
     constexpr uint32_t kTileBytes = kTilePages * T::kPageBytes;
-    uint32_t gi = 0;
-    int uidx = -1, prev_u = -1;
-    TileDesc prev{};
-    bool has_prev = false, ok = true;
-
-    auto pv = [&](const TileDesc& d, uint32_t i, int ui) -> bool {
-      if (!warp_wait(&sm.p_ready[i & 1], (i >> 1) & 1, st)) return false;
+    int ui = -1;
+    for (uint32_t i = 0;; ++i) {
+      if (!warp_wait(&sm.full[i % NB], (i / NB) & 1, st)) break;
+      const TileDesc d = sm.ring[i % kRing];
+      if (d.flags & kEnd) break;
+      if (d.flags & kFirst) ++ui;
+      if (!warp_wait(&sm.p_ready[i & 1], (i >> 1) & 1, st)) break;
       const int ob = ui & 1;
-      if ((d.flags & kFirst) && ui >= 2 && !warp_wait(&sm.o_free[ob], ((ui >> 1) - 1) & 1, st)) return false;
+      if ((d.flags & kFirst) && ui >= 2 && !warp_wait(&sm.o_free[ob], ((ui >> 1) - 1) & 1, st)) break;
       tc::fence_after();
       const uint64_t a_tile = pv_a0 + (((i % NB) * kTileBytes) >> 4);
       const uint64_t b_p = pv_b0 + (((i & 1) * sizeof(sm.p[0])) >> 4);
@@ -261,53 +286,16 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       tc::commit_warp(&sm.empty[i % NB]);
       tc::commit_warp(&sm.pfree[i & 1]);
       if (d.flags & kLast) tc::commit_warp(&sm.o_done[ob]);
-      return true;
-    };
-
-    // Order per tile: P.V of the previous tile first (it frees that tile's
-    // buffer for the producer as early as possible, so the HBM load of the
-    // tile after next overlaps this tile's QK^T and softmax), then QK^T.
-    while (true) {
-      if (has_prev && !pv(prev, gi - 1, prev_u)) { ok = false; break; }
-      has_prev = false;
-      const int b = gi % NB;
-      if (!warp_wait(&sm.full[b], (gi / NB) & 1, st)) { ok = false; break; }
-      const TileDesc d = sm.ring[gi % kRing];
-      if (d.flags & kEnd) break;
-      if (d.flags & kFirst) {
-        ++uidx;
-        if (!warp_wait(&sm.q_ready, uidx & 1, st)) { ok = false; break; }
-      }
-      tc::fence_after();
-      const uint64_t a_tile = qk_a0 + ((b * kTileBytes) >> 4);
-      const uint32_t d_s = tmem + 32 * (gi & 1);
-#pragma unroll
-      for (int ks = 0; ks < 32; ++ks) {
-        const uint64_t ad = a_tile + ((T::k_cb(ks) * 128) >> 4);
-        const uint64_t bd = qk_b0 + ((2 * ks * 128) >> 4);
-        tc::mma_bf16_warp(d_s, ad, bd, id_qk, ks > 0);
-      }
-      tc::commit_warp(&sm.s_ready[gi & 1]);
-      if (d.flags & kLast) tc::commit_warp(&sm.q_free);  // Q may be replaced once this completes
-      prev = d;
-      prev_u = uidx;
-      has_prev = true;
-      ++gi;
     }
-    (void)ok;
   } else if (warp == 6) {
     // -------------------------------------------------------------- q loader
-    // Ordering: wait until the last QK^T of the previous unit has completed
-    // (q_free), which also guarantees that every earlier tile has landed, so
-    // the `full` wait below is never more than one phase behind.
-    uint32_t first = 0;
-    int u = 0;
-    while (true) {
-      if (u > 0 && !mbar_wait(&sm.q_free, (u - 1) & 1, st)) break;
-      if (!mbar_wait(&sm.full[first % NB], (first / NB) & 1, st)) break;
-      const TileDesc d = sm.ring[first % kRing];
-      if (d.flags & kEnd) break;
-      const uint16_t* src = a.q + static_cast<int64_t>(d.q_row) * HQ * 512;
+    // Unit k's rows overwrite Q once the last QK^T of unit k - 1 has
+    // completed (q_free); by then they are usually in L2 already.
+    int k = 0;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++k) {
+      const int q_row = a.cu_q_rows[plan_seq(sm.ub, a.batch, u)];
+      if (k > 0 && !warp_wait(&sm.q_free, (k - 1) & 1, st)) break;
+      const uint16_t* src = a.q + static_cast<int64_t>(q_row) * HQ * 512;
       for (int c = lane; c < HQ * 64; c += 32) {
         const int h = c >> 6, cb = c & 63;
         cp_async16(sm.q + (((h >> 3) * 64 + cb) * 128 + (h & 7) * 16), src + h * 512 + cb * 8);
@@ -316,9 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       asm volatile("cp.async.wait_group 0;" ::: "memory");
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.q_ready);
-      first += d.ntiles;
-      ++u;
+      if (lane == 0) {
+        mbar_arrive(&sm.q_ready);
+        const int un = u + gridDim.x;
+        if (un < total_units)
+          prefetch_l2(a.q + static_cast<int64_t>(a.cu_q_rows[plan_seq(sm.ub, a.batch, un)]) * HQ * 512, HQ * 1024);
+      }
     }
   } else {
     // ------------------------------------------------- softmax + epilogue
@@ -481,11 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
 
 template <int LAYOUT, int HQ>
 cudaError_t launch_layout(const LocalArgs& a, cudaStream_t stream) {
-  cudaError_t e = launch_plan(a, kSplitGlobal, 0, stream);
-  if (e != cudaSuccess) return e;
   auto kern = global_decode_kernel<LAYOUT, HQ>;
   const size_t smem = sizeof(GSmem<LAYOUT, HQ>);
-  e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_sms()), dim3(kThreads), smem, stream, a);
   if (e != cudaSuccess) return e;

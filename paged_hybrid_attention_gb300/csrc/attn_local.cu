@@ -35,6 +35,7 @@
 // lane bits (one shuffle + add per value and level).  The conversions double
 // the instructions per byte, so the kernel is bound by issue latency and runs
 // more warps than the HBM stream alone would need.
+#include "plan.cuh"
 #include "tma.cuh"
 
 namespace gw {
@@ -73,11 +74,7 @@ struct Traits {
 
 template <class T>
 __device__ __forceinline__ Unit decode_unit(const LocalArgs& a, const int32_t* ub, int u) {
-  int lo = 0, hi = a.batch;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (ub[mid] <= u) lo = mid; else hi = mid - 1;
-  }
+  const int lo = plan_seq(ub, a.batch, u);
   Unit d;
   d.s = lo;
   const int L = a.seq_lens[lo];
@@ -153,58 +150,9 @@ __device__ __forceinline__ void xreduce(float* x) {
   }
 }
 
-// The split plan of the batch, computed by every CTA into its own shared
-// memory: ub[s] = units of the decode-row sequences before s (ub[batch] =
-// total).  CTA 0 also stores it to the workspace for the combine kernel.
 template <int kChunk>
-__device__ void plan_in_smem(const LocalArgs& a, int32_t* ub, int32_t* scratch) {
-  const int nt = blockDim.x, t = threadIdx.x;
-  const int per = (a.batch + nt - 1) / nt;
-  const int s0 = min(a.batch, t * per), s1 = min(a.batch, s0 + per);
-  int mine = 0;
-  for (int s = s0; s < s1; ++s) {
-    const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
-    const int L = a.seq_lens[s];
-    int units = 0;
-    if (n == 1) {
-      if (L >= 1 && static_cast<int64_t>(L) <= static_cast<int64_t>(a.max_pages) * kPage)
-        units = a.kv_heads * local_chunks(L, a.window, kChunk);
-      else if (blockIdx.x == 0)
-        set_status(a.status, GW_DEV_LEN_RANGE);
-    }
-    ub[s] = units;  // per-sequence count for now
-    mine += units;
-  }
-  // exclusive scan of the per-thread sums
-  const int lane = t & 31, w = t >> 5;
-  int x = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) scratch[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    int v = lane < (nt >> 5) ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += y;
-    }
-    if (lane < (nt >> 5)) scratch[lane] = v;
-  }
-  __syncthreads();
-  int run = (w > 0 ? scratch[w - 1] : 0) + x - mine;
-  for (int s = s0; s < s1; ++s) {
-    const int c = ub[s];
-    ub[s] = run;
-    run += c;
-  }
-  if (t == nt - 1) ub[a.batch] = run;
-  __syncthreads();
-  if (blockIdx.x == 0)
-    for (int s = t; s <= a.batch; s += nt) a.unit_base[s] = ub[s];
+__device__ __forceinline__ void local_plan(const LocalArgs& a, int32_t* ub) {
+  plan_in_smem(a, ub, ub + kMaxBatch + 1, [&](int L) { return a.kv_heads * local_chunks(L, a.window, kChunk); });
 }
 
 template <int DT, int G>
@@ -224,7 +172,7 @@ __global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kerne
   int32_t* ub = reinterpret_cast<int32_t*>(smem_raw + sizeof(typename T::Smem) * kWarps);
   pdl_wait();
   pdl_trigger();
-  plan_in_smem<T::kChunk>(a, ub, ub + kLocalMaxBatch + 1);
+  local_plan<T::kChunk>(a, ub);
   const int total_units = ub[a.batch];
   if (total_units > a.max_units) {
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.status, GW_DEV_WORKSPACE);
@@ -470,7 +418,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
   int32_t* ub = reinterpret_cast<int32_t*>(smem_raw + sizeof(TcWarpSmem) * kTcWarps);
   pdl_wait();
   pdl_trigger();
-  plan_in_smem<T::kChunk>(a, ub, ub + kLocalMaxBatch + 1);
+  local_plan<T::kChunk>(a, ub);
   const int total_units = ub[a.batch];
   if (total_units > a.max_units) {
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.status, GW_DEV_WORKSPACE);
@@ -672,7 +620,7 @@ cudaError_t launch_tc(const LocalArgs& a, cudaStream_t st) {
   CUtensorMap map;
   cudaError_t e = make_local_kv_map(a, &map);
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(TcWarpSmem) * kTcWarps + sizeof(int32_t) * (kLocalMaxBatch + 1 + 32);
+  const size_t smem = sizeof(TcWarpSmem) * kTcWarps + sizeof(int32_t) * (kMaxBatch + 1 + 32);
   auto kern = local_decode_tc_kernel<G>;
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
@@ -686,7 +634,7 @@ cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   using T = Traits<DT>;
   cudaError_t e;
   constexpr int kWarps = warps_for<DT, G>();
-  const size_t smem = sizeof(typename T::Smem) * kWarps + sizeof(int32_t) * (kLocalMaxBatch + 1 + 32);
+  const size_t smem = sizeof(typename T::Smem) * kWarps + sizeof(int32_t) * (kMaxBatch + 1 + 32);
   auto kern = local_decode_kernel<DT, G>;
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;

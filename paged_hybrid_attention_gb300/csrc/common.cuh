@@ -89,6 +89,12 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
+// Prefetch [src, src + bytes) into L2 (no completion tracking); 16-byte
+// aligned address, size a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // L2 policy for data read many times in a short span (prompt-row K/V tiles).
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;

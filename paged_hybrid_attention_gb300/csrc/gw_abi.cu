@@ -109,7 +109,7 @@ WsLayout ws_layout(int layout, int dtype, int kv_heads, int num_q_heads, int bat
   }
   const int D = layout == GW_LAYOUT_LOCAL ? 256 : 512;
   w.max_units = units;
-  w.counter = 0;
+  w.reserved = 0;
   w.unit_base = 256;
   w.ml = w.unit_base + round_up(static_cast<size_t>(batch + 1) * 4, 256);
   w.o = w.ml + round_up(static_cast<size_t>(units) * w.heads_per_unit * 8, 256);
@@ -196,8 +196,8 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
   if (!local && num_q_heads != 8 && num_q_heads != 16 && num_q_heads != 32)
     return fail(GW_ERR_UNSUPPORTED, fn, "num_q_heads must be 8, 16 or 32 (got %d)", num_q_heads);
   if (local && window < 1) return fail(GW_ERR_INVALID_ARG, fn, "window must be >= 1");
-  if (local && batch > kLocalMaxBatch)
-    return fail(GW_ERR_UNSUPPORTED, fn, "batch (%d) exceeds %d sequences per call", batch, kLocalMaxBatch);
+  if (batch > kMaxBatch)
+    return fail(GW_ERR_UNSUPPORTED, fn, "batch (%d) exceeds %d sequences per call", batch, kMaxBatch);
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(GW_ERR_INVALID_ARG, fn, "scale must be finite and > 0");
   if (max_pages_per_seq < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_pages_per_seq must be >= 1");
   if (max_q_rows < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_q_rows must be >= 1");
@@ -229,7 +229,6 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
   a.window = local ? window : 0x7fffffff;
   a.scale_log2 = scale * 1.4426950408889634f;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  a.counter = reinterpret_cast<int32_t*>(ws + w.counter);
   a.unit_base = reinterpret_cast<int32_t*>(ws + w.unit_base);
   a.part_ml = reinterpret_cast<float2*>(ws + w.ml);
   a.part_o = reinterpret_cast<float*>(ws + w.o);

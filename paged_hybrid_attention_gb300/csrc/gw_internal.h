@@ -23,8 +23,8 @@ constexpr int kLocalChunkPagesE4m3 = 8;
 constexpr int kGlobalChunkPagesMin = 16;
 constexpr int kGlobalMaxChunks = 128;
 
-// Local decode keeps the batch's split plan in shared memory.
-constexpr int kLocalMaxBatch = 4096;
+// The decode kernels keep the batch's split plan in shared memory.
+constexpr int kMaxBatch = 4096;
 
 constexpr int kSplitLocal = 0;
 constexpr int kSplitGlobal = 1;
@@ -48,13 +48,13 @@ __host__ __device__ __forceinline__ int global_chunks(int L) {
 }
 
 // Workspace layout (offsets from the 256-byte aligned workspace base):
-//   [0, 256)          int32 work counter (+ padding)
+//   [0, 256)          reserved
 //   [256, ub_end)     int32 unit_base[batch + 1], rounded up to 256 bytes
 //   [ub_end, ml_end)  float2 (m, l) per (unit, head of the unit)
 //   [ml_end, o_end)   float  o[unit][head of the unit][head_dim]
 //   [o_end, ...)      int32 prompt_base[batch + 1] (prompt-row tile offsets)
 struct WsLayout {
-  size_t counter, unit_base, ml, o, prompt_base, total;
+  size_t reserved, unit_base, ml, o, prompt_base, total;
   int64_t max_units;
   int heads_per_unit;
 };
@@ -76,7 +76,6 @@ struct LocalArgs {
   int32_t max_pages;
   int32_t window;  // local; ignored for global
   float scale_log2;  // softmax scale * log2(e)
-  int32_t* counter;
   int32_t* unit_base;
   float2* part_ml;
   float* part_o;
@@ -105,10 +104,6 @@ int num_sms();
 // prefixed by `fn`, and returns `code`.
 gw_status set_error(gw_status code, const char* fn, const char* fmt, ...);
 
-// Split-KV plan: unit_base[s] = units of the decode-row sequences before s;
-// zeroes the work counter.  mode: kSplitLocal (units = kv_heads * chunks of
-// `chunk` pages of the window) or kSplitGlobal (units = global_chunks(L)).
-cudaError_t launch_plan(const LocalArgs& a, int mode, int chunk, cudaStream_t st);
 // Log-sum-exp merge of each decode row's partials into bf16 `out`.
 cudaError_t launch_combine(const LocalArgs& a, int mode, int heads_per_unit, int head_dim, int chunk,
                            cudaStream_t st);

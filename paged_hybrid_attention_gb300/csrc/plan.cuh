@@ -1,0 +1,81 @@
+// The split-KV plan of a decode call, computed inside the decode kernels.
+//
+// Every CTA scans the batch's lengths into its own shared memory (a few
+// hundred nanoseconds for serving batches), so no plan kernel and no work
+// counter sit in front of the decode.  Units are dealt round-robin over the
+// CTAs (or warps), so the plan is all a CTA needs to find its own work.
+#pragma once
+
+#include "common.cuh"
+
+namespace gw {
+
+// ub[s] = units of the decode-row sequences before s (ub[batch] = total),
+// with units_of(L) the units of one decode row of length L.  Rows of invalid
+// length (L < 1 or beyond the block table) get no units and raise
+// GW_DEV_LEN_RANGE.  Must be called by every thread of the block; scratch
+// holds 32 ints.  CTA 0 also stores the plan to the workspace for the combine
+// kernel.
+template <class UnitsOf>
+__device__ void plan_in_smem(const LocalArgs& a, int32_t* ub, int32_t* scratch, UnitsOf units_of) {
+  const int nt = blockDim.x, t = threadIdx.x;
+  const int per = (a.batch + nt - 1) / nt;
+  const int s0 = min(a.batch, t * per), s1 = min(a.batch, s0 + per);
+  int mine = 0;
+  for (int s = s0; s < s1; ++s) {
+    const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
+    const int L = a.seq_lens[s];
+    int units = 0;
+    if (n == 1) {
+      if (L >= 1 && static_cast<int64_t>(L) <= static_cast<int64_t>(a.max_pages) * kPage)
+        units = units_of(L);
+      else if (blockIdx.x == 0)
+        set_status(a.status, GW_DEV_LEN_RANGE);
+    }
+    ub[s] = units;  // per-sequence count for now
+    mine += units;
+  }
+  // exclusive scan of the per-thread sums
+  const int lane = t & 31, w = t >> 5;
+  int x = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int v = lane < (nt >> 5) ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane < (nt >> 5)) scratch[lane] = v;
+  }
+  __syncthreads();
+  int run = (w > 0 ? scratch[w - 1] : 0) + x - mine;
+  for (int s = s0; s < s1; ++s) {
+    const int c = ub[s];
+    ub[s] = run;
+    run += c;
+  }
+  if (t == nt - 1) ub[a.batch] = run;
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int s = t; s <= a.batch; s += nt) a.unit_base[s] = ub[s];
+}
+
+// The sequence that owns unit u (0 <= u < ub[batch]): the largest s with
+// ub[s] <= u, which skips sequences without units.
+__device__ __forceinline__ int plan_seq(const int32_t* ub, int batch, int u) {
+  int lo = 0, hi = batch;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ub[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace gw

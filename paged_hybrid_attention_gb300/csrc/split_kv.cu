@@ -1,5 +1,5 @@
-// Split-KV bookkeeping shared by the local and global decode kernels: the
-// plan (unit offsets from sequence lengths) and the log-sum-exp combine.
+// The log-sum-exp combine of split-KV partials, shared by the local and
+// global decode kernels (their plans are computed in-kernel, plan.cuh).
 //
 // A sequence's partials are merged in chunk order, so its output depends only
 // on its own length and data ("Gemma 4" (pegainfer model page), "Reproducibility
@@ -11,63 +11,6 @@ namespace {
 
 __device__ __forceinline__ bool len_ok(const LocalArgs& a, int L, int n) {
   return L >= 1 && L >= n && static_cast<int64_t>(L) <= static_cast<int64_t>(a.max_pages) * kPage;
-}
-
-__device__ __forceinline__ int seq_units(const LocalArgs& a, int mode, int chunk, int L) {
-  return mode == kSplitLocal ? a.kv_heads * local_chunks(L, a.window, chunk) : global_chunks(L);
-}
-
-// One CTA: unit_base[s] = units of decode-row sequences before s; counter = 0.
-__global__ void plan_kernel(const LocalArgs a, int mode, int chunk) {
-  __shared__ int32_t warp_sums[32];
-  __shared__ int32_t carry;
-  pdl_wait();
-  pdl_trigger();
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  for (int base = 0; base < a.batch; base += blockDim.x) {
-    const int s = base + threadIdx.x;
-    int units = 0;
-    if (s < a.batch) {
-      const int n = a.cu_q_rows[s + 1] - a.cu_q_rows[s];
-      const int L = a.seq_lens[s];
-      if (n == 1) {
-        if (len_ok(a, L, n))
-          units = seq_units(a, mode, chunk, L);
-        else
-          set_status(a.status, GW_DEV_LEN_RANGE);
-      }
-    }
-    int x = units;  // inclusive warp scan
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sums[w] = x;
-    __syncthreads();
-    if (w == 0) {
-      int v = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
-      }
-      warp_sums[lane] = v;
-    }
-    __syncthreads();
-    const int excl = carry + (w > 0 ? warp_sums[w - 1] : 0) + x - units;
-    if (s < a.batch) a.unit_base[s] = excl;
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) carry = excl + units;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    a.unit_base[a.batch] = carry;
-    *a.counter = 0;
-    if (carry > a.max_units) set_status(a.status, GW_DEV_WORKSPACE);
-  }
 }
 
 // One warp per (sequence, q head, 128-dim slice); lane l owns 4 dims of the
@@ -143,10 +86,6 @@ __global__ void combine_kernel(const LocalArgs a, int mode, int G, int chunk) {
 }
 
 }  // namespace
-
-cudaError_t launch_plan(const LocalArgs& a, int mode, int chunk, cudaStream_t st) {
-  return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, a, mode, chunk);
-}
 
 cudaError_t launch_combine(const LocalArgs& a, int mode, int heads_per_unit, int head_dim, int chunk,
                            cudaStream_t st) {
