@@ -6,28 +6,34 @@
 // k_norm and RoPE on 128 of the 512 dims.  "Gewell - Gemma4 inference
 // engine", "the Why": so a token can be cached as V plus the rotated K slice
 // (0.625x of K+V) and K rebuilt for the math.  Here that rebuild costs
-// nothing: the folded page tile in shared memory holds V[0:512] and
-// k_rot[0:128] as 8x8 core matrices, and the QK^T contraction simply points
-// its K-dimension descriptors at k_rot for dims [0,128) and at V for dims
+// nothing: the folded pages in shared memory hold V[0:512] and k_rot[0:128]
+// as 8x8 core matrices, and the QK^T contraction simply points its
+// K-dimension descriptors at k_rot for dims [0,128) and at V for dims
 // [128,512) - the same V bytes then feed P.V.
 //
 // All q heads share one KV head, so per 64-token tile the work is two real
 // dense contractions (~51 flop per KV byte):
-//   S^T[64 tok x HQ] = K_tile[64 x 512] . Q^T        (UMMA M=64, N=HQ, K=512)
-//   O^T[512 x HQ]   += V_tile^T[512 x 64] . P^T      (UMMA M=128 x4, N=HQ, K=16 per page)
+//   S^T[64 tok x HQ] = K_tile[64 x 512] . Q^T     (UMMA M=64, N=HQ, K=512: 32 MMAs)
+//   O^T[512 x HQ]   += V_tile^T[512 x 64] . P^T   (UMMA M=128 x4 per page, K=16)
 // with fp32 accumulators in tensor memory.
+//
+// A tile's four pages sit in page slots that are released one by one: P.V
+// commits each page's MMAs to that slot's barrier and the producer refills
+// the slot at once.  The folded layout double-buffers its tiles, so one tile
+// streams in while the other is computed; the full K+V control layout, whose
+// pages are 1.6x larger, has room for one tile only.  (One 128-token tile of
+// eight slots halves the MMAs per byte but leaves nothing streaming during
+// QK^T and the softmax, and was slower.)
 //
 // Warp roles (256 threads, one persistent CTA per SM):
 //   warps 0-3  softmax + epilogue: warp w owns TMEM lanes [32w, 32w+32), i.e.
 //              tokens [16w, 16w+16) of the tile (the M=64 accumulator uses
 //              lanes 0-15 of each 32-lane quadrant) and dims of O^T.
 //   warp 4     producer: walks the CTA's split-KV units (sequence, chunk of
-//              pages; dealt round-robin from the in-kernel plan) and streams
-//              whole pages with cp.async.bulk into a double-buffered 4-page
-//              tile (single buffer for the full K+V control layout, whose
-//              pages are 1.6x larger).  Lanes 0-3 fetch the next tile's page
-//              numbers while the producer waits for a free buffer, and issue
-//              one page copy each.
+//              pages; dealt round-robin from the in-kernel plan).  Lane j owns
+//              page slot j of each buffer: it fetches its page number of the
+//              next tile early, waits for its slot and issues the page's bulk
+//              copy.
 //   warp 5     QK^T issue and TMEM owner.
 //   warp 6     loads each unit's q rows into the K-major Q operand as soon as
 //              the previous unit's last QK^T has completed, and prefetches
@@ -41,9 +47,9 @@
 namespace gw {
 namespace {
 
-constexpr int kTilePages = 4;  // 64 tokens = UMMA M for QK^T
-constexpr int kRing = 4;       // tile descriptors in flight
 constexpr int kThreads = 256;
+constexpr int kTilePages = 4;  // 64 tokens = UMMA M of QK^T
+constexpr int kRing = 4;       // tile descriptors in flight
 constexpr float kLazyThreshold = 8.f;
 
 template <int LAYOUT>
@@ -52,7 +58,7 @@ template <>
 struct GTraits<GW_LAYOUT_GLOBAL_FOLDED> {
   static constexpr int kPageBytes = 20480;
   static constexpr int kBlk = 80;   // 8-column blocks per 8-token block
-  static constexpr int kNumBuf = 2;
+  static constexpr int kNumBuf = 2;  // tile buffers
   static constexpr int kVcb = 0;    // column block of V dim 0
   // column block holding K dims [16 ks, 16 ks + 16)
   __device__ static int k_cb(int ks) { return ks < 8 ? 64 + 2 * ks : 2 * ks; }
@@ -68,10 +74,9 @@ struct GTraits<GW_LAYOUT_GLOBAL_FULL> {
 
 struct TileDesc {
   int32_t unit, s, q_row, L;
-  int32_t tok0;    // absolute position of the tile's first token
-  int32_t flags;   // bit0 first tile of unit, bit1 last tile, bit2 end; bits 8..11 page valid
-  int32_t ntiles;  // tiles of this unit
-  int32_t pad;
+  int32_t tok0;   // absolute position of the tile's first token
+  int32_t flags;  // bit0 first tile of unit, bit1 last tile, bit2 end; bits 8.. page valid
+  int32_t pad[2];
 };
 constexpr int kFirst = 1, kLast = 2, kEnd = 4;
 
@@ -79,16 +84,16 @@ template <int LAYOUT, int HQ>
 struct GSmem {
   using T = GTraits<LAYOUT>;
   static constexpr int kNP = HQ < 16 ? 16 : HQ;  // P.V N (M=128 needs N % 16 == 0)
-  uint8_t tiles[T::kNumBuf][kTilePages * T::kPageBytes];
+  uint8_t tiles[T::kNumBuf][kTilePages][T::kPageBytes];
   uint8_t q[HQ * 512 * 2];     // K-major Q: [hb][cb 64][8][8] bf16
   uint8_t p[2][64 * kNP * 2];  // MN-major P^T: [tb 8][hb][8 tokens][8 heads] bf16
-  float stage[64 * 33];        // [token][head] staging for max / l reductions
+  float red[4][32];            // per-warp head reductions
   float mvec[32];              // reference max per head (log2 units)
   TileDesc ring[kRing];
-  uint64_t full[T::kNumBuf], empty[T::kNumBuf];
+  uint64_t full[T::kNumBuf], slot_empty[T::kNumBuf][kTilePages];
   uint64_t s_ready[2], p_ready[2], pfree[2], o_done[2], o_free[2], q_ready, q_free;
   uint32_t tmem_base;
-  int32_t flag;
+  int32_t flag[2];  // per tile parity: index + 1 of the last tile that asked for a new max
   int32_t ub[kMaxBatch + 1 + 32];  // split plan (+ scan scratch)
 };
 static_assert(sizeof(GSmem<GW_LAYOUT_GLOBAL_FOLDED, 32>) <= 232448, "shared memory of one CTA");
@@ -106,12 +111,50 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
 }
 
+// Adds `bytes` to the transaction count the current phase of `bar` waits for
+// (no arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Per-head reduction over the 32 lanes of a warp by a transposing fold: at
+// each level a lane keeps half of its heads and merges the partner's copy of
+// them.  Returns head (lane & (HQ-1)) reduced over all lanes; x is consumed.
+template <int N, bool kMax>
+__device__ __forceinline__ void head_fold(float* x, int lane) {
+  if constexpr (N > 1) {
+    constexpr int H = N / 2;
+    const bool up = lane & H;
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+      const float send = up ? x[i] : x[i + H];
+      const float keep = up ? x[i + H] : x[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, H);
+      x[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+    head_fold<H, kMax>(x, lane);
+  }
+}
+template <int HQ, bool kMax>
+__device__ __forceinline__ float head_reduce(float (&x)[HQ], int lane) {
+  head_fold<HQ, kMax>(x, lane);
+  float v = x[0];
+#pragma unroll
+  for (int o = HQ; o < 32; o <<= 1) {
+    const float r = __shfl_xor_sync(0xffffffffu, v, o);
+    v = kMax ? fmaxf(v, r) : v + r;
+  }
+  return v;
+}
+
 template <int LAYOUT, int HQ>
 __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalArgs a) {
   using T = GTraits<LAYOUT>;
   using SM = GSmem<LAYOUT, HQ>;
   constexpr int NB = T::kNumBuf;
   constexpr int NP = SM::kNP;
+  constexpr uint32_t kTileBytes = kTilePages * T::kPageBytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -128,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
   if (tid == 0) {
     for (int b = 0; b < NB; ++b) {
       mbar_init(&sm.full[b], 1);
-      mbar_init(&sm.empty[b], 1);
+      for (int j = 0; j < kTilePages; ++j) mbar_init(&sm.slot_empty[b][j], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.s_ready[b], 1);
@@ -136,32 +179,29 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       mbar_init(&sm.pfree[b], 1);
       mbar_init(&sm.o_done[b], 1);
       mbar_init(&sm.o_free[b], 128);
+      sm.flag[b] = 0;
     }
     mbar_init(&sm.q_ready, 1);
     mbar_init(&sm.q_free, 1);
-    sm.flag = 0;
     fence_mbar_init();
-  }
-  pdl_wait();
-  pdl_trigger();
-  plan_in_smem(a, sm.ub, sm.ub + kMaxBatch + 1, [](int L) { return global_chunks(L); });
-  const int total_units = sm.ub[a.batch];
-  if (total_units > a.max_units) {  // uniform; nothing allocated yet
-    if (blockIdx.x == 0 && tid == 0) set_status(st, GW_DEV_WORKSPACE);
-    return;
   }
   if (warp == 5) {
     tc::alloc(&sm.tmem_base, 512);
     tc::relinquish();
   }
+  pdl_wait();
+  pdl_trigger();
+  plan_in_smem(a, sm.ub, sm.ub + kMaxBatch + 1, [](int L) { return global_chunks(L); });
+  const int total_units = sm.ub[a.batch];
   fence_proxy_async_smem();
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = sm.tmem_base;
   // TMEM columns: S^T buffers at 0 and 32; O^T buffers at 64 and 192 (4 blocks of 32).
-
-  if (warp == 4) {
+  if (total_units > a.max_units) {  // uniform
+    if (blockIdx.x == 0 && tid == 0) set_status(st, GW_DEV_WORKSPACE);
+  } else if (warp == 4) {
     // ------------------------------------------------------------- producer
     const uint64_t pol = policy_evict_first();
     int u = blockIdx.x;
@@ -175,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       p1 = min(p0 + cpg, (L + kPage - 1) / kPage);
       ntiles = (p1 - p0 + kTilePages - 1) / kTilePages;
     };
-    // lanes 0-3: physical page of page `lane` of tile t (raw; checked after
-    // the buffer wait so that the load's latency hides behind it)
+    // lane j < 4: physical page of page j of tile t (raw; checked after the
+    // slot wait so that the load's latency hides behind it)
     auto fetch_page = [&](bool& in_unit) -> int32_t {
       const int lp = p0 + t * kTilePages + lane;
       in_unit = lane < kTilePages && lp < p1;
@@ -186,12 +226,27 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     if (!end) unit_info();
     bool in_unit = false;
     int32_t pg = end ? -1 : fetch_page(in_unit);
-    for (uint32_t fill = 0;; ++fill) {
-      const int b = fill % NB;
-      if (fill >= NB && !warp_wait(&sm.empty[b], ((fill / NB) - 1) & 1, st)) break;
-      const bool ok = in_unit && pg >= 0 && pg < a.num_pages;
-      if (in_unit && !ok) set_status(st, GW_DEV_PAGE_RANGE);
+    for (uint32_t n = 0;; ++n) {
+      const int b = n % NB;
+      const uint32_t k = n / NB;  // use of buffer b
+      bool waited = true, ok = false;
+      if (lane < kTilePages) {
+        // This lane's slot is free once P.V of the buffer's previous tile has
+        // read it.  That P.V followed the softmax of that tile, so the
+        // previous phase of full[b] is complete before this tile adds to it
+        // (the end marker waits too, so its arrival never lands on an open
+        // phase).
+        if (k > 0) waited = mbar_wait(&sm.slot_empty[b][lane], (k - 1) & 1, st);
+        ok = !end && waited && in_unit && pg >= 0 && pg < a.num_pages;
+        if (!end && waited && in_unit && !ok) set_status(st, GW_DEV_PAGE_RANGE);
+        if (ok) {
+          mbar_expect_tx(&sm.full[b], T::kPageBytes);
+          bulk_g2s(sm.tiles[b][lane], a.pool + static_cast<int64_t>(pg) * T::kPageBytes, T::kPageBytes,
+                   &sm.full[b], pol);
+        }
+      }
       const uint32_t mask = __ballot_sync(0xffffffffu, ok);
+      if (__any_sync(0xffffffffu, !waited)) break;
       if (lane == 0) {
         TileDesc d{};
         if (end) {
@@ -202,16 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
           d.q_row = q_row;
           d.L = L;
           d.tok0 = (p0 + t * kTilePages) * kPage;
-          d.ntiles = ntiles;
           d.flags = (t == 0 ? kFirst : 0) | (t == ntiles - 1 ? kLast : 0) | static_cast<int>(mask << 8);
         }
-        sm.ring[fill % kRing] = d;
-        mbar_arrive_expect_tx(&sm.full[b], __popc(mask) * T::kPageBytes);
+        sm.ring[n % kRing] = d;
+        mbar_arrive(&sm.full[b]);  // after every expect_tx of this tile (ordered by the votes above)
       }
-      __syncwarp();
-      if (ok)
-        bulk_g2s(sm.tiles[b] + lane * T::kPageBytes, a.pool + static_cast<int64_t>(pg) * T::kPageBytes,
-                 T::kPageBytes, &sm.full[b], pol);
       if (end) break;
       if (++t == ntiles) {
         t = 0;
@@ -231,29 +281,28 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     // so a byte offset o is added as o >> 4 (all addresses stay below 256 KiB)
     const uint64_t qk_a0 = tc::smem_desc(smem_u32(sm.tiles[0]), 128, T::kBlk * 128);
     const uint64_t qk_b0 = tc::smem_desc(smem_u32(sm.q), 128, 64 * 128);
-    constexpr uint32_t kTileBytes = kTilePages * T::kPageBytes;
     int uidx = -1;
-    for (uint32_t gi = 0;; ++gi) {
-      const int b = gi % NB;
-      if (!warp_wait(&sm.full[b], (gi / NB) & 1, st)) break;
-      const TileDesc d = sm.ring[gi % kRing];
+    for (uint32_t n = 0;; ++n) {
+      const int b = n % NB;
+      if (!warp_wait(&sm.full[b], (n / NB) & 1, st)) break;
+      const TileDesc d = sm.ring[n % kRing];
       if (d.flags & kEnd) break;
       if (d.flags & kFirst) {
         ++uidx;
         if (!warp_wait(&sm.q_ready, uidx & 1, st)) break;
       }
-      // S^T buffer gi & 1 is free once the softmax of tile gi - 2 has read it
-      if (gi >= 2 && !warp_wait(&sm.p_ready[gi & 1], ((gi >> 1) - 1) & 1, st)) break;
+      // S^T buffer n & 1 is free once the softmax of tile n - 2 has read it
+      if (n >= 2 && !warp_wait(&sm.p_ready[n & 1], ((n >> 1) - 1) & 1, st)) break;
       tc::fence_after();
       const uint64_t a_tile = qk_a0 + ((b * kTileBytes) >> 4);
-      const uint32_t d_s = tmem + 32 * (gi & 1);
+      const uint32_t d_s = tmem + 32 * (n & 1);
 #pragma unroll
       for (int ks = 0; ks < 32; ++ks) {
         const uint64_t ad = a_tile + ((T::k_cb(ks) * 128) >> 4);
         const uint64_t bd = qk_b0 + ((2 * ks * 128) >> 4);
         tc::mma_bf16_warp(d_s, ad, bd, id_qk, ks > 0);
       }
-      tc::commit_warp(&sm.s_ready[gi & 1]);
+      tc::commit_warp(&sm.s_ready[n & 1]);
       if (d.flags & kLast) tc::commit_warp(&sm.q_free);  // Q may be replaced once this completes
     }
   } else if (warp == 7) {
@@ -261,19 +310,19 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     const uint32_t id_pv = tc::idesc_bf16(128, NP, true, true);
     const uint64_t pv_a0 = tc::smem_desc(smem_u32(sm.tiles[0]), T::kBlk * 128, 128);
     const uint64_t pv_b0 = tc::smem_desc(smem_u32(sm.p[0]), (NP / 8) * 128, 128);
-    constexpr uint32_t kTileBytes = kTilePages * T::kPageBytes;
     int ui = -1;
-    for (uint32_t i = 0;; ++i) {
-      if (!warp_wait(&sm.full[i % NB], (i / NB) & 1, st)) break;
-      const TileDesc d = sm.ring[i % kRing];
+    for (uint32_t n = 0;; ++n) {
+      const int b = n % NB;
+      if (!warp_wait(&sm.full[b], (n / NB) & 1, st)) break;
+      const TileDesc d = sm.ring[n % kRing];
       if (d.flags & kEnd) break;
       if (d.flags & kFirst) ++ui;
-      if (!warp_wait(&sm.p_ready[i & 1], (i >> 1) & 1, st)) break;
+      if (!warp_wait(&sm.p_ready[n & 1], (n >> 1) & 1, st)) break;
       const int ob = ui & 1;
       if ((d.flags & kFirst) && ui >= 2 && !warp_wait(&sm.o_free[ob], ((ui >> 1) - 1) & 1, st)) break;
       tc::fence_after();
-      const uint64_t a_tile = pv_a0 + (((i % NB) * kTileBytes) >> 4);
-      const uint64_t b_p = pv_b0 + (((i & 1) * sizeof(sm.p[0])) >> 4);
+      const uint64_t a_tile = pv_a0 + ((b * kTileBytes) >> 4);
+      const uint64_t b_p = pv_b0 + (((n & 1) * sizeof(sm.p[0])) >> 4);
 #pragma unroll
       for (int j = 0; j < kTilePages; ++j) {
         const uint64_t bd = b_p + ((2 * j * (NP / 8) * 128) >> 4);
@@ -282,9 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
           const uint64_t ad = a_tile + ((j * T::kPageBytes + (T::kVcb + 16 * blk) * 128) >> 4);
           tc::mma_bf16_warp(tmem + 64 + 128 * ob + 32 * blk, ad, bd, id_pv, !((d.flags & kFirst) && j == 0));
         }
+        tc::commit_warp(&sm.slot_empty[b][j]);  // the producer may refill this page slot
       }
-      tc::commit_warp(&sm.empty[i % NB]);
-      tc::commit_warp(&sm.pfree[i & 1]);
+      tc::commit_warp(&sm.pfree[n & 1]);
       if (d.flags & kLast) tc::commit_warp(&sm.o_done[ob]);
     }
   } else if (warp == 6) {
@@ -311,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
           prefetch_l2(a.q + static_cast<int64_t>(a.cu_q_rows[plan_seq(sm.ub, a.batch, un)]) * HQ * 512, HQ * 1024);
       }
     }
-  } else {
+  } else if (warp < 4) {
     // ------------------------------------------------- softmax + epilogue
     const bool active = lane < 16;
     const int t = 16 * warp + lane;  // token of the tile (active lanes)
@@ -322,19 +371,18 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       m_run[h] = -INFINITY;
       l_acc[h] = 0.f;
     }
-    uint32_t gi = 0;
     int uidx = -1;
-    while (true) {
-      const int b = gi % NB;
-      if (!mbar_wait(&sm.full[b], (gi / NB) & 1, st)) break;
-      const TileDesc d = sm.ring[gi % kRing];
+    for (uint32_t n = 0;; ++n) {
+      const int b = n % NB;
+      if (!mbar_wait(&sm.full[b], (n / NB) & 1, st)) break;
+      const TileDesc d = sm.ring[n % kRing];
       if (d.flags & kEnd) break;
       const bool first = d.flags & kFirst;
       if (first) ++uidx;
-      if (!mbar_wait(&sm.s_ready[gi & 1], (gi >> 1) & 1, st)) break;
+      if (!mbar_wait(&sm.s_ready[n & 1], (n >> 1) & 1, st)) break;
       tc::fence_after();
       uint32_t r[32];
-      tc::ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * (gi & 1), r);
+      tc::ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * (n & 1), r);
       tc::wait_ld();
       const int tabs = d.tok0 + t;
       const bool pvalid = (d.flags >> (8 + j)) & 1;
@@ -346,31 +394,27 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
         s[h] = valid ? __uint_as_float(r[h]) * a.scale_log2 : -INFINITY;
         need |= s[h] > m_run[h] + kLazyThreshold;
       }
-      if (need) sm.flag = 1;
+      // A thread asking for a new max tags the flag of this tile's parity
+      // with the tile; the other parity's flag may meanwhile be written for
+      // the next tile (whose QK^T can complete before this softmax ends), and
+      // this parity is not written again before every thread has passed the
+      // barrier below on the next tile.
+      if (need) sm.flag[n & 1] = static_cast<int32_t>(n + 1);
       softmax_bar();
-      if (first || sm.flag) {
+      if (first || sm.flag[n & 1] == static_cast<int32_t>(n + 1)) {
         // ---- slow path: tile max per head, maybe rescale
-        if (active) {
+        float x[HQ];
 #pragma unroll
-          for (int h = 0; h < HQ; ++h) sm.stage[t * 33 + h] = s[h];
+        for (int h = 0; h < HQ; ++h) x[h] = s[h];
+        const float wmax = head_reduce<HQ, true>(x, lane);
+        if (lane < HQ) sm.red[warp][lane] = wmax;
+        softmax_bar();
+        if (tid < HQ) {
+          const float mx = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
+          const float mo = first ? -INFINITY : sm.mvec[tid];
+          sm.mvec[tid] = (first || mx > mo + kLazyThreshold) ? fmaxf(mo, mx) : mo;
         }
         softmax_bar();
-        {
-          const int hh = tid >> 2, qq = tid & 3;
-          float mx = -INFINITY;
-          if (hh < HQ) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) mx = fmaxf(mx, sm.stage[(16 * qq + i) * 33 + hh]);
-          }
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          if (hh < HQ && qq == 0) {
-            const float mo = first ? -INFINITY : sm.mvec[hh];
-            sm.mvec[hh] = (first || mx > mo + kLazyThreshold) ? fmaxf(mo, mx) : mo;
-          }
-        }
-        softmax_bar();
-        if (tid == 0) sm.flag = 0;
         float alpha[HQ];
         bool rescale = false;
 #pragma unroll
@@ -383,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
         }
         if (rescale) {
           // O^T *= alpha per head column, once P.V of the previous tile is done
-          if (!mbar_wait(&sm.pfree[(gi - 1) & 1], ((gi - 1) >> 1) & 1, st)) break;
+          if (!mbar_wait(&sm.pfree[(n - 1) & 1], ((n - 1) >> 1) & 1, st)) break;
           tc::fence_after();
           const uint32_t ob = uidx & 1;
 #pragma unroll 1
@@ -400,9 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
         }
       }
       // ---- P^T (bf16) for this tile; wait until P.V two tiles back released the buffer
-      if (gi >= 2 && !mbar_wait(&sm.pfree[gi & 1], ((gi >> 1) - 1) & 1, st)) break;
+      if (n >= 2 && !mbar_wait(&sm.pfree[n & 1], ((n >> 1) - 1) & 1, st)) break;
       if (active) {
-        uint8_t* pdst = sm.p[gi & 1] + ((t >> 3) * (NP / 8)) * 128 + (t & 7) * 16;
+        uint8_t* pdst = sm.p[n & 1] + ((t >> 3) * (NP / 8)) * 128 + (t & 7) * 16;
 #pragma unroll
         for (int hb = 0; hb < HQ / 8; ++hb) {
           uint32_t w[4];
@@ -421,13 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
         if (pvalid && tabs >= d.L) {
           // token past the end of the sequence in a valid page: clear its row
           // so whatever the pool holds there cannot reach P.V
-          uint8_t* row = sm.tiles[b] + j * T::kPageBytes + (lane >> 3) * T::kBlk * 128 + (lane & 7) * 16;
+          uint8_t* row = sm.tiles[b][j] + (lane >> 3) * T::kBlk * 128 + (lane & 7) * 16;
           for (int cb = 0; cb < T::kBlk; ++cb) *reinterpret_cast<uint4*>(row + cb * 128) = make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();
       tc::fence_before();
-      mbar_arrive(&sm.p_ready[gi & 1]);
+      mbar_arrive(&sm.p_ready[n & 1]);
 
       if (d.flags & kLast) {
         // ---- epilogue: unnormalised partial (m, l, o) of this unit
@@ -444,21 +488,20 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
 #pragma unroll
           for (int h = 0; h < HQ; ++h) po[h * 512 + dim] = __uint_as_float(o[h]);
         }
-        if (active) {
+        float x[HQ];
 #pragma unroll
-          for (int h = 0; h < HQ; ++h) sm.stage[t * 33 + h] = l_acc[h];
-        }
+        for (int h = 0; h < HQ; ++h) x[h] = l_acc[h];
+        const float wl = head_reduce<HQ, false>(x, lane);
+        if (lane < HQ) sm.red[warp][lane] = wl;
         softmax_bar();
         if (tid < HQ) {
-          float l = 0.f;
-          for (int k = 0; k < 64; ++k) l += sm.stage[k * 33 + tid];
+          const float l = ((sm.red[0][tid] + sm.red[1][tid]) + sm.red[2][tid]) + sm.red[3][tid];
           a.part_ml[static_cast<int64_t>(d.unit) * HQ + tid] = make_float2(sm.mvec[tid], l);
         }
         softmax_bar();
         tc::fence_before();
         mbar_arrive(&sm.o_free[ob]);
       }
-      ++gi;
     }
   }
 

@@ -81,12 +81,16 @@ def test_global_long_context_sampled(key):
 
 
 def test_folded_equals_full_bitwise():
+    """Compressed-K attention equals attention over the materialised full K
+    (tied K/V): both layouts agree with the oracle, and with each other bit
+    for bit."""
     lens = [5, 77, 1000, 2049]
     outs = []
     for layout in ["folded", "full"]:
         fam = synth.Family("global", "bf16", layout, 1, 512, 128, 1e6, 0)
         layer = synth.Layer(synth.custom("ff", 99, 32, lens, [1] * 4, {"global": fam}), "global")
-        out, _, _ = _run(layer, [])
+        out, ref_pool, _ = _run(layer)
+        _compare(layer, out, ref_pool, range(layer.B))
         outs.append(out)
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
 
