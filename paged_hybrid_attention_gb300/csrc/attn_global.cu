@@ -521,7 +521,7 @@ cudaError_t launch_layout(const LocalArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_sms()), dim3(kThreads), smem, stream, a);
   if (e != cudaSuccess) return e;
-  return launch_combine(a, kSplitGlobal, HQ, 512, 0, stream);
+  return launch_combine(a, HQ, 512, stream);
 }
 
 template <int LAYOUT>

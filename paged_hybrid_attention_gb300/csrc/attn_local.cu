@@ -626,7 +626,7 @@ cudaError_t launch_tc(const LocalArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_sms()), dim3(kTcWarps * 32), smem, st, a, map);
   if (e != cudaSuccess) return e;
-  return launch_combine(a, kSplitLocal, G, 256, TcTraits::kChunk, st);
+  return launch_combine(a, G, 256, st);
 }
 
 template <int DT, int G>
@@ -640,7 +640,7 @@ cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_sms()), dim3(kWarps * 32), smem, st, a);
   if (e != cudaSuccess) return e;
-  return launch_combine(a, kSplitLocal, G, 256, T::kChunk, st);
+  return launch_combine(a, G, 256, st);
 }
 
 template <int DT>

@@ -17,17 +17,15 @@ namespace gw {
 // length, so a row's arithmetic never depends on the rest of the batch.
 constexpr int kLocalChunkPagesBf16 = 8;
 constexpr int kLocalChunkPagesE4m3 = 8;
-// Global chunks start at 16 pages and double until a sequence has at most
+// Global chunks start at 32 pages and double until a sequence has at most
 // kGlobalMaxChunks of them (long contexts get long chunks, so the partials
 // stay a small fraction of the KV bytes).
-constexpr int kGlobalChunkPagesMin = 16;
+constexpr int kGlobalChunkPagesMin = 32;
 constexpr int kGlobalMaxChunks = 128;
 
 // The decode kernels keep the batch's split plan in shared memory.
 constexpr int kMaxBatch = 4096;
 
-constexpr int kSplitLocal = 0;
-constexpr int kSplitGlobal = 1;
 
 __host__ __device__ __forceinline__ int local_chunks(int L, int window, int chunk) {
   const int first = L > window ? L - window : 0;
@@ -104,9 +102,9 @@ int num_sms();
 // prefixed by `fn`, and returns `code`.
 gw_status set_error(gw_status code, const char* fn, const char* fmt, ...);
 
-// Log-sum-exp merge of each decode row's partials into bf16 `out`.
-cudaError_t launch_combine(const LocalArgs& a, int mode, int heads_per_unit, int head_dim, int chunk,
-                           cudaStream_t st);
+// Log-sum-exp merge of each decode row's partials into bf16 `out`; units of
+// heads_per_unit q heads, planned as in a.unit_base.
+cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim, cudaStream_t st);
 
 cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_bw_probe(const void* buf, int64_t chunks, int32_t* status, cudaStream_t st);
