@@ -150,6 +150,28 @@ __device__ __forceinline__ void xreduce(float* x) {
   }
 }
 
+// Warps per CTA that take units.  Units are dealt in rounds of warps x CTAs
+// and are nearly all the same size, so a call lasts as long as the warps
+// that get the most rounds; a partial last round leaves the others idle.  Of
+// wmax, wmax - 1 and wmax - 2 warps, take the one that wastes least of the
+// final round, counting each warp given up as 3% of streaming capacity.
+// Which warp runs a unit never changes its arithmetic.
+__device__ __forceinline__ int active_warps(int units, int wmax) {
+  int best = wmax;
+  float best_score = -1.f;
+  for (int w = wmax; w >= wmax - 2 && w >= 1; --w) {
+    const int slots = w * static_cast<int>(gridDim.x);
+    const int rounds = (units + slots - 1) / slots;
+    const float eff = rounds > 0 ? static_cast<float>(units) / static_cast<float>(rounds * slots) : 1.f;
+    const float score = eff * (1.f - 0.03f * static_cast<float>(wmax - w));
+    if (score > best_score) {
+      best_score = score;
+      best = w;
+    }
+  }
+  return best;
+}
+
 template <int kChunk>
 __device__ __forceinline__ void local_plan(const LocalArgs& a, int32_t* ub) {
   plan_in_smem(a, ub, ub + kMaxBatch + 1, [&](int L) { return a.kv_heads * local_chunks(L, a.window, kChunk); });
@@ -178,10 +200,12 @@ __global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kerne
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.status, GW_DEV_WORKSPACE);
     return;
   }
-  const uint64_t pol = policy_evict_first();
   // units are dealt round-robin over the warps, SM-minor, so every SM gets
   // an equal share of each round
-  const int n_warps = gridDim.x * kWarps;
+  const int n_active = active_warps(total_units, kWarps);
+  if (warp >= n_active) return;
+  const uint64_t pol = policy_evict_first();
+  const int n_warps = gridDim.x * n_active;
   int next_u = warp * gridDim.x + blockIdx.x;
   const int64_t head_bytes = 2LL * kPage * 256 * T::kEs;  // K + V of one KV head in one page
   const int perm = (lane >> (5 - T::kLevels)) & (kTok - 1);
@@ -424,21 +448,28 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.status, GW_DEV_WORKSPACE);
     return;
   }
+  const int n_active = active_warps(total_units, kTcWarps);
+  if (warp >= n_active) return;
   const uint64_t pol = policy_evict_first();
-  const int n_warps = gridDim.x * kTcWarps;
+  const int n_warps = gridDim.x * n_active;
   int next_u = warp * gridDim.x + blockIdx.x;
   constexpr int kRing = kTcStages + 2;
 
   int f_slot = 0, f_i = 0;
-  bool f_done = false;
+  bool f_done = false, have_next = false;
   uint32_t issued = 0, consumed = 0;
+  // Lane i holds the physical page of page i of the unit being issued (cur)
+  // and of the unit after it (nxt).  A unit's page numbers are loaded when
+  // the unit before it starts issuing, so no stage issue waits for a load.
+  int32_t pg_cur = -1, pg_nxt = -1;
 
-  auto grab = [&](int slot) -> bool {
+  auto grab = [&](int slot, int32_t& pg) -> bool {
     const int u = next_u;
     next_u += n_warps;
     if (u >= total_units) return false;
     const Unit d = decode_unit<T>(a, ub, u);
     if (lane == 0) sm.ring[slot] = d;
+    pg = lane < d.n ? a.block_table[static_cast<int64_t>(d.s) * a.max_pages + d.hp_lo + lane] : -1;
     __syncwarp();
     return true;
   };
@@ -446,10 +477,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
   auto issue = [&]() {
     const Unit d = sm.ring[f_slot];
     const int st = issued % kTcStages;
-    const int lp = d.hp_lo + f_i;  // one page per stage
-    int32_t phys = 0;
-    if (lane == 0) phys = a.block_table[static_cast<int64_t>(d.s) * a.max_pages + lp];
-    phys = __shfl_sync(0xffffffffu, phys, 0);
+    const int32_t phys = __shfl_sync(0xffffffffu, pg_cur, f_i);  // one page per stage
     if (phys < 0 || phys >= a.num_pages) {
       if (lane == 0) {
         sm.valid[st] = 0;
@@ -473,11 +501,16 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     if (++f_i == d.n) {
       f_i = 0;
       f_slot = (f_slot + 1) % kRing;
-      f_done = !grab(f_slot);
+      f_done = !have_next;
+      if (have_next) {
+        pg_cur = pg_nxt;
+        have_next = grab((f_slot + 1) % kRing, pg_nxt);
+      }
     }
   };
 
-  f_done = !grab(0);
+  f_done = !grab(0, pg_cur);
+  if (!f_done) have_next = grab(1, pg_nxt);
   while (!f_done && issued - consumed < kTcStages) issue();
 
   const int hq = lane >> 2;        // S row (q head of the group) this lane holds
