@@ -52,8 +52,7 @@ UNIT = "GB/s"
 # was captured from; reported as null once the source no longer matches.
 # workload: (bytes, source file under csrc/, sha256)
 NCU_TRAFFIC = {
-    "serving": (276518656, "attn_local.cu", "82c5752574d5b32d5d0c95830508037f3c14ebf9196eba63554f5dd163371e35"),
-    "fp8_local": (552995840, "attn_local.cu", "82c5752574d5b32d5d0c95830508037f3c14ebf9196eba63554f5dd163371e35"),
+    "serving": (276047104, "attn_local.cu", "a4498056895369e6e8b1f0399c60c2c3b8510f2da62af401b0c2b24ba79a51a2"),
 }
 
 
