@@ -212,15 +212,21 @@ __global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kerne
   const bool canon = (lane & ((1 << (5 - T::kLevels)) - 1)) == 0;
 
   int f_slot = 0, f_i = 0;
-  bool f_done = false;
+  bool f_done = false, have_next = false;
   uint32_t issued = 0, consumed = 0;
+  // Lane i holds the physical page of page i of the unit being issued (cur)
+  // and of the unit after it (nxt), loaded when the unit before starts
+  // issuing, so no stage issue waits for a block-table load.
+  int32_t pg_cur = -1, pg_nxt = -1;
 
-  auto grab = [&](int slot) -> bool {
+  auto grab = [&](int slot, int32_t& pg) -> bool {
     const int u = next_u;
     next_u += n_warps;
     if (u >= total_units) return false;
     const Unit d = decode_unit<T>(a, ub, u);
     if (lane == 0) sm.ring[slot] = d;
+    const int lp0 = d.hp_lo / T::kSpp, np = (d.hp_lo + d.n - 1) / T::kSpp + 1 - lp0;
+    pg = lane < np ? a.block_table[static_cast<int64_t>(d.s) * a.max_pages + lp0 + lane] : -1;
     __syncwarp();
     return true;
   };
@@ -230,8 +236,8 @@ __global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kerne
     const int st = issued % kStages;
     const int hp = d.hp_lo + f_i;
     const int lp = hp / T::kSpp, half = hp % T::kSpp;
+    const int32_t phys = __shfl_sync(0xffffffffu, pg_cur, lp - d.hp_lo / T::kSpp);
     if (lane == 0) {
-      const int32_t phys = a.block_table[static_cast<int64_t>(d.s) * a.max_pages + lp];
       if (phys < 0 || phys >= a.num_pages) {
         sm.valid[st] = 0;
         set_status(a.status, GW_DEV_PAGE_RANGE);
@@ -249,11 +255,16 @@ __global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kerne
     if (++f_i == d.n) {
       f_i = 0;
       f_slot = (f_slot + 1) % kRing;
-      f_done = !grab(f_slot);
+      f_done = !have_next;
+      if (have_next) {
+        pg_cur = pg_nxt;
+        have_next = grab((f_slot + 1) % kRing, pg_nxt);
+      }
     }
   };
 
-  f_done = !grab(0);
+  f_done = !grab(0, pg_cur);
+  if (!f_done) have_next = grab(1, pg_nxt);
   while (!f_done && issued - consumed < kStages) issue();
 
   using X = Mix<DT>;
