@@ -377,16 +377,19 @@ def main():
     if args.impl == "reference":
         if int(os.environ.get("RANK", "0")) != 0:
             return
-        ref_steps = []
+        ref_steps, ref_secs = [], []
         desc = ""
         for _ in range(args.warmup + args.steps):
             gbs, desc, secs = oracle_sample(args.workload, budget_s=max(1.0, 60.0 / max(1, args.steps + args.warmup)))
             ref_steps.append(gbs)
+            ref_secs.append(secs)
         val = statistics.median(ref_steps[args.warmup:]) if args.steps else ref_steps[-1]
+        ms = 1000.0 * (statistics.median(ref_secs[args.warmup:]) if args.steps else ref_secs[-1])
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": args.workload, "l2": "n/a (CPU)"},
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload, "l2": "n/a (CPU)",
+                           "step": "one bounded sample of the workload (see cpu_baseline.sample)"},
                 "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
                 "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
