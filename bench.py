@@ -63,7 +63,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="serving",
-                    help="serving (default), fp8_local, long_global, long_global_full, mixed, chunked, stack48")
+                    help="serving (default), fp8_local, long_global, long_global_full, mixed, chunked, stack48, "
+                         "prefill_lane (the serving step beside an SM-capped prefill lane)")
+    ap.add_argument("--lane-share", type=float, default=0.35,
+                    help="prefill_lane: share of the SMs given to the prefill lane")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch every step eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu", action="store_true")
@@ -84,7 +87,7 @@ def peaks():
 
 def workload_layers(name, rank):
     """[(Layer, family key)] of one step; each layer has its own page tables."""
-    base = {"long_global_full": "long_global"}.get(name, name)
+    base = {"long_global_full": "long_global", "prefill_lane": "serving"}.get(name, name)
     sp = synth.spec(base)
     if rank:
         sp = synth.custom(sp.name, sp.seed + 7919 * rank, sp.num_q_heads, sp.lens, sp.n_rows, sp.families,
@@ -397,6 +400,167 @@ class Ranks:
             torch.distributed.destroy_process_group()
 
 
+def prefill_lane_main(args, peak, peak_kind):
+    """NEXT-4: the serving decode step with an async prefill lane beside it.
+
+    The decode lane replays the serving step (5 local + 1 global layers, one
+    decode row per sequence) on one stream; the prefill lane replays the
+    appends and prompt rows of 4 new 2048-token prompts on the same six
+    layer shapes on a second stream, its attention kernels capped at a share
+    of the SMs (gw_set_max_ctas: these kernels run one CTA per SM, so a CTA
+    cap is an SM cap) and the decode lane's at the rest.  Reported: the
+    decode step alone, beside the capped lane and beside the uncapped lane,
+    and the prefill step alone and in each lane.  `value` is the decode KV
+    GB/s beside the capped lane."""
+    ranks = Ranks("nccl")
+    world, rank = ranks.world, ranks.rank
+    dev = torch.device("cuda", ranks.local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    ranks.device = dev
+    from paged_hybrid_attention_gb300 import gw
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    share = args.lane_share
+    cap_pre = max(1, int(round(share * sms)))
+    cap_dec = max(1, sms - cap_pre)
+    sp_d, layers_d = workload_layers("serving", rank)
+    sp_p, layers_p = workload_layers("prefill", rank)
+    gen = torch.Generator(device=dev).manual_seed(sp_d.seed + 17 * rank)
+    dec = [GpuLayer(l, gw, gen, dev) for l in layers_d]
+    pre = [GpuLayer(l, gw, gen, dev) for l in layers_p]
+    torch.cuda.synchronize()
+    dec_bytes = sum(g.kv_bytes for g in dec)
+    pre_flops = sum(g.prompt_flops for g in pre)
+
+    def capture(gls, cap, early=True):
+        gw.set_max_ctas(cap)
+        gw.set_early_launch(early)
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                for _ in range(2):
+                    for g in gls:
+                        g.run(gw, side)
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                for g in gls:
+                    g.run(gw, torch.cuda.current_stream())
+        finally:
+            gw.set_max_ctas(0)
+            gw.set_early_launch(True)
+        return gr
+
+    # the capped prefill lane launches each kernel only once its predecessor
+    # has finished: early (programmatic) launches would park its CTAs on the
+    # decode lane's SMs while they wait out a prompt kernel
+    g_dec, g_pre = capture(dec, 0), capture(pre, 0)
+    g_dec_c, g_pre_c = capture(dec, cap_dec), capture(pre, cap_pre, early=False)
+    g_pre_ce = capture(pre, cap_pre)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(gr, st, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st):
+            e0.record(st)
+            for _ in range(n):
+                gr.replay()
+            e1.record(st)
+        return e0, e1
+
+    for gr in (g_dec, g_pre, g_dec_c, g_pre_c, g_pre_ce):
+        for _ in range(max(3, args.warmup)):
+            gr.replay()
+    torch.cuda.synchronize()
+    ranks.barrier()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    K = max(3, args.steps)
+    a0, a1 = timed(g_dec, sa, K)
+    torch.cuda.synchronize()
+    dec_alone = a0.elapsed_time(a1) / K
+    a0, a1 = timed(g_dec_c, sa, K)
+    torch.cuda.synchronize()
+    dec_capped_alone = a0.elapsed_time(a1) / K
+    KP = max(2, min(K, 20))
+    b0, b1 = timed(g_pre, sb, KP)
+    torch.cuda.synchronize()
+    pre_alone = b0.elapsed_time(b1) / KP
+    b0, b1 = timed(g_pre_c, sb, 2)
+    torch.cuda.synchronize()
+    pre_capped_alone = b0.elapsed_time(b1) / 2
+
+    def lanes(gd, gp):
+        # the prefill lane runs M steps; the decode lane runs N steps inside
+        # them, an event after each (the worst step is the longest gap
+        # between two tokens of a decode stream)
+        M = 3
+        N = max(3, int(0.5 * M * pre_alone * (sms / cap_pre) / dec_alone))
+        p0, p1 = timed(gp, sb, M)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(N + 1)]
+        with torch.cuda.stream(sa):
+            evs[0].record(sa)
+            for i in range(N):
+                gd.replay()
+                evs[i + 1].record(sa)
+        torch.cuda.synchronize()
+        steps = [evs[i].elapsed_time(evs[i + 1]) for i in range(N)]
+        worst = {"ms": max(steps), "step": int(np.argmax(steps)), "median_ms": statistics.median(steps)}
+        return evs[0].elapsed_time(evs[N]) / N, worst, p0.elapsed_time(p1) / M, N, M
+
+    dec_cap, dec_cap_worst, pre_cap, n_cap, m_cap = lanes(g_dec_c, g_pre_c)
+    dec_cape, dec_cape_worst, pre_cape, _, _ = lanes(g_dec_c, g_pre_ce)
+    dec_unc, dec_unc_worst, pre_unc, n_unc, m_unc = lanes(g_dec, g_pre)
+    clk = clocks.stop()
+    ranks.barrier()
+    dec_cap_max = ranks.max(dec_cap)
+    status = int(sum(int(g.status.item()) for g in dec + pre))
+    if rank != 0:
+        ranks.close()
+        return
+    gbs = lambda ms: dec_bytes / (ms * 1e-3) / 1e9
+    value = ranks.throughput(dec_bytes, dec_cap)
+    lane = {
+        "sms": sms, "prefill_ctas": cap_pre, "decode_ctas": cap_dec, "share": share,
+        "decode_step_alone_ms": dec_alone, "decode_gbs_alone": gbs(dec_alone),
+        "decode_step_capped_alone_ms": dec_capped_alone, "prefill_step_capped_alone_ms": pre_capped_alone,
+        "decode_step_capped_lane_ms": dec_cap, "decode_steps_capped_lane": dec_cap_worst,
+        "decode_steps_uncapped_lane": dec_unc_worst,
+        "capped_lane_with_early_launch": {"decode_step_ms": dec_cape, "decode_steps": dec_cape_worst,
+                                          "prefill_step_ms": pre_cape}, "decode_gbs_capped_lane": gbs(dec_cap),
+        "decode_step_uncapped_lane_ms": dec_unc, "decode_gbs_uncapped_lane": gbs(dec_unc),
+        "prefill_step_alone_ms": pre_alone, "prefill_step_capped_ms": pre_cap, "prefill_step_uncapped_ms": pre_unc,
+        "prefill_tflops_alone": pre_flops / (pre_alone * 1e-3) / 1e12,
+        "prefill_tflops_capped": pre_flops / (pre_cap * 1e-3) / 1e12,
+        "decode_steps_measured": {"capped": n_cap, "uncapped": n_unc},
+        "prefill_steps_measured": {"capped": m_cap, "uncapped": m_unc},
+        "how": "decode lane: CUDA graph of the serving step replayed on one stream; prefill lane: CUDA graph of the "
+               "appends + prompt rows of 4 x 2048-token prompts replayed on a second stream, enqueued first; the "
+               "decode steps timed with events on their stream while the prefill lane runs",
+    }
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n_cap,
+        "warmup": args.warmup, "ms_per_step": dec_cap_max, "steps_per_s": 1000.0 / dec_cap_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill_lane", "launch": "cuda_graph", "decode": "serving step (5 local + 1 global)",
+                   "prefill": "4 prompts x 2048 rows, same layer shapes",
+                   "l2": "inputs larger than L2: 1.43 GB of decode KV per step",
+                   "parallelism": "dp%d (sequences sharded, no collective)" % world},
+        "roofline": {"kernel": "serving decode step beside the capped prefill lane (all its kernels)", "bound": "hbm",
+                     "achieved": gbs(dec_cap), "peak": peak, "unit": "GB/s", "frac": gbs(dec_cap) / peak,
+                     "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes_per_launch": dec_bytes,
+                     "ms_per_launch": dec_cap},
+        "lane": lane, "cpu_baseline": None, "e2e": None,
+        "gpu_launches": (3 * len(dec)) * n_cap,
+        "clocks": clk, "device_status": status,
+    }
+    print(json.dumps(line))
+    ranks.close()
+
+
 def main():
     args = parse()
     peak, peak_tf, peak_kind = peaks()
@@ -420,6 +584,10 @@ def main():
                 "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
                 "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
+        return
+
+    if args.workload == "prefill_lane":
+        prefill_lane_main(args, peak, peak_kind)
         return
 
     ranks = Ranks("nccl")

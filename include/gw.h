@@ -240,6 +240,36 @@ gw_status gw_decode_attn_local_noalloc(const gw_kv_pool* pool, const void* q, vo
 size_t gw_noalloc_scratch_bytes(void);
 
 /*
+ * gw_set_max_ctas - cap the CTAs of the attention kernels that the calling
+ * thread launches from now on (0 = one per SM, the default); appends then
+ * launch at most 16 CTAs per allowed SM.
+ *
+ * [pegainfer] "Async prefill lane": a new prompt's prefill runs on its own
+ * stream while decode goes on, capped at a share of the SMs so that it
+ * cannot take the whole GPU.  The decode and prompt-row kernels here are
+ * persistent with one CTA per SM (their shared memory allows no second), and
+ * deal their work round-robin over the CTAs they have, so a CTA cap is an SM
+ * cap: a prefill lane launched with a cap of N and a decode lane with the
+ * SM count minus N run side by side on disjoint SMs.  Results do not depend
+ * on the cap (a work unit's arithmetic never depends on which CTA runs it).
+ * The setting is per host thread and is read when a call launches (for a
+ * CUDA graph: when it is captured).
+ * Errors: GW_ERR_INVALID_ARG (max_ctas < 0).
+ */
+gw_status gw_set_max_ctas(int32_t max_ctas);
+
+/*
+ * gw_set_early_launch - whether the calling thread's later launches may
+ * start while the previous kernel of their stream is still running (1, the
+ * default: programmatic dependent launch, whose early CTAs wait on chip for
+ * their predecessor) or only once it has finished (0).  A capped prefill
+ * lane beside a decode lane should use 0: its early CTAs, waiting out a long
+ * prompt kernel, would otherwise hold registers and threads on the decode
+ * lane's SMs and keep its kernels from starting.  Never an error.
+ */
+gw_status gw_set_early_launch(int32_t on);
+
+/*
  * gw_bw_probe - a measurement aid, not part of the method: streams the first
  * floor(bytes / 8192) * 8192 bytes of the device buffer `buf` through the
  * copy pipeline of the local decode kernel (one CTA per SM, 8 warps, each

@@ -519,7 +519,7 @@ cudaError_t launch_layout(const LocalArgs& a, cudaStream_t stream) {
   const size_t smem = sizeof(GSmem<LAYOUT, HQ>);
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(num_sms()), dim3(kThreads), smem, stream, a);
+  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kThreads), smem, stream, a);
   if (e != cudaSuccess) return e;
   return launch_combine(a, HQ, 512, stream);
 }

@@ -668,7 +668,7 @@ cudaError_t launch_tc(const LocalArgs& a, cudaStream_t st) {
   auto kern = local_decode_tc_kernel<G>;
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(num_sms()), dim3(kTcWarps * 32), smem, st, a, map);
+  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kTcWarps * 32), smem, st, a, map);
   if (e != cudaSuccess) return e;
   return launch_combine(a, G, 256, st);
 }
@@ -682,7 +682,7 @@ cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   auto kern = local_decode_kernel<DT, G>;
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(num_sms()), dim3(kWarps * 32), smem, st, a);
+  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kWarps * 32), smem, st, a);
   if (e != cudaSuccess) return e;
   return launch_combine(a, G, 256, st);
 }

@@ -441,7 +441,7 @@ cudaError_t launch_lh(const LocalArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(GPSmem<LAYOUT>);
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(num_sms()), dim3(kGThreads), smem, st, a);
+  return launch_pdl(kern, dim3(grid_ctas()), dim3(kGThreads), smem, st, a);
 }
 
 template <int LAYOUT>

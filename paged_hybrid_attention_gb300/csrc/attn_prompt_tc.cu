@@ -446,7 +446,7 @@ cudaError_t launch_g(const LocalArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(TcSmem);
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(num_sms()), dim3(kTcThreads), smem, st, a, map);
+  return launch_pdl(kern, dim3(grid_ctas()), dim3(kTcThreads), smem, st, a, map);
 }
 
 }  // namespace

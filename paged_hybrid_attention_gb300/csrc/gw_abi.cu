@@ -79,6 +79,16 @@ gw_status set_error(gw_status code, const char* fn, const char* fmt, ...) {
   return code;
 }
 
+thread_local int g_max_ctas = 0;
+thread_local bool g_early_launch = true;
+
+bool early_launch() { return g_early_launch; }
+
+int grid_ctas() {
+  const int n = num_sms();
+  return g_max_ctas > 0 && g_max_ctas < n ? g_max_ctas : n;
+}
+
 int num_sms() {
   static int cached = 0;
   static std::once_flag once;
@@ -262,6 +272,19 @@ gw_status gw_decode_attn_global(const gw_kv_pool* pool, const void* q, void* out
   return attn_common("gw_decode_attn_global", false, pool, q, out, num_q_heads, batch, cu_q_rows, seq_lens,
                      block_table, max_pages_per_seq, max_q_rows, 0, scale, workspace, workspace_bytes, dev_status,
                      stream);
+}
+
+gw_status gw_set_max_ctas(int32_t max_ctas) {
+  g_err[0] = 0;
+  if (max_ctas < 0) return fail(GW_ERR_INVALID_ARG, "gw_set_max_ctas", "max_ctas (%d) < 0", max_ctas);
+  g_max_ctas = max_ctas;
+  return GW_OK;
+}
+
+gw_status gw_set_early_launch(int32_t on) {
+  g_err[0] = 0;
+  g_early_launch = on != 0;
+  return GW_OK;
 }
 
 gw_status gw_bw_probe(const void* buf, size_t bytes, int32_t* dev_status, void* stream) {

@@ -97,6 +97,12 @@ struct AppendArgs {
 };
 
 int num_sms();
+// CTAs of a persistent attention kernel: one per SM, or the calling thread's
+// gw_set_max_ctas cap if smaller.
+int grid_ctas();
+// Whether this thread's launches may start before their predecessor in the
+// stream has finished (programmatic dependent launch); gw_set_early_launch.
+bool early_launch();
 
 // Records `fmt` (printf-style) as the calling thread's gw_last_error message,
 // prefixed by `fn`, and returns `code`.

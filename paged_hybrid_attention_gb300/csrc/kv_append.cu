@@ -184,7 +184,7 @@ __global__ void append_global_kernel(const AppendArgs a) {
 
 int grid_for(int64_t items, int block) {
   int64_t blocks = (items + block - 1) / block;
-  const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+  const int64_t cap = static_cast<int64_t>(grid_ctas()) * 16;
   return static_cast<int>(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);
 }
 

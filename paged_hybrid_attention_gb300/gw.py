@@ -29,7 +29,7 @@ LAYOUTS = {"local": LAYOUT_LOCAL, "folded": LAYOUT_GLOBAL_FOLDED, "full": LAYOUT
 DTYPES = {"bf16": KV_BF16, "e4m3": KV_E4M3}
 EXPORTS = ["gw_pool_page_bytes", "gw_kv_append", "gw_decode_attn_local", "gw_decode_attn_global",
            "gw_attn_workspace_bytes", "gw_last_error", "gw_version", "gw_decode_attn_local_noalloc",
-           "gw_noalloc_scratch_bytes", "gw_bw_probe"]
+           "gw_noalloc_scratch_bytes", "gw_bw_probe", "gw_set_max_ctas", "gw_set_early_launch"]
 
 
 class GwError(RuntimeError):
@@ -65,6 +65,10 @@ _lib.gw_noalloc_scratch_bytes.argtypes = []
 _lib.gw_noalloc_scratch_bytes.restype = _sz
 _lib.gw_bw_probe.argtypes = [_vp, _sz, _vp, _vp]
 _lib.gw_bw_probe.restype = _i32
+_lib.gw_set_max_ctas.argtypes = [_i32]
+_lib.gw_set_max_ctas.restype = _i32
+_lib.gw_set_early_launch.argtypes = [_i32]
+_lib.gw_set_early_launch.restype = _i32
 _lib.gw_last_error.argtypes = []
 _lib.gw_last_error.restype = ctypes.c_char_p
 _lib.gw_version.argtypes = []
@@ -188,6 +192,18 @@ def decode_attn_local_noalloc(pool, q, out, cu_q_rows, seq_lens, block_table, wi
                                              int(seq_lens.numel()), _ptr(cu_q_rows), _ptr(seq_lens),
                                              _ptr(block_table), int(block_table.shape[1]), int(max_q_rows),
                                              int(window), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def set_max_ctas(max_ctas):
+    """gw_set_max_ctas: cap the CTAs (= SMs) of this thread's later attention
+    calls; 0 restores one per SM."""
+    _check(_lib.gw_set_max_ctas(int(max_ctas)))
+
+
+def set_early_launch(on):
+    """gw_set_early_launch: allow (True) or forbid programmatic early launch
+    for this thread's later calls."""
+    _check(_lib.gw_set_early_launch(1 if on else 0))
 
 
 def bw_probe(buf, dev_status=None, stream=None):

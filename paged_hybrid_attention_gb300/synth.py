@@ -23,6 +23,9 @@ layers per global layer):
               chunked walk); both families.
   stack48     the serving shapes over a 48-layer stack (40 local + 8 global
               layers, each with its own pools).
+  prefill     4 new prompts of 2048 rows with the serving families (5 local
+              + 1 global layers): the work of an async prefill lane that runs
+              beside the serving decode step.
 
 Every sequence's tensors come from their own generator seed, so one sequence
 can be regenerated alone (the oracle checks samples of the big workloads).
@@ -108,6 +111,10 @@ def spec(name):
         loc = Family("local", "bf16", "local", 16, 256, 256, 1e4, 1024)
         glo = Family("global", "bf16", "folded", 1, 512, 128, 1e6, 0)
         return Spec(name, 1006, 32, lens, rows, {"local": loc, "global": glo}, 5, 1)
+    if name == "prefill":
+        base = spec("serving")
+        return Spec(name, 1007, base.num_q_heads, np.full(4, 2048, np.int32), np.full(4, 2048, np.int32),
+                    base.families, 5, 1)
     if name == "stack48":
         base = spec("serving")
         return Spec(name, base.seed, base.num_q_heads, base.lens, base.n_rows, base.families, 40, 8)

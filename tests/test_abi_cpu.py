@@ -128,3 +128,13 @@ def test_bw_probe_host_validation():
     assert L.gw_bw_probe(_fake((1 << 24) + 8), 1 << 20, None, None) == gw.GW_ERR_INVALID_ARG   # misaligned
     assert L.gw_bw_probe(_fake(), 4096, None, None) == gw.GW_ERR_INVALID_ARG                   # < one stage
     assert "8192" in gw.last_error()
+
+
+def test_set_max_ctas_validation():
+    L = gw.lib()
+    assert L.gw_set_max_ctas(-1) == gw.GW_ERR_INVALID_ARG
+    assert gw.last_error().startswith("gw_set_max_ctas:")
+    assert L.gw_set_max_ctas(40) == gw.GW_OK
+    assert L.gw_set_max_ctas(0) == gw.GW_OK
+    assert L.gw_set_early_launch(0) == gw.GW_OK
+    assert L.gw_set_early_launch(1) == gw.GW_OK
