@@ -54,6 +54,7 @@ UNIT = "GB/s"
 NCU_TRAFFIC = {
     "serving": (275993344, "attn_local.cu", "fd1ef7069c77a633b591b7a12b1e79d7774fc13c1ce4c2e2de4bf58eec9b7157"),
     "fp8_local": (552958208, "attn_local.cu", "fd1ef7069c77a633b591b7a12b1e79d7774fc13c1ce4c2e2de4bf58eec9b7157"),
+    "long_global": (1354883072, "attn_global.cu", "51404db639b8c990aefc6dadc489ac1d85a653b1199e6bfcc80ec05359004c0d"),
 }
 
 
