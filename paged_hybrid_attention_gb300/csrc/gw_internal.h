@@ -33,6 +33,19 @@ __host__ __device__ __forceinline__ int local_chunks(int L, int window, int chun
   return (p1 - p0 + chunk) / chunk;
 }
 
+// An upper bound on local_chunks(L, window, chunk) over L <= 16 * max_pages.
+__host__ __device__ __forceinline__ int local_max_chunks(int max_pages, int window, int chunk) {
+  const int span = (window - 1) / 16 + 1;  // p1 - p0 once L > window
+  const int d = max_pages - 1 < span ? max_pages - 1 : span;
+  return (d + chunk) / chunk;
+}
+
+// An upper bound on global_chunks(L) over L <= 16 * max_pages.
+__host__ __device__ __forceinline__ int global_max_chunks(int max_pages) {
+  const int c = (max_pages + kGlobalChunkPagesMin - 1) / kGlobalChunkPagesMin;
+  return c < kGlobalMaxChunks ? c : kGlobalMaxChunks;
+}
+
 __host__ __device__ __forceinline__ int global_chunk_pages(int L) {
   const int pages = (L + 15) / 16;
   int cpg = kGlobalChunkPagesMin;
@@ -109,8 +122,9 @@ bool early_launch();
 gw_status set_error(gw_status code, const char* fn, const char* fmt, ...);
 
 // Log-sum-exp merge of each decode row's partials into bf16 `out`; units of
-// heads_per_unit q heads, planned as in a.unit_base.
-cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim, cudaStream_t st);
+// heads_per_unit q heads, planned as in a.unit_base, at most max_chunks
+// chunks per sequence.
+cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim, int max_chunks, cudaStream_t st);
 
 cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_bw_probe(const void* buf, int64_t chunks, int32_t* status, cudaStream_t st);

@@ -9,72 +9,135 @@
 namespace gw {
 namespace {
 
-// One warp per (sequence, q head, 128-dim slice); lane l owns 4 dims of the
-// slice.  The sequence's units of this head's group are consecutive (unit_base
-// holds the plan the decode kernel used).  The (m, l) of chunks lane,
-// lane + 32, ... give the warp maximum M while the first batch of kB chunks'
-// partials is already being fetched; then every lane sums w_c * o_c over its
-// dims in chunk order, kB chunks' loads in flight at a time.  The result is
-// written as bf16.
+// A task is (sequence, q head, 128-dim slice); lane l owns 4 dims of the
+// slice.  The sequence's units of this head's group are consecutive
+// (unit_base holds the plan the decode kernel used), and its nc chunks are
+// merged in groups of kB: with M the maximum of the chunks' m and
+// w_c = 2^(m_c - M),
+//   S_g = sum over the group's chunks, in chunk order, of w_c * o_c
+//   D_g = sum over the group's chunks, in chunk order, of w_c * l_c
+//   o   = (S_0 + S_1 + ...) / (D_0 + D_1 + ...), groups added in order.
+// That arithmetic depends only on nc, so a row's bits never depend on how
+// the tasks are mapped to warps.  A task gets W warps (1, 2, 4 or 8, chosen
+// from the call's bound on chunks per sequence): warp j of the task merges
+// groups j, j + W, ... (R rounds), the task's maximum and group sums meeting
+// in shared memory, so a long sequence's partials are fetched by W warps at
+// once.  Lane b < kB fetches (m, l) of the group's chunk b, every lane its
+// dims of all kB chunks.  The result is written as bf16.
 template <int D>
-__global__ void combine_kernel(const LocalArgs a, int G) {
+__global__ void __launch_bounds__(256, 2) combine_kernel(const LocalArgs a, int G, int W, int R) {
   constexpr int kSlices = D / 128;
-  constexpr int kB = 16;  // chunks per batch
+  constexpr int kB = 16;  // chunks per group
+  __shared__ float4 s_sum[8][32];
+  __shared__ float s_den[8], s_max[8];
   pdl_wait();
   pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (wid >= static_cast<int64_t>(a.batch) * a.num_q_heads * kSlices) return;
-  const int slice = static_cast<int>(wid % kSlices);
-  const int64_t sh = wid / kSlices;
-  const int s = static_cast<int>(sh / a.num_q_heads), h = static_cast<int>(sh % a.num_q_heads);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int j = warp % W, tw = warp - j;  // warp within the task, the task's first warp
+  const int64_t task = (static_cast<int64_t>(blockIdx.x) * 8 + warp) / W;
+  const bool in_grid = task < static_cast<int64_t>(a.batch) * a.num_q_heads * kSlices;
+  const int slice = static_cast<int>(task % kSlices);
+  const int64_t sh = task / kSlices;
+  const int s = in_grid ? static_cast<int>(sh / a.num_q_heads) : 0;
+  const int h = static_cast<int>(sh % a.num_q_heads);
   // independent loads, issued together (one round trip before the partials)
   const int row0 = a.cu_q_rows[s], row1 = a.cu_q_rows[s + 1];
   const int ub_s = a.unit_base[s], ub_s1 = a.unit_base[s + 1], ub_total = a.unit_base[a.batch];
-  if (row1 - row0 != 1) return;
+  const bool live = in_grid && row1 - row0 == 1;
   const int groups = a.num_q_heads / G;  // units of a sequence = groups x chunks
-  const int nc = ub_total <= a.max_units ? (ub_s1 - ub_s) / groups : 0;
-  const int g = h / G, hh = h % G;
-  const int64_t ub = ub_s + static_cast<int64_t>(g) * nc;
+  const int nc = live && ub_total <= a.max_units ? (ub_s1 - ub_s) / groups : 0;
+  const int64_t ub = ub_s + static_cast<int64_t>(h / G) * nc;
+  const int hh = h % G;
   const int dim0 = slice * 128 + lane * 4;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
   float4 u[kB];
-  float2 ml[kB];
-  auto fetch = [&](int c0) {
+  float2 ml = make_float2(-INFINITY, 0.f);
+  const float2* ml_base = a.part_ml + ub * G + hh;  // chunk c at ml_base[c * G]
+  const float* o_base = a.part_o + (ub * G + hh) * D + dim0;  // chunk c at o_base + c * G * D
+  const int o_stride = G * D;
+  const float* line_base = o_base - lane * 4;  // the slice's first 128-byte line, chunk 0
+  auto fetch = [&](int g) {
+    const int c0 = g * kB;
+    if (lane < kB && c0 + lane < nc) ml = ml_base[(c0 + lane) * G];
+    const float* po = o_base + static_cast<int64_t>(c0) * o_stride;
 #pragma unroll
-    for (int b = 0; b < kB; ++b) {
-      if (c0 + b < nc) {
-        const int64_t row = (ub + c0 + b) * G + hh;
-        ml[b] = a.part_ml[row];
-        u[b] = *reinterpret_cast<const float4*>(a.part_o + row * D + dim0);
-      }
+    for (int b = 0; b < kB; ++b)
+      if (c0 + b < nc) u[b] = *reinterpret_cast<const float4*>(po + b * o_stride);
+  };
+  fetch(j);
+  // the maximum over this warp's groups, then over the task's warps
+  float mx = ml.x;
+  for (int r = 1; r < R; ++r) {
+    const int c = (r * W + j) * kB + lane;
+    if (lane < kB && c < nc) mx = fmaxf(mx, ml_base[c * G].x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float M = mx;
+  if (W > 1) {
+    if (lane == 0) s_max[warp] = mx;
+    __syncthreads();
+    for (int k = 0; k < W; ++k) M = fmaxf(M, s_max[tw + k]);
+  }
+  float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  auto add = [&](int g, const float4& sg, float dg) {  // groups in order
+    if (g == 0) {
+      tot = sg;
+      den = dg;
+    } else {
+      tot.x += sg.x;
+      tot.y += sg.y;
+      tot.z += sg.z;
+      tot.w += sg.w;
+      den += dg;
     }
   };
-  fetch(0);
-  float M = -INFINITY;
-  for (int c = lane; c < nc; c += 32) M = fmaxf(M, a.part_ml[(ub + c) * G + hh].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (M != -INFINITY) {
-    for (int c0 = 0; c0 < nc; c0 += kB) {
-      if (c0 > 0) fetch(c0);
+  for (int r = 0; r < R; ++r) {
+    const int g = r * W + j;
+    if (r > 0) fetch(g);
+    float4 sg = make_float4(0.f, 0.f, 0.f, 0.f);
+    float dg = 0.f;
+    if (M != -INFINITY) {
+      const float wl = lane < kB && g * kB + lane < nc ? ex2(ml.x - M) : 0.f;
 #pragma unroll
       for (int b = 0; b < kB; ++b) {
-        if (c0 + b < nc) {
-          const float wgt = ex2(ml[b].x - M);
-          den += wgt * ml[b].y;
-          acc.x += wgt * u[b].x;
-          acc.y += wgt * u[b].y;
-          acc.z += wgt * u[b].z;
-          acc.w += wgt * u[b].w;
+        if (g * kB + b < nc) {
+          const float wb = __shfl_sync(0xffffffffu, wl, b);
+          const float lb = __shfl_sync(0xffffffffu, ml.y, b);
+          dg = fmaf(wb, lb, dg);
+          sg.x = fmaf(wb, u[b].x, sg.x);
+          sg.y = fmaf(wb, u[b].y, sg.y);
+          sg.z = fmaf(wb, u[b].z, sg.z);
+          sg.w = fmaf(wb, u[b].w, sg.w);
         }
       }
+      // Every lane has consumed its loads of the group's slices: drop their
+      // four 128-byte lines per chunk from L2 unwritten (nothing reads them
+      // again before the next decode call rewrites them).
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int idx = lane + 32 * k, b = idx >> 2;
+        if (g * kB + b < nc)
+          discard_l2(line_base + static_cast<int64_t>(g * kB + b) * o_stride + (idx & 3) * 32);
+      }
+    }
+    if (W == 1) {
+      if (g * kB < nc) add(g, sg, dg);
+    } else {
+      s_sum[warp][lane] = sg;
+      if (lane == 0) s_den[warp] = dg;
+      __syncthreads();
+      if (j == 0)
+        for (int k = 0; k < W; ++k)
+          if ((r * W + k) * kB < nc) add(r * W + k, s_sum[tw + k][lane], s_den[tw + k]);
+      __syncthreads();
     }
   }
+  if (j != 0 || !live) return;
   const float inv = den > 0.f ? 1.f / den : 0.f;
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  __nv_bfloat162 lo = __floats2bfloat162_rn(tot.x * inv, tot.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(tot.z * inv, tot.w * inv);
   uint2 w;
   w.x = *reinterpret_cast<uint32_t*>(&lo);
   w.y = *reinterpret_cast<uint32_t*>(&hi);
@@ -83,11 +146,15 @@ __global__ void combine_kernel(const LocalArgs a, int G) {
 
 }  // namespace
 
-cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim, cudaStream_t st) {
-  const int64_t warps = static_cast<int64_t>(a.batch) * a.num_q_heads * (head_dim / 128);
+cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim, int max_chunks, cudaStream_t st) {
+  constexpr int kB = 16;
+  const int ngroups = (max_chunks + kB - 1) / kB;
+  const int W = ngroups <= 2 ? 1 : ngroups <= 4 ? 4 : 8;
+  const int R = (ngroups + W - 1) / W > 0 ? (ngroups + W - 1) / W : 1;
+  const int64_t warps = static_cast<int64_t>(a.batch) * a.num_q_heads * (head_dim / 128) * W;
   const dim3 grid(static_cast<unsigned>((warps + 7) / 8));
-  if (head_dim == 256) return launch_pdl(combine_kernel<256>, grid, dim3(256), 0, st, a, heads_per_unit);
-  return launch_pdl(combine_kernel<512>, grid, dim3(256), 0, st, a, heads_per_unit);
+  if (head_dim == 256) return launch_pdl(combine_kernel<256>, grid, dim3(256), 0, st, a, heads_per_unit, W, R);
+  return launch_pdl(combine_kernel<512>, grid, dim3(256), 0, st, a, heads_per_unit, W, R);
 }
 
 }  // namespace gw
