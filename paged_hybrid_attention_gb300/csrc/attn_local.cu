@@ -365,16 +365,14 @@ __global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kerne
     if (++c_i == d.n) {
       // ---- unit done: write the unnormalised partial
       float* po = a.part_o + static_cast<int64_t>(d.unit) * G * 256 + lane * 8;
-      const uint64_t keep = policy_evict_last();
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float l = lsum[h];
 #pragma unroll
         for (int O = 1; O < 32; O <<= 1) l += __shfl_xor_sync(0xffffffffu, l, O);
-        st_hint(reinterpret_cast<float4*>(po + h * 256), make_float4(o[h][0], o[h][1], o[h][2], o[h][3]), keep);
-        st_hint(reinterpret_cast<float4*>(po + h * 256 + 4), make_float4(o[h][4], o[h][5], o[h][6], o[h][7]),
-                keep);
-        if (lane == h) st_hint(a.part_ml + static_cast<int64_t>(d.unit) * G + h, make_float2(m[h], l), keep);
+        *reinterpret_cast<float4*>(po + h * 256) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+        *reinterpret_cast<float4*>(po + h * 256 + 4) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+        if (lane == h) a.part_ml[static_cast<int64_t>(d.unit) * G + h] = make_float2(m[h], l);
       }
       c_i = 0;
       c_slot = (c_slot + 1) % kRing;
@@ -641,19 +639,17 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
       // ---- unit done: write the unnormalised partial (m, l, o)
       float l = lsum + __shfl_xor_sync(0xffffffffu, lsum, 1);
       l += __shfl_xor_sync(0xffffffffu, l, 2);
-      const uint64_t keep = policy_evict_last();
-      if ((lane & 3) == 0 && hq < G)
-        st_hint(a.part_ml + static_cast<int64_t>(d.unit) * G + hq, make_float2(m_ref, l), keep);
+      if ((lane & 3) == 0 && hq < G) a.part_ml[static_cast<int64_t>(d.unit) * G + hq] = make_float2(m_ref, l);
       float* po = a.part_o + static_cast<int64_t>(d.unit) * G * 256 + (lane >> 2);
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         if (kq < G) {
-          st_hint(po + kq * 256 + 16 * j, o[j][0], keep);
-          st_hint(po + kq * 256 + 16 * j + 8, o[j][2], keep);
+          po[kq * 256 + 16 * j] = o[j][0];
+          po[kq * 256 + 16 * j + 8] = o[j][2];
         }
         if (kq + 1 < G) {
-          st_hint(po + (kq + 1) * 256 + 16 * j, o[j][1], keep);
-          st_hint(po + (kq + 1) * 256 + 16 * j + 8, o[j][3], keep);
+          po[(kq + 1) * 256 + 16 * j] = o[j][1];
+          po[(kq + 1) * 256 + 16 * j + 8] = o[j][3];
         }
       }
       c_i = 0;
@@ -674,7 +670,7 @@ cudaError_t launch_tc(const LocalArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(grid_ctas()), dim3(kTcWarps * 32), smem, st, a, map);
   if (e != cudaSuccess) return e;
-  return launch_combine(a, G, 256, local_max_chunks(a.max_pages, a.window, TcTraits::kChunk), st);
+  return launch_combine(a, G, 256, local_max_chunks(a.max_pages, a.window, TcTraits::kChunk), false, st);
 }
 
 template <int DT, int G>
@@ -688,7 +684,7 @@ cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(grid_ctas()), dim3(kWarps * 32), smem, st, a);
   if (e != cudaSuccess) return e;
-  return launch_combine(a, G, 256, local_max_chunks(a.max_pages, a.window, T::kChunk), st);
+  return launch_combine(a, G, 256, local_max_chunks(a.max_pages, a.window, T::kChunk), false, st);
 }
 
 template <int DT>

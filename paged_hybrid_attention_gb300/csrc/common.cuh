@@ -109,21 +109,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
-// Stores under an L2 eviction policy: split-KV partials are written with
-// evict_last so that they are still in L2 when the combine reads them.
-__device__ __forceinline__ void st_hint(float* p, float v, uint64_t pol) {
-  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
-}
-__device__ __forceinline__ void st_hint(float2* p, float2 v, uint64_t pol) {
-  asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(p), "f"(v.x), "f"(v.y), "l"(pol)
-               : "memory");
-}
-__device__ __forceinline__ void st_hint(float4* p, float4 v, uint64_t pol) {
-  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y),
-               "f"(v.z), "f"(v.w), "l"(pol)
-               : "memory");
-}
-
 // Invalidate the 128-byte L2 line at p (128-byte aligned) without writing it
 // back: scratch data that has been read for the last time.
 __device__ __forceinline__ void discard_l2(const void* p) {

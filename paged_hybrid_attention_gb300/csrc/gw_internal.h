@@ -123,8 +123,10 @@ gw_status set_error(gw_status code, const char* fn, const char* fmt, ...);
 
 // Log-sum-exp merge of each decode row's partials into bf16 `out`; units of
 // heads_per_unit q heads, planned as in a.unit_base, at most max_chunks
-// chunks per sequence.
-cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim, int max_chunks, cudaStream_t st);
+// chunks per sequence; with `discard`, the merged partials' L2 lines are
+// dropped unwritten.
+cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim, int max_chunks, bool discard,
+                           cudaStream_t st);
 
 cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_bw_probe(const void* buf, int64_t chunks, int32_t* status, cudaStream_t st);

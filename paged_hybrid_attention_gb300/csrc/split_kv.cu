@@ -23,9 +23,11 @@ namespace {
 // groups j, j + W, ... (R rounds), the task's maximum and group sums meeting
 // in shared memory, so a long sequence's partials are fetched by W warps at
 // once.  Lane b < kB fetches (m, l) of the group's chunk b, every lane its
-// dims of all kB chunks.  The result is written as bf16.
+// dims of all kB chunks.  The result is written as bf16.  With `discard`,
+// each merged chunk slice is then dropped from L2 unwritten (nothing reads
+// it again before the next decode call rewrites it).
 template <int D>
-__global__ void __launch_bounds__(256, 2) combine_kernel(const LocalArgs a, int G, int W, int R) {
+__global__ void __launch_bounds__(256, 2) combine_kernel(const LocalArgs a, int G, int W, int R, bool discard) {
   constexpr int kSlices = D / 128;
   constexpr int kB = 16;  // chunks per group
   __shared__ float4 s_sum[8][32];
@@ -111,15 +113,16 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const LocalArgs a, int 
           sg.w = fmaf(wb, u[b].w, sg.w);
         }
       }
-      // Every lane has consumed its loads of the group's slices: drop their
-      // four 128-byte lines per chunk from L2 unwritten (nothing reads them
-      // again before the next decode call rewrites them).
-      __syncwarp();
+      if (discard) {
+        // every lane has consumed its loads of the group's slices: drop
+        // their four 128-byte lines per chunk
+        __syncwarp();
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int idx = lane + 32 * k, b = idx >> 2;
-        if (g * kB + b < nc)
-          discard_l2(line_base + static_cast<int64_t>(g * kB + b) * o_stride + (idx & 3) * 32);
+        for (int k = 0; k < 2; ++k) {
+          const int idx = lane + 32 * k, b = idx >> 2;
+          if (g * kB + b < nc)
+            discard_l2(line_base + static_cast<int64_t>(g * kB + b) * o_stride + (idx & 3) * 32);
+        }
       }
     }
     if (W == 1) {
@@ -146,15 +149,16 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const LocalArgs a, int 
 
 }  // namespace
 
-cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim, int max_chunks, cudaStream_t st) {
+cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim, int max_chunks, bool discard,
+                           cudaStream_t st) {
   constexpr int kB = 16;
   const int ngroups = (max_chunks + kB - 1) / kB;
   const int W = ngroups <= 2 ? 1 : ngroups <= 4 ? 4 : 8;
   const int R = (ngroups + W - 1) / W > 0 ? (ngroups + W - 1) / W : 1;
   const int64_t warps = static_cast<int64_t>(a.batch) * a.num_q_heads * (head_dim / 128) * W;
   const dim3 grid(static_cast<unsigned>((warps + 7) / 8));
-  if (head_dim == 256) return launch_pdl(combine_kernel<256>, grid, dim3(256), 0, st, a, heads_per_unit, W, R);
-  return launch_pdl(combine_kernel<512>, grid, dim3(256), 0, st, a, heads_per_unit, W, R);
+  if (head_dim == 256) return launch_pdl(combine_kernel<256>, grid, dim3(256), 0, st, a, heads_per_unit, W, R, discard);
+  return launch_pdl(combine_kernel<512>, grid, dim3(256), 0, st, a, heads_per_unit, W, R, discard);
 }
 
 }  // namespace gw
