@@ -52,9 +52,9 @@ UNIT = "GB/s"
 # was captured from; reported as null once the source no longer matches.
 # workload: (bytes, source file under csrc/, sha256)
 NCU_TRAFFIC = {
-    "serving": (275993344, "attn_local.cu", "fd1ef7069c77a633b591b7a12b1e79d7774fc13c1ce4c2e2de4bf58eec9b7157"),
-    "fp8_local": (552958208, "attn_local.cu", "fd1ef7069c77a633b591b7a12b1e79d7774fc13c1ce4c2e2de4bf58eec9b7157"),
-    "long_global": (1354883072, "attn_global.cu", "51404db639b8c990aefc6dadc489ac1d85a653b1199e6bfcc80ec05359004c0d"),
+    "serving": (276123392, "attn_local.cu", "f646b15136100a9cd5a6080101f3973ee5d70400f77d9973b1b3f31ce60198fc"),
+    "fp8_local": (552956672, "attn_local.cu", "f646b15136100a9cd5a6080101f3973ee5d70400f77d9973b1b3f31ce60198fc"),
+    "long_global": (1354902016, "attn_global.cu", "45415b71619aa2fdb9035e3a5794e19fbd62e50c0e01c7327185d1cffa24e588"),
 }
 
 
