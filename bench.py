@@ -52,9 +52,9 @@ UNIT = "GB/s"
 # was captured from; reported as null once the source no longer matches.
 # workload: (bytes, source file under csrc/, sha256)
 NCU_TRAFFIC = {
-    "serving": (276123392, "attn_local.cu", "f646b15136100a9cd5a6080101f3973ee5d70400f77d9973b1b3f31ce60198fc"),
-    "fp8_local": (552956672, "attn_local.cu", "f646b15136100a9cd5a6080101f3973ee5d70400f77d9973b1b3f31ce60198fc"),
-    "long_global": (1354902016, "attn_global.cu", "45415b71619aa2fdb9035e3a5794e19fbd62e50c0e01c7327185d1cffa24e588"),
+    "serving": (275295232, "attn_local.cu", "c048a84f0f6460a271be8624ef52ca8e3fc47ba421d3a2c32a5a894a96fc7994"),
+    "fp8_local": (552702976, "attn_local.cu", "c048a84f0f6460a271be8624ef52ca8e3fc47ba421d3a2c32a5a894a96fc7994"),
+    "long_global": (1354113536, "attn_global.cu", "f5e5e772b7fe6919bc81088f7656f3f034de56d3e829e58306333b7b79f06b50"),
 }
 
 

@@ -521,9 +521,9 @@ cudaError_t launch_layout(const LocalArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(grid_ctas()), dim3(kThreads), smem, stream, a);
   if (e != cudaSuccess) return e;
-  // Dropping the merged partials from L2 pays for the folded pool (24.7 vs
-  // 26.9 us per serving call) but not for the full control (427 vs 415 us
-  // per long-context call), measured.
+  // Dropping the merged partials from L2 unwritten pays for the folded pool
+  // (24.7 vs 26.9 us per serving call) but not for the full control (427 vs
+  // 415 us per long-context call), measured.
   return launch_combine(a, HQ, 512, global_max_chunks(a.max_pages), LAYOUT == GW_LAYOUT_GLOBAL_FOLDED, stream);
 }
 
