@@ -18,7 +18,7 @@ namespace {
 //   D_g = sum over the group's chunks, in chunk order, of w_c * l_c
 //   o   = (S_0 + S_1 + ...) / (D_0 + D_1 + ...), groups added in order.
 // That arithmetic depends only on nc, so a row's bits never depend on how
-// the tasks are mapped to warps.  A task gets W warps (1, 2, 4 or 8, chosen
+// the tasks are mapped to warps.  A task gets W warps (1, 4 or 8, chosen
 // from the call's bound on chunks per sequence): warp j of the task merges
 // groups j, j + W, ... (R rounds), the task's maximum and group sums meeting
 // in shared memory, so a long sequence's partials are fetched by W warps at
@@ -153,6 +153,9 @@ cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim,
                            cudaStream_t st) {
   constexpr int kB = 16;
   const int ngroups = (max_chunks + kB - 1) / kB;
+  // One warp walks up to two groups itself (a serving layer's block table
+  // bounds a sequence at 15 global or 9 local chunks); longer sequences
+  // spread their groups over 4 or 8 warps of one CTA.
   const int W = ngroups <= 2 ? 1 : ngroups <= 4 ? 4 : 8;
   const int R = (ngroups + W - 1) / W > 0 ? (ngroups + W - 1) / W : 1;
   const int64_t warps = static_cast<int64_t>(a.batch) * a.num_q_heads * (head_dim / 128) * W;
