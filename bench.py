@@ -69,6 +69,9 @@ def parse():
                          "prefill_lane (the serving step beside an SM-capped prefill lane)")
     ap.add_argument("--lane-share", type=float, default=0.35,
                     help="prefill_lane: share of the SMs given to the prefill lane")
+    ap.add_argument("--bucket", type=int, default=0,
+                    help="pad every layer's step to this many sequence slots, as a CUDA graph captured for a "
+                         "batch bucket runs a smaller batch (0: no padding)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch every step eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu", action="store_true")
@@ -136,7 +139,7 @@ def prompt_flops(layer):
 
 
 class GpuLayer:
-    def __init__(self, layer, gw, gen, dev):
+    def __init__(self, layer, gw, gen, dev, bucket=0):
         fam, sp = layer.fam, layer.spec
         self.layer, self.fam = layer, fam
         self.pool = gw.KVPool(fam.layout, fam.dtype, layer.num_pages, fam.kv_heads, device=dev)
@@ -167,6 +170,29 @@ class GpuLayer:
                                      max(1, fam.window), device=dev)
         self.kv_bytes = kv_bytes(layer)
         self.prompt_flops = prompt_flops(layer)
+        if bucket > len(sp.lens):
+            self._pad_to_bucket(gw, bucket, dev)
+
+    def _pad_to_bucket(self, gw, bucket, dev):
+        """Pad the step to `bucket` sequence slots, as a graph captured for a
+        batch bucket runs a smaller batch: the extra slots get zero query rows
+        (the decode kernels plan no work for them) and append rows that write
+        a sink page no sequence reads."""
+        fam, sp = self.fam, self.layer.spec
+        extra = bucket - len(sp.lens)
+        sink = int(self.layer.unused_pages[0])
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.cu = torch.cat([self.cu, self.cu[-1:].repeat(extra)])
+        self.lens = torch.cat([self.lens, torch.zeros(extra, **i32)])
+        self.bt = torch.cat([self.bt, torch.full((extra, self.bt.shape[1]), -1, **i32)])
+        self.slot_new = torch.cat([self.slot_new, sink * 16 + torch.arange(extra, **i32) % 16])
+        self.pos_new = torch.cat([self.pos_new, torch.zeros(extra, **i32)])
+        self.k_new = torch.cat([self.k_new, torch.zeros((extra,) + tuple(self.k_new.shape[1:]), dtype=torch.bfloat16,
+                                                        device=dev)])
+        self.v_new = torch.cat([self.v_new, torch.zeros((extra,) + tuple(self.v_new.shape[1:]), dtype=torch.bfloat16,
+                                                        device=dev)])
+        self.ws = gw.alloc_workspace(self.pool, sp.num_q_heads, bucket, self.bt.shape[1], self.max_q_rows,
+                                     max(1, fam.window), device=dev)
 
     def _append_random(self, gw, gen, dev, slot, pos, sig, chunk=1 << 18):
         fam = self.fam
@@ -601,7 +627,7 @@ def main():
 
     sp, layers = workload_layers(args.workload, rank)
     gen = torch.Generator(device=dev).manual_seed(sp.seed + 17 * rank)
-    glayers = [GpuLayer(l, gw, gen, dev) for l in layers]
+    glayers = [GpuLayer(l, gw, gen, dev, bucket=args.bucket) for l in layers]
     arena_in = Arena(glayers, GpuLayer.INPUTS, dev)   # the step's inputs, one upload
     arena_out = Arena(glayers, ("out",), dev)         # the step's outputs, one download
     torch.cuda.synchronize()
@@ -847,6 +873,7 @@ def main():
                    "layers": "%d local + %d global" % (sp.n_local_layers,
                                                                                    sp.n_global_layers),
                    "batch": int(len(sp.lens)), "kv_bytes_per_step": step_bytes, "q_heads": sp.num_q_heads,
+                   "bucket": args.bucket if args.bucket > len(sp.lens) else None,
                    "l2": "inputs larger than L2: %.2f GB of KV read per step" % (step_bytes / 1e9),
                    "parallelism": "dp%d (sequences sharded, no collective)" % world},
         "roofline": roofline,
