@@ -52,9 +52,9 @@ UNIT = "GB/s"
 # was captured from; reported as null once the source no longer matches.
 # workload: (bytes, source file under csrc/, sha256)
 NCU_TRAFFIC = {
-    "serving": (275295232, "attn_local.cu", "c048a84f0f6460a271be8624ef52ca8e3fc47ba421d3a2c32a5a894a96fc7994"),
-    "fp8_local": (552702976, "attn_local.cu", "c048a84f0f6460a271be8624ef52ca8e3fc47ba421d3a2c32a5a894a96fc7994"),
-    "long_global": (1354113536, "attn_global.cu", "f5e5e772b7fe6919bc81088f7656f3f034de56d3e829e58306333b7b79f06b50"),
+    "serving": (275542528, "attn_local.cu", "db9fb085d8075f8b289ad1d35df850b9606686f187eccb4dee26c40c180e501d"),
+    "fp8_local": (552907520, "attn_local.cu", "db9fb085d8075f8b289ad1d35df850b9606686f187eccb4dee26c40c180e501d"),
+    "long_global": (1354496512, "attn_global.cu", "f6add234ef69883f75cd07c7c8ad98348d3192bd7b1e56001c15c1040c3ccc69"),
 }
 
 
@@ -72,6 +72,11 @@ def parse():
     ap.add_argument("--bucket", type=int, default=0,
                     help="pad every layer's step to this many sequence slots, as a CUDA graph captured for a "
                          "batch bucket runs a smaller batch (0: no padding)")
+    ap.add_argument("--no-early-inputs", action="store_true",
+                    help="decode kernels read their plan inputs only after the previous kernel has finished "
+                         "(gw_set_early_inputs(0)); by default they read them while it runs, which holds here "
+                         "because a step's row offsets, lengths and block tables are uploaded before its first "
+                         "layer")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch every step eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu", action="store_true")
@@ -446,6 +451,7 @@ def prefill_lane_main(args, peak, peak_kind):
     torch.cuda.set_device(dev)
     ranks.device = dev
     from paged_hybrid_attention_gb300 import gw
+    gw.set_early_inputs(not args.no_early_inputs)
 
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     share = args.lane_share
@@ -573,7 +579,7 @@ def prefill_lane_main(args, peak, peak_kind):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n_cap,
         "warmup": args.warmup, "ms_per_step": dec_cap_max, "steps_per_s": 1000.0 / dec_cap_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "prefill_lane", "launch": "cuda_graph", "decode": "serving step (5 local + 1 global)",
+        "config": {"workload": "prefill_lane", "launch": "cuda_graph", "early_inputs": not args.no_early_inputs, "decode": "serving step (5 local + 1 global)",
                    "prefill": "4 prompts x 2048 rows, same layer shapes",
                    "l2": "inputs larger than L2: 1.43 GB of decode KV per step",
                    "parallelism": "dp%d (sequences sharded, no collective)" % world},
@@ -624,6 +630,7 @@ def main():
     torch.cuda.set_device(dev)
     ranks.device = dev
     from paged_hybrid_attention_gb300 import gw
+    gw.set_early_inputs(not args.no_early_inputs)
 
     sp, layers = workload_layers(args.workload, rank)
     gen = torch.Generator(device=dev).manual_seed(sp.seed + 17 * rank)
@@ -874,6 +881,7 @@ def main():
                                                                                    sp.n_global_layers),
                    "batch": int(len(sp.lens)), "kv_bytes_per_step": step_bytes, "q_heads": sp.num_q_heads,
                    "bucket": args.bucket if args.bucket > len(sp.lens) else None,
+                   "early_inputs": not args.no_early_inputs,
                    "l2": "inputs larger than L2: %.2f GB of KV read per step" % (step_bytes / 1e9),
                    "parallelism": "dp%d (sequences sharded, no collective)" % world},
         "roofline": roofline,

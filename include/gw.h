@@ -175,8 +175,10 @@ gw_status gw_kv_append(const gw_kv_pool* pool, const void* k, const void* v, int
  *   workspace    device scratch of at least gw_attn_workspace_bytes(...),
  *                256-byte aligned; contents need no initialisation.
  * Errors: GW_ERR_INVALID_ARG, GW_ERR_WORKSPACE, GW_ERR_UNSUPPORTED
- * (num_q_heads / kv_heads not in {1,2,4,8}, or batch > 4096: the decode
- * kernel keeps the batch's split plan in shared memory), GW_ERR_CUDA.
+ * (num_q_heads / kv_heads not in {1,2,4,8}; batch > 4096, since the decode
+ * kernel keeps the batch's split plan in shared memory; max_q_rows > 1 on an
+ * e4m3 pool, since the prompt-row kernel reads bf16 pages only), GW_ERR_CUDA.
+ * Every error but GW_ERR_CUDA is returned before anything is launched.
  */
 gw_status gw_decode_attn_local(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,
                                int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,
@@ -268,6 +270,26 @@ gw_status gw_set_max_ctas(int32_t max_ctas);
  * lane's SMs and keep its kernels from starting.  Never an error.
  */
 gw_status gw_set_early_launch(int32_t on);
+
+/*
+ * gw_set_early_inputs - whether the calling thread's later decode-attention
+ * calls may read their index inputs before the previous kernel of their
+ * stream has finished (1) or only after it (0, the default).
+ *
+ * With programmatic dependent launch a decode kernel starts while its
+ * predecessor (typically this layer's gw_kv_append, or the previous layer's
+ * combine) is still running, and waits on chip before touching anything that
+ * predecessor may write.  With 1, the decode kernels compute their split plan
+ * from cu_q_rows and seq_lens and fetch their first units' block-table
+ * entries before that wait, which takes two dependent round trips off the
+ * call.  KV pages, q, the workspace, out and dev_status are still touched
+ * only after the wait.  The caller promises that the kernel just before each
+ * call in its stream does not write that call's cu_q_rows, seq_lens or
+ * block_table, as holds when they are uploaded for the whole step before its
+ * first layer.  Results do not depend on the setting.  Read when a call
+ * launches (for a CUDA graph: when it is captured).  Never an error.
+ */
+gw_status gw_set_early_inputs(int32_t on);
 
 /*
  * gw_bw_probe - a measurement aid, not part of the method: streams the first

@@ -189,10 +189,22 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     tc::alloc(&sm.tmem_base, 512);
     tc::relinquish();
   }
-  pdl_wait();
-  pdl_trigger();
-  plan_in_smem(a, sm.ub, sm.ub + kMaxBatch + 1, [](int L) { return global_chunks(L); });
+  // With early inputs the plan and the producer's first page numbers are
+  // read before the wait on the previous kernel (gw_set_early_inputs); every
+  // role then waits before its first access to pages, q or the workspace.
+  const bool early = a.early_inputs != 0;
+  if (!early) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  plan_in_smem(a, sm.ub, sm.ub + kMaxBatch + 1, [](int L) { return global_chunks(L); }, !early);
   const int total_units = sm.ub[a.batch];
+  auto wait_prev = [&]() {
+    if (early) {
+      pdl_wait();
+      pdl_trigger();
+    }
+  };
   fence_proxy_async_smem();
   tc::fence_before();
   __syncthreads();
@@ -200,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
   const uint32_t tmem = sm.tmem_base;
   // TMEM columns: S^T buffers at 0 and 32; O^T buffers at 64 and 192 (4 blocks of 32).
   if (total_units > a.max_units) {  // uniform
+    wait_prev();
     if (blockIdx.x == 0 && tid == 0) set_status(st, GW_DEV_WORKSPACE);
   } else if (warp == 4) {
     // ------------------------------------------------------------- producer
@@ -226,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     if (!end) unit_info();
     bool in_unit = false;
     int32_t pg = end ? -1 : fetch_page(in_unit);
+    wait_prev();
     for (uint32_t n = 0;; ++n) {
       const int b = n % NB;
       const uint32_t k = n / NB;  // use of buffer b
@@ -274,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     }
   } else if (warp == 5) {
     // ----------------------------------------------------------- QK^T issue
+    wait_prev();
     // The whole warp runs this loop with warp-uniform values; elect.sync
     // picks the issuing lane inside mma_bf16_warp / commit_warp.
     const uint32_t id_qk = tc::idesc_bf16(64, HQ, false, false);
@@ -307,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     }
   } else if (warp == 7) {
     // ------------------------------------------------------------ P.V issue
+    wait_prev();
     const uint32_t id_pv = tc::idesc_bf16(128, NP, true, true);
     const uint64_t pv_a0 = tc::smem_desc(smem_u32(sm.tiles[0]), T::kBlk * 128, 128);
     const uint64_t pv_b0 = tc::smem_desc(smem_u32(sm.p[0]), (NP / 8) * 128, 128);
@@ -338,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     }
   } else if (warp == 6) {
     // -------------------------------------------------------------- q loader
+    wait_prev();
     // Unit k's rows overwrite Q once the last QK^T of unit k - 1 has
     // completed (q_free); by then they are usually in L2 already.
     int k = 0;
@@ -362,6 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     }
   } else if (warp < 4) {
     // ------------------------------------------------- softmax + epilogue
+    wait_prev();
+    if (early) publish_plan(a, sm.ub, tid, 128);
     const bool active = lane < 16;
     const int t = 16 * warp + lane;  // token of the tile (active lanes)
     const int j = warp;              // page of the tile

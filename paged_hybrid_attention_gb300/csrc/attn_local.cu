@@ -173,8 +173,9 @@ __device__ __forceinline__ int active_warps(int units, int wmax) {
 }
 
 template <int kChunk>
-__device__ __forceinline__ void local_plan(const LocalArgs& a, int32_t* ub) {
-  plan_in_smem(a, ub, ub + kMaxBatch + 1, [&](int L) { return a.kv_heads * local_chunks(L, a.window, kChunk); });
+__device__ __forceinline__ void local_plan(const LocalArgs& a, int32_t* ub, bool publish) {
+  plan_in_smem(a, ub, ub + kMaxBatch + 1, [&](int L) { return a.kv_heads * local_chunks(L, a.window, kChunk); },
+               publish);
 }
 
 template <int DT, int G>
@@ -192,11 +193,17 @@ __global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kerne
     fence_mbar_init();
   }
   int32_t* ub = reinterpret_cast<int32_t*>(smem_raw + sizeof(typename T::Smem) * kWarps);
-  pdl_wait();
-  pdl_trigger();
-  local_plan<T::kChunk>(a, ub);
+  // With early inputs the plan and the first units' page numbers are read
+  // before the wait on the previous kernel (gw_set_early_inputs).
+  const bool early = a.early_inputs != 0;
+  if (!early) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  local_plan<T::kChunk>(a, ub, !early);
   const int total_units = ub[a.batch];
   if (total_units > a.max_units) {
+    if (early) pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.status, GW_DEV_WORKSPACE);
     return;
   }
@@ -265,6 +272,11 @@ __global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kerne
 
   f_done = !grab(0, pg_cur);
   if (!f_done) have_next = grab(1, pg_nxt);
+  if (early) {
+    pdl_wait();
+    pdl_trigger();
+    publish_plan(a, ub, threadIdx.x, n_active * 32);
+  }
   while (!f_done && issued - consumed < kStages) issue();
 
   using X = Mix<DT>;
@@ -451,11 +463,17 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     fence_mbar_init();
   }
   int32_t* ub = reinterpret_cast<int32_t*>(smem_raw + sizeof(TcWarpSmem) * kTcWarps);
-  pdl_wait();
-  pdl_trigger();
-  local_plan<T::kChunk>(a, ub);
+  // With early inputs the plan and the first units' page numbers are read
+  // before the wait on the previous kernel (gw_set_early_inputs).
+  const bool early = a.early_inputs != 0;
+  if (!early) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  local_plan<T::kChunk>(a, ub, !early);
   const int total_units = ub[a.batch];
   if (total_units > a.max_units) {
+    if (early) pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.status, GW_DEV_WORKSPACE);
     return;
   }
@@ -522,6 +540,11 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
 
   f_done = !grab(0, pg_cur);
   if (!f_done) have_next = grab(1, pg_nxt);
+  if (early) {
+    pdl_wait();
+    pdl_trigger();
+    publish_plan(a, ub, threadIdx.x, n_active * 32);
+  }
   while (!f_done && issued - consumed < kTcStages) issue();
 
   const int hq = lane >> 2;        // S row (q head of the group) this lane holds

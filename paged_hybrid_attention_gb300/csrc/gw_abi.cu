@@ -81,8 +81,10 @@ gw_status set_error(gw_status code, const char* fn, const char* fmt, ...) {
 
 thread_local int g_max_ctas = 0;
 thread_local bool g_early_launch = true;
+thread_local bool g_early_inputs = false;
 
 bool early_launch() { return g_early_launch; }
+bool early_inputs() { return g_early_inputs; }
 
 int grid_ctas() {
   const int n = num_sms();
@@ -211,6 +213,9 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(GW_ERR_INVALID_ARG, fn, "scale must be finite and > 0");
   if (max_pages_per_seq < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_pages_per_seq must be >= 1");
   if (max_q_rows < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_q_rows must be >= 1");
+  if (local && pool->dtype == GW_KV_E4M3 && max_q_rows > 1)
+    return fail(GW_ERR_UNSUPPORTED, fn, "prompt rows (max_q_rows %d > 1) on an e4m3 pool: the prompt-row kernel "
+                "reads bf16 pages only", max_q_rows);
   if (!q || !out || !aligned(q, 16) || !aligned(out, 16)) return fail(GW_ERR_INVALID_ARG, fn, "q/out NULL or not 16-byte aligned");
   if (!cu_q_rows || !seq_lens || !block_table || !aligned(cu_q_rows, 4) || !aligned(seq_lens, 4) ||
       !aligned(block_table, 4))
@@ -245,6 +250,7 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
   a.prompt_base = reinterpret_cast<int32_t*>(ws + w.prompt_base);
   a.max_units = w.max_units;
   a.status = dev_status;
+  a.early_inputs = g_early_inputs ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (local) {
@@ -284,6 +290,12 @@ gw_status gw_set_max_ctas(int32_t max_ctas) {
 gw_status gw_set_early_launch(int32_t on) {
   g_err[0] = 0;
   g_early_launch = on != 0;
+  return GW_OK;
+}
+
+gw_status gw_set_early_inputs(int32_t on) {
+  g_err[0] = 0;
+  g_early_inputs = on != 0;
   return GW_OK;
 }
 

@@ -93,6 +93,7 @@ struct LocalArgs {
   int64_t max_units;
   int32_t* status;
   int32_t* prompt_base;  // tile offsets of the prompt-row kernels
+  int32_t early_inputs;  // gw_set_early_inputs: plan before the wait on the previous kernel
 };
 
 struct AppendArgs {
@@ -116,6 +117,9 @@ int grid_ctas();
 // Whether this thread's launches may start before their predecessor in the
 // stream has finished (programmatic dependent launch); gw_set_early_launch.
 bool early_launch();
+// Whether the calling thread's calls may read their index inputs before the
+// previous kernel of their stream has finished; gw_set_early_inputs.
+bool early_inputs();
 
 // Records `fmt` (printf-style) as the calling thread's gw_last_error message,
 // prefixed by `fn`, and returns `code`.

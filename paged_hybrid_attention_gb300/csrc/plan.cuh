@@ -10,14 +10,21 @@
 
 namespace gw {
 
+__device__ __forceinline__ bool plan_len_ok(const LocalArgs& a, int L) {
+  return L >= 1 && static_cast<int64_t>(L) <= static_cast<int64_t>(a.max_pages) * kPage;
+}
+
 // ub[s] = units of the decode-row sequences before s (ub[batch] = total),
 // with units_of(L) the units of one decode row of length L.  Rows of invalid
-// length (L < 1 or beyond the block table) get no units and raise
-// GW_DEV_LEN_RANGE.  Must be called by every thread of the block; scratch
-// holds 32 ints.  CTA 0 also stores the plan to the workspace for the combine
-// kernel.
+// length (L < 1 or beyond the block table) get no units.  Must be called by
+// every thread of the block; scratch holds 32 ints.  With `publish`, CTA 0
+// also stores the plan to the workspace for the combine kernel and raises
+// GW_DEV_LEN_RANGE for invalid rows; without it (a plan made before the wait
+// on the previous kernel) nothing is written to global memory, and
+// publish_plan does both once the wait is over.
 template <class UnitsOf>
-__device__ void plan_in_smem(const LocalArgs& a, int32_t* ub, int32_t* scratch, UnitsOf units_of) {
+__device__ void plan_in_smem(const LocalArgs& a, int32_t* ub, int32_t* scratch, UnitsOf units_of,
+                             bool publish = true) {
   const int nt = blockDim.x, t = threadIdx.x;
   const int per = (a.batch + nt - 1) / nt;
   const int s0 = min(a.batch, t * per), s1 = min(a.batch, s0 + per);
@@ -27,9 +34,9 @@ __device__ void plan_in_smem(const LocalArgs& a, int32_t* ub, int32_t* scratch, 
     const int L = a.seq_lens[s];
     int units = 0;
     if (n == 1) {
-      if (L >= 1 && static_cast<int64_t>(L) <= static_cast<int64_t>(a.max_pages) * kPage)
+      if (plan_len_ok(a, L))
         units = units_of(L);
-      else if (blockIdx.x == 0)
+      else if (blockIdx.x == 0 && publish)
         set_status(a.status, GW_DEV_LEN_RANGE);
     }
     ub[s] = units;  // per-sequence count for now
@@ -63,8 +70,20 @@ __device__ void plan_in_smem(const LocalArgs& a, int32_t* ub, int32_t* scratch, 
   }
   if (t == nt - 1) ub[a.batch] = run;
   __syncthreads();
-  if (blockIdx.x == 0)
+  if (blockIdx.x == 0 && publish)
     for (int s = t; s <= a.batch; s += nt) a.unit_base[s] = ub[s];
+}
+
+// The global half of a plan made with publish = false, once the previous
+// kernel has finished: CTA 0's threads t of nt store the plan and raise
+// GW_DEV_LEN_RANGE for invalid decode rows.
+__device__ __forceinline__ void publish_plan(const LocalArgs& a, const int32_t* ub, int t, int nt) {
+  if (blockIdx.x != 0) return;
+  for (int s = t; s <= a.batch; s += nt) {
+    a.unit_base[s] = ub[s];
+    if (s < a.batch && a.cu_q_rows[s + 1] - a.cu_q_rows[s] == 1 && !plan_len_ok(a, a.seq_lens[s]))
+      set_status(a.status, GW_DEV_LEN_RANGE);
+  }
 }
 
 // The sequence that owns unit u (0 <= u < ub[batch]): the largest s with

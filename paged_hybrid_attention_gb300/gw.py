@@ -29,7 +29,8 @@ LAYOUTS = {"local": LAYOUT_LOCAL, "folded": LAYOUT_GLOBAL_FOLDED, "full": LAYOUT
 DTYPES = {"bf16": KV_BF16, "e4m3": KV_E4M3}
 EXPORTS = ["gw_pool_page_bytes", "gw_kv_append", "gw_decode_attn_local", "gw_decode_attn_global",
            "gw_attn_workspace_bytes", "gw_last_error", "gw_version", "gw_decode_attn_local_noalloc",
-           "gw_noalloc_scratch_bytes", "gw_bw_probe", "gw_set_max_ctas", "gw_set_early_launch"]
+           "gw_noalloc_scratch_bytes", "gw_bw_probe", "gw_set_max_ctas", "gw_set_early_launch",
+           "gw_set_early_inputs"]
 
 
 class GwError(RuntimeError):
@@ -69,6 +70,8 @@ _lib.gw_set_max_ctas.argtypes = [_i32]
 _lib.gw_set_max_ctas.restype = _i32
 _lib.gw_set_early_launch.argtypes = [_i32]
 _lib.gw_set_early_launch.restype = _i32
+_lib.gw_set_early_inputs.argtypes = [_i32]
+_lib.gw_set_early_inputs.restype = _i32
 _lib.gw_last_error.argtypes = []
 _lib.gw_last_error.restype = ctypes.c_char_p
 _lib.gw_version.argtypes = []
@@ -204,6 +207,13 @@ def set_early_launch(on):
     """gw_set_early_launch: allow (True) or forbid programmatic early launch
     for this thread's later calls."""
     _check(_lib.gw_set_early_launch(1 if on else 0))
+
+
+def set_early_inputs(on):
+    """gw_set_early_inputs: let this thread's later decode calls read cu_q_rows,
+    seq_lens and block_table before the previous kernel of their stream ends
+    (the caller guarantees that kernel does not write them)."""
+    _check(_lib.gw_set_early_inputs(1 if on else 0))
 
 
 def bw_probe(buf, dev_status=None, stream=None):

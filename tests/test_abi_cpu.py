@@ -86,6 +86,10 @@ def test_attention_host_validation():
     assert _local_call(d, batch=0) == gw.GW_OK                        # empty batch: nothing to do
     assert _local_call(d, batch=4097) == gw.GW_ERR_UNSUPPORTED        # split plan lives in shared memory
     assert "4096" in gw.last_error()
+    e8 = _desc(dtype=gw.KV_E4M3)
+    assert _local_call(e8, mq=1) != gw.GW_ERR_UNSUPPORTED
+    assert _local_call(e8, mq=2) == gw.GW_ERR_UNSUPPORTED             # prompt rows read bf16 pages only
+    assert "e4m3" in gw.last_error()
     g = _desc(gw.LAYOUT_GLOBAL_FOLDED, kvh=1, hd=512, rd=128)
     assert _local_call(g) == gw.GW_ERR_INVALID_ARG                    # global pool on the local entry
     L = gw.lib()
@@ -138,3 +142,5 @@ def test_set_max_ctas_validation():
     assert L.gw_set_max_ctas(0) == gw.GW_OK
     assert L.gw_set_early_launch(0) == gw.GW_OK
     assert L.gw_set_early_launch(1) == gw.GW_OK
+    assert L.gw_set_early_inputs(1) == gw.GW_OK
+    assert L.gw_set_early_inputs(0) == gw.GW_OK
