@@ -282,12 +282,14 @@ gw_status gw_set_early_launch(int32_t on);
  * predecessor may write.  With 1, the decode kernels compute their split plan
  * from cu_q_rows and seq_lens and fetch their first units' block-table
  * entries before that wait, which takes two dependent round trips off the
- * call.  KV pages, q, the workspace, out and dev_status are still touched
- * only after the wait.  The caller promises that the kernel just before each
- * call in its stream does not write that call's cu_q_rows, seq_lens or
- * block_table, as holds when they are uploaded for the whole step before its
- * first layer.  Results do not depend on the setting.  Read when a call
- * launches (for a CUDA graph: when it is captured).  Never an error.
+ * call; gw_kv_append likewise reads slot, pos and the RoPE table rows they
+ * select before its wait.  KV pages, q, k, v, the workspace, out and
+ * dev_status are still touched only after the wait.  The caller promises
+ * that the kernel just before each call in its stream does not write that
+ * call's cu_q_rows, seq_lens, block_table, slot, pos or rope_cs, as holds
+ * when they are uploaded for the whole step before its first layer.  Results
+ * do not depend on the setting.  Read when a call launches (for a CUDA
+ * graph: when it is captured).  Never an error.
  */
 gw_status gw_set_early_inputs(int32_t on);
 

@@ -170,6 +170,7 @@ gw_status gw_kv_append(const gw_kv_pool* pool, const void* k, const void* v, int
   a.pos = pos;
   a.rope_cs = rope_cs;
   a.max_pos = max_pos;
+  a.early_inputs = g_early_inputs ? 1 : 0;
   a.status = dev_status;
   return cuda_status(launch_append(pool->layout, pool->dtype, a, static_cast<cudaStream_t>(stream)), fn);
 }

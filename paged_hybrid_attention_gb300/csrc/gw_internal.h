@@ -108,6 +108,7 @@ struct AppendArgs {
   const float* rope_cs;
   int32_t max_pos;
   int32_t* status;
+  int32_t early_inputs;  // gw_set_early_inputs: slot, pos and RoPE rows read before the wait
 };
 
 int num_sms();

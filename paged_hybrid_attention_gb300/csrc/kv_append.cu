@@ -43,17 +43,28 @@ __device__ __forceinline__ uint2 f32x8_to_e4m3(const float (&f)[8]) {
   return make_uint2(w[0], w[1]);
 }
 
-// Rotate 8 pairs (x0[i], x1[i]) with table entries cs[2i], cs[2i+1].
-__device__ __forceinline__ void rotate8(float (&x0)[8], float (&x1)[8], const float* cs) {
+// The (cos, sin) table entries of 8 rotation pairs: cs[2i], cs[2i+1].
+struct CosSin8 {
   float c[8], s[8];
+};
+
+__device__ __forceinline__ CosSin8 load_cs8(const float* cs) {
+  CosSin8 r;
 #pragma unroll
   for (int i = 0; i < 8; i += 2) {
     float4 t = *reinterpret_cast<const float4*>(cs + 2 * i);
-    c[i] = t.x;
-    s[i] = t.y;
-    c[i + 1] = t.z;
-    s[i + 1] = t.w;
+    r.c[i] = t.x;
+    r.s[i] = t.y;
+    r.c[i + 1] = t.z;
+    r.s[i + 1] = t.w;
   }
+  return r;
+}
+
+// Rotate 8 pairs (x0[i], x1[i]) by the angles of cs.
+__device__ __forceinline__ void rotate8(float (&x0)[8], float (&x1)[8], const CosSin8& cs) {
+  const float (&c)[8] = cs.c;
+  const float (&s)[8] = cs.s;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float r0 = __fsub_rn(__fmul_rn(x0[i], c[i]), __fmul_rn(x1[i], s[i]));
@@ -72,27 +83,40 @@ __device__ __forceinline__ void store8(uint8_t* base, int64_t elem, const float 
   }
 }
 
-__device__ __forceinline__ bool row_ok(const AppendArgs& a, int64_t row, int32_t& slot, int32_t& pos,
-                                       bool report) {
+// 0 if the row's slot and pos are in range, else the GW_DEV_* bit to report.
+__device__ __forceinline__ int32_t row_check(const AppendArgs& a, int64_t row, int32_t& slot, int32_t& pos) {
   slot = a.slot[row];
   pos = a.pos[row];
-  if (slot < 0 || static_cast<int64_t>(slot) >= a.num_pages * kPage) {
-    if (report) set_status(a.status, GW_DEV_SLOT_RANGE);
-    return false;
-  }
-  if (pos < 0 || pos >= a.max_pos) {
-    if (report) set_status(a.status, GW_DEV_POS_RANGE);
-    return false;
-  }
-  return true;
+  if (slot < 0 || static_cast<int64_t>(slot) >= a.num_pages * kPage) return GW_DEV_SLOT_RANGE;
+  if (pos < 0 || pos >= a.max_pos) return GW_DEV_POS_RANGE;
+  return 0;
 }
+
+// Programmatic dependent launch: slot, pos and the RoPE table are index
+// inputs, read before the wait on the previous kernel when the caller allows
+// it (gw_set_early_inputs); k, v, the pool and the status word only after.
+struct PdlGate {
+  bool waited;
+  __device__ explicit PdlGate(const AppendArgs& a) : waited(a.early_inputs == 0) {
+    if (waited) {
+      pdl_wait();
+      pdl_trigger();
+    }
+  }
+  __device__ void pass() {
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
+  }
+};
 
 // LOCAL: one work item = (row, kv head, j in [0,16)): pairs (8j+i, 128+8j+i)
 // of K, and V chunks 8j and 128+8j.
 template <int DT>
 __global__ void append_local_kernel(const AppendArgs a) {
-  pdl_wait();
-  pdl_trigger();
+  PdlGate gate(a);
   const int64_t total = static_cast<int64_t>(a.num_rows) * a.kv_heads * 16;
   for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
        w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -101,14 +125,20 @@ __global__ void append_local_kernel(const AppendArgs a) {
     const int g = static_cast<int>(rh % a.kv_heads);
     const int64_t row = rh / a.kv_heads;
     int32_t slot, pos;
-    if (!row_ok(a, row, slot, pos, j == 0 && g == 0)) continue;
+    const int32_t bad = row_check(a, row, slot, pos);
+    const CosSin8 cs = load_cs8(a.rope_cs + (static_cast<int64_t>(bad ? 0 : pos) * 128 + 8 * j) * 2);
+    gate.pass();
+    if (bad) {
+      if (j == 0 && g == 0) set_status(a.status, bad);
+      continue;
+    }
     const int64_t page = slot / kPage, off = slot % kPage;
     const uint16_t* krow = a.k + (row * a.kv_heads + g) * 256;
     const uint16_t* vrow = a.v + (row * a.kv_heads + g) * 256;
     float x0[8], x1[8];
     load_bf16x8(krow + 8 * j, x0);
     load_bf16x8(krow + 128 + 8 * j, x1);
-    rotate8(x0, x1, a.rope_cs + (static_cast<int64_t>(pos) * 128 + 8 * j) * 2);
+    rotate8(x0, x1, cs);
     const int64_t kbase = (((page * a.kv_heads + g) * 2 + 0) * kPage + off) * 256;
     const int64_t vbase = (((page * a.kv_heads + g) * 2 + 1) * kPage + off) * 256;
     store8<DT>(a.pool, kbase + 8 * j, x0);
@@ -144,8 +174,7 @@ __global__ void append_global_kernel(const AppendArgs a) {
   constexpr bool kFolded = LAYOUT == GW_LAYOUT_GLOBAL_FOLDED;
   constexpr int kRow = kFolded ? 640 : 1024;
   constexpr int kItems = kFolded ? 72 : 120;
-  pdl_wait();
-  pdl_trigger();
+  PdlGate gate(a);
   const int64_t total = static_cast<int64_t>(a.num_rows) * kItems;
   uint16_t* pool = reinterpret_cast<uint16_t*>(a.pool);
   for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
@@ -153,18 +182,26 @@ __global__ void append_global_kernel(const AppendArgs a) {
     const int it = static_cast<int>(w % kItems);
     const int64_t row = w / kItems;
     int32_t slot, pos;
-    if (!row_ok(a, row, slot, pos, it == 0)) continue;
+    const int32_t bad = row_check(a, row, slot, pos);
+    const int rot_item = kFolded ? it - 64 : it;  // rotation items
+    const bool rot = rot_item >= 0 && rot_item < 8;
+    CosSin8 cs{};
+    if (rot) cs = load_cs8(a.rope_cs + (static_cast<int64_t>(bad ? 0 : pos) * 64 + 8 * rot_item) * 2);
+    gate.pass();
+    if (bad) {
+      if (it == 0) set_status(a.status, bad);
+      continue;
+    }
     const int64_t page = slot / kPage;
     const int off = slot % kPage;
     const uint16_t* krow = a.k + row * 512;
     const uint16_t* vrow = a.v + row * 512;
-    const int rot_item = kFolded ? it - 64 : it;  // rotation items
-    if (rot_item >= 0 && rot_item < 8) {
+    if (rot) {
       const int t = rot_item;
       float x0[8], x1[8];
       load_bf16x8(krow + 8 * t, x0);
       load_bf16x8(krow + 64 + 8 * t, x1);
-      rotate8(x0, x1, a.rope_cs + (static_cast<int64_t>(pos) * 64 + 8 * t) * 2);
+      rotate8(x0, x1, cs);
       const int e0 = kFolded ? 512 + 8 * t : 8 * t;
       *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, e0)) = f32x8_to_bf16(x0);
       *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, e0 + 64)) = f32x8_to_bf16(x1);
