@@ -211,8 +211,9 @@ def set_early_launch(on):
 
 def set_early_inputs(on):
     """gw_set_early_inputs: let this thread's later decode calls read cu_q_rows,
-    seq_lens and block_table before the previous kernel of their stream ends
-    (the caller guarantees that kernel does not write them)."""
+    seq_lens and block_table, and its appends slot, pos and rope_cs, before
+    the previous kernel of their stream ends (the caller guarantees that
+    kernel does not write them)."""
     _check(_lib.gw_set_early_inputs(1 if on else 0))
 
 
