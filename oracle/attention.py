@@ -103,10 +103,11 @@ def local_rows(pool_u8, kv_heads, dtype, block_row, L, q64, window, scale):
 
 
 def global_rows(pool_u8, layout, block_row, L, q64, scale):
-    """Outputs for the rows of one sequence on a global layer (folded or full pool)."""
+    """Outputs for the rows of one sequence on a global layer (folded, full or
+    folded_e4m3 pool)."""
     n = q64.shape[0]
     rows = pages.read_global_rows(pool_u8, layout, block_row, np.arange(L))
-    K, V = rebuild_global_k(rows) if layout == "folded" else split_full_rows(rows)
+    K, V = split_full_rows(rows) if layout == "full" else rebuild_global_k(rows)
     out = np.empty_like(q64)
     for r in range(n):
         p = L - n + r

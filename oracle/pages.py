@@ -25,6 +25,11 @@ GLOBAL FOLDED, bf16, one token row is the 640-vector  V(512) || k_rot(128):
 GLOBAL FULL (control), bf16, one token row is the 1024-vector K(512) || V(512):
     [tb (2)][cb (128)][r (8)][c (8)]  -> 32768 B per page.
 
+GLOBAL FOLDED E4M3 (an opt-in the pages do not serve), e4m3, one token row is
+the folded 640-vector V(512) || k_rot(128), each element rounded once to e4m3:
+    [tb (2)][cb (40)][r (8)][c (16)]  with e = 16*cb + c
+    -> 10240 B per page; each 8 x 16 block is 128 contiguous bytes.
+
 Reading any element back is the inverse map; the reader below gathers the
 tokens of one sequence through its block table.
 """
@@ -66,6 +71,19 @@ def full_page_bytes():
     return PAGE * FULL_ROW * 2
 
 
+def folded_e4m3_page_bytes():
+    return PAGE * FOLDED_ROW
+
+
+def global_page_bytes(layout):
+    return {"folded": folded_page_bytes(), "full": full_page_bytes(),
+            "folded_e4m3": folded_e4m3_page_bytes()}[layout]
+
+
+def global_row_len(layout):
+    return FULL_ROW if layout == "full" else FOLDED_ROW
+
+
 # ------------------------------------------------------------ element offsets
 def local_offset(page, g, kind, o, d, kv_heads):
     """Element index of (page, kv head g, K/V kind, token offset o, dim d)."""
@@ -73,15 +91,17 @@ def local_offset(page, g, kind, o, d, kv_heads):
     return ((((page * kv_heads + g) * 2 + kind) * PAGE + o) * LOCAL_D + d)
 
 
-def tiled_offset(page, o, e, row_len):
-    """Element index in a GLOBAL page whose token rows have ``row_len`` elements."""
+def tiled_offset(page, o, e, row_len, blk=8):
+    """Element index in a GLOBAL page whose token rows have ``row_len``
+    elements, in blocks of 8 tokens x ``blk`` elements (16 bytes per block
+    row: blk = 8 for bf16, 16 for e4m3)."""
     page = np.asarray(page, dtype=np.int64)
     o = np.asarray(o, dtype=np.int64)
     e = np.asarray(e, dtype=np.int64)
     tb, r = o // 8, o % 8
-    cb, c = e // 8, e % 8
-    nblk = row_len // 8
-    return page * (PAGE * row_len) + ((tb * nblk + cb) * 8 + r) * 8 + c
+    cb, c = e // blk, e % blk
+    nblk = row_len // blk
+    return page * (PAGE * row_len) + ((tb * nblk + cb) * 8 + r) * blk + c
 
 
 # --------------------------------------------------------------- pool buffers
@@ -135,14 +155,29 @@ def full_rows(k_bits, v_bits, pos, table):
     return np.concatenate([K, np.asarray(v_bits, dtype=np.uint16)], axis=1)
 
 
+def folded_e4m3_rows(k_bits, v_bits, pos, table):
+    """Token rows V || k_rot as e4m3 codes [T, 640]: V rounded once from bf16,
+    the rotated slice rounded once from its float32 rotation (as the local
+    e4m3 pool rounds its rotated K)."""
+    k32 = bf16_bits_to_f32(np.asarray(k_bits)[:, :GLOBAL_ROT])
+    krot = f32_to_e4m3(rotate_half_f32(k32, table[np.asarray(pos)]))
+    return np.concatenate([bf16_bits_to_e4m3(v_bits), krot], axis=1)
+
+
 def write_global(pool_u8, layout, k_bits, v_bits, slot, pos, table):
-    """Append T global rows; layout is "folded" or "full"; k, v bf16 bits [T, 512]."""
-    rows = (folded_rows if layout == "folded" else full_rows)(k_bits, v_bits, pos, table)
+    """Append T global rows; layout is "folded", "full" or "folded_e4m3";
+    k, v bf16 bits [T, 512]."""
+    make = {"folded": folded_rows, "full": full_rows, "folded_e4m3": folded_e4m3_rows}[layout]
+    rows = make(k_bits, v_bits, pos, table)
     row_len = rows.shape[1]
     slot = np.asarray(slot, dtype=np.int64)
+    blk = 16 if layout == "folded_e4m3" else 8
     off = tiled_offset((slot // PAGE)[:, None], (slot % PAGE)[:, None],
-                       np.arange(row_len)[None, :], row_len)
-    pool_u8.view(np.uint16)[off] = rows
+                       np.arange(row_len)[None, :], row_len, blk)
+    if layout == "folded_e4m3":
+        pool_u8[off] = rows
+    else:
+        pool_u8.view(np.uint16)[off] = rows
     return rows.shape[0]
 
 
@@ -171,9 +206,12 @@ def read_local(pool_u8, kv_heads, dtype, block_row, positions):
 
 
 def read_global_rows(pool_u8, layout, block_row, positions):
-    """Stored token rows (float64) [n, 640] folded or [n, 1024] full."""
-    row_len = FOLDED_ROW if layout == "folded" else FULL_ROW
+    """Stored token rows (float64) [n, 640] folded (bf16 or e4m3) or [n, 1024] full."""
+    row_len = global_row_len(layout)
     slot = token_slots(block_row, positions)
+    blk = 16 if layout == "folded_e4m3" else 8
     off = tiled_offset((slot // PAGE)[:, None], (slot % PAGE)[:, None],
-                       np.arange(row_len)[None, :], row_len)
+                       np.arange(row_len)[None, :], row_len, blk)
+    if layout == "folded_e4m3":
+        return e4m3_to_f64(pool_u8[off])
     return bf16_bits_to_f64(pool_u8.view(np.uint16)[off])

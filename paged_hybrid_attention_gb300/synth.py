@@ -46,7 +46,7 @@ PAGE = 16
 class Family:
     kind: str            # "local" or "global"
     dtype: str           # "bf16" or "e4m3"
-    layout: str          # "local", "folded" or "full"
+    layout: str          # "local", "folded", "full" or "folded_e4m3"
     kv_heads: int
     head_dim: int
     rot_dim: int

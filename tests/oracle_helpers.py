@@ -13,7 +13,7 @@ def family_table(fam, max_pos):
 def page_bytes(fam):
     if fam.layout == "local":
         return pages.local_page_bytes(fam.kv_heads, fam.dtype)
-    return pages.folded_page_bytes() if fam.layout == "folded" else pages.full_page_bytes()
+    return pages.global_page_bytes(fam.layout)
 
 
 def build_pool(layer, table, seqs=None, part="all", pool=None):

@@ -231,3 +231,61 @@ def test_e4m3_pool_reads_back_rounded_values():
     exact = formats.bf16_bits_to_f64(v)
     big = np.abs(exact) >= 2.0 ** -6
     assert np.all(np.abs(V - exact)[big] <= np.abs(exact)[big] * 2.0 ** -4 + 1e-30)
+
+
+@pytest.mark.parametrize("fam_key,layout", [("global", "folded"), ("global_full", "full")])
+def test_global_prompt_rows_match_brute_force(fam_key, layout):
+    """Global prompt rows (n > 1): row r of a segment of n rows sits at
+    p = L - n + r and attends causally to keys [0, p], over a K rebuilt from
+    the folded row (k_rot || V[128:]) or read from the full pool.  Checked
+    against plain-Python loops over the unpaged tokens, and against the
+    wrong reading that lets a row see one key past its own position."""
+    fam = synth.Family("global", "bf16", layout, 1, 512, 128, 1e6, 0)
+    L, n = 50, 20
+    sp = synth.custom("gp", 21, 4, [L], [n], {fam_key: fam})
+    layer = synth.Layer(sp, fam_key)
+    table = H.family_table(fam, L + 1)
+    pool = H.build_pool(layer, table)
+    got = H.oracle_rows(layer, pool, 0)
+    pos, k, v = layer.kv(0)
+    assert np.array_equal(pos, np.arange(L))
+    krot = formats.f32_to_bf16_bits(rope.rotate_half_f32(formats.bf16_bits_to_f32(k[:, :128]), table[pos]))
+    K = formats.bf16_bits_to_f64(np.concatenate([krot, k[:, 128:]], axis=1))
+    V = formats.bf16_bits_to_f64(v)
+    q = H.q64(layer, 0)
+    scale = 1.0 / math.sqrt(512)
+    for r in [0, 1, 9, n - 1]:
+        p = L - n + r
+        for h in range(sp.num_q_heads):
+            want = _brute(list(q[r, h]), [list(K[j]) for j in range(p + 1)], [list(V[j]) for j in range(p + 1)],
+                          scale)
+            assert np.max(np.abs(np.array(want) - got[r, h])) < 1e-12, (r, h)
+        if p + 1 < L:
+            wrong = _brute(list(q[r, 0]), [list(K[j]) for j in range(p + 2)], [list(V[j]) for j in range(p + 2)],
+                           scale)
+            assert np.max(np.abs(np.array(wrong) - got[r, 0])) > 1e-6
+
+
+def test_folded_e4m3_pool_attention_matches_brute_force():
+    """Global decode rows over the opt-in e4m3 folded pool: plain-Python
+    attention over K = e4m3(k_rot) || e4m3(V)[128:] and V = e4m3(V), built
+    directly from the unpaged tokens (each element rounded once: V from its
+    bf16 value, k_rot from its float32 rotation)."""
+    fam = synth.Family("global", "e4m3", "folded_e4m3", 1, 512, 128, 1e6, 0, sigma=0.5)
+    sp = synth.custom("g8", 23, 8, [37, 100], [1, 1], {"global": fam})
+    layer = synth.Layer(sp, "global")
+    table = H.family_table(fam, 101)
+    pool = H.build_pool(layer, table)
+    for s in range(layer.B):
+        L = int(sp.lens[s])
+        pos, k, v = layer.kv(s)
+        kr = formats.e4m3_to_f64(formats.f32_to_e4m3(rope.rotate_half_f32(
+            formats.bf16_bits_to_f32(k[:, :128]), table[pos])))
+        V = formats.e4m3_to_f64(formats.bf16_bits_to_e4m3(v))
+        K = np.concatenate([kr, V[:, 128:]], axis=1)
+        got = H.oracle_rows(layer, pool, s)
+        q = H.q64(layer, s)
+        for h in range(0, sp.num_q_heads, 3):
+            want = _brute(list(q[0, h]), [list(K[j]) for j in range(L)], [list(V[j]) for j in range(L)],
+                          1.0 / math.sqrt(512))
+            assert np.max(np.abs(np.array(want) - got[0, h])) < 1e-12

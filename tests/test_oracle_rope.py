@@ -8,6 +8,7 @@ and the proportional-RoPE denominator of the global layers.
 """
 
 import math
+from fractions import Fraction
 
 import numpy as np
 
@@ -78,12 +79,48 @@ def test_norm_and_relative_position():
     assert abs(d1 - d2) < 1e-3 * (1 + abs(d1))
 
 
-def test_rotation_op_order_is_binary32_without_fma():
-    # a case where a fused multiply-add would round differently
-    x = np.array([[1.0 + 2.0 ** -20, 3.0]], np.float32)
-    cs = np.array([[[1.0 - 2.0 ** -23, 2.0 ** -22 + 2.0 ** -40]]], np.float32)
-    r = rope.rotate_half_f32(x, cs)
-    c, s = cs[0, 0, 0], cs[0, 0, 1]
-    want0 = np.float32(np.float32(x[0, 0] * c) - np.float32(x[0, 1] * s))
-    want1 = np.float32(np.float32(x[0, 1] * c) + np.float32(x[0, 0] * s))
-    assert r[0, 0] == want0 and r[0, 1] == want1
+def _rne32(r):
+    """The binary32 value nearest the rational r (ties to even mantissa),
+    from the format's definition: 24 significant bits, normal range only."""
+    if r == 0:
+        return Fraction(0)
+    sign = -1 if r < 0 else 1
+    a = abs(r)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    assert -126 <= e <= 127
+    ulp = Fraction(2) ** (e - 23)
+    qv = a / ulp
+    n = qv.numerator // qv.denominator
+    rem = qv - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return sign * n * ulp
+
+
+def test_rotation_op_order_against_exact_arithmetic():
+    """Each of the four products and the sum/difference is rounded once to
+    binary32, in the stated order, with no fused multiply-add.  The expected
+    values come from exact rational arithmetic and a rounding written from
+    the binary32 definition; the inputs include cases where a fused
+    multiply-add (one rounding of x0*c - fl(x1*s)) would give other bits."""
+    g = np.random.Generator(np.random.PCG64(23))
+    x = g.normal(size=(4000, 2)).astype(np.float32)
+    ang = g.uniform(0, 2 * np.pi, 4000)
+    cs = np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
+    got = rope.rotate_half_f32(x, cs[:, None, :])
+    fused_differs = 0
+    for t in range(len(x)):
+        x0, x1 = Fraction(float(x[t, 0])), Fraction(float(x[t, 1]))
+        c, s = Fraction(float(cs[t, 0])), Fraction(float(cs[t, 1]))
+        if min(abs(x0), abs(x1), abs(c), abs(s)) < Fraction(1, 2 ** 40):
+            continue
+        p1, p2 = _rne32(x0 * c), _rne32(x1 * s)
+        want0 = _rne32(p1 - p2)
+        want1 = _rne32(_rne32(x1 * c) + _rne32(x0 * s))
+        if want0 == 0 or want1 == 0:
+            continue
+        assert Fraction(float(got[t, 0])) == want0 and Fraction(float(got[t, 1])) == want1, t
+        fused_differs += _rne32(x0 * c - p2) != want0
+    assert fused_differs > 0        # the order is observable on these inputs
