@@ -149,7 +149,7 @@ class GpuLayer:
         self.layer, self.fam = layer, fam
         self.pool = gw.KVPool(fam.layout, fam.dtype, layer.num_pages, fam.kv_heads, device=dev)
         max_pos = int(np.max(sp.lens)) + 1
-        self.table = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, max_pos).to(dev)
+        self.table = gw.rope_cs(fam.theta, fam.rot_dim, fam.head_dim, max_pos, device=dev)
         sig = fam.sigma
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         # history: every token the step reads that was cached before it

@@ -1,4 +1,5 @@
 // gw_bw_probe: the read bandwidth the decode kernels' copy pipeline can reach.
+// gw_wait_selftest: the bounded-wait path of the kernels, made to run out.
 //
 // Not part of the method: a measurement aid for the roofline.  It streams a
 // buffer through exactly the pipeline shape of the local decode kernel - one
@@ -64,7 +65,39 @@ __global__ void __launch_bounds__(kProbeWarps * 32, 1) bw_probe_kernel(const uin
   if (acc == 0x7FC00001u && status) atomicOr(status, 0);
 }
 
+// gw_wait_selftest: one warp, one mbarrier of arrival count 1.  Phase 0 is
+// completed by an arrival, then waited on (must succeed); phase 1 is never
+// arrived on, so its wait must give up after limit_ns, raise GW_DEV_TIMEOUT
+// and return.  result = {phase-0 wait succeeded, phase-1 wait gave up,
+// microseconds spent in the phase-1 wait}.
+__global__ void wait_selftest_kernel(int32_t* status, int32_t* result, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_arrive(&bar);
+  __syncwarp();
+  const bool ok0 = __all_sync(0xffffffffu, mbar_wait(&bar, 0, status, limit_ns));
+  const uint64_t t0 = global_ns();
+  const bool ok1 = __all_sync(0xffffffffu, mbar_wait(&bar, 1, status, limit_ns));
+  const uint64_t dt = global_ns() - t0;
+  if (threadIdx.x == 0) {
+    result[0] = ok0 ? 1 : 0;
+    result[1] = ok1 ? 0 : 1;
+    result[2] = static_cast<int32_t>(dt / 1000 < 0x7fffffffull ? dt / 1000 : 0x7fffffffull);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(int32_t* status, int32_t* result, int64_t limit_ns, cudaStream_t st) {
+  return launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0, st, status, result,
+                    static_cast<uint64_t>(limit_ns));
+}
 
 cudaError_t launch_bw_probe(const void* buf, int64_t chunks, int32_t* status, cudaStream_t st) {
   const size_t smem = sizeof(ProbeWarp) * kProbeWarps;

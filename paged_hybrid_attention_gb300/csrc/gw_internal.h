@@ -122,6 +122,13 @@ bool early_launch();
 // previous kernel of their stream has finished; gw_set_early_inputs.
 bool early_inputs();
 
+// Every host-side check of gw_decode_attn_local, workspace size included,
+// with errors reported under the name `fn`; launches nothing.
+gw_status validate_local_call(const char* fn, const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,
+                              int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,
+                              const int32_t* block_table, int32_t max_pages_per_seq, int32_t max_q_rows,
+                              int32_t window, float scale, size_t workspace_bytes, int32_t* dev_status);
+
 // Records `fmt` (printf-style) as the calling thread's gw_last_error message,
 // prefixed by `fn`, and returns `code`.
 gw_status set_error(gw_status code, const char* fn, const char* fmt, ...);
@@ -134,7 +141,10 @@ cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim,
                            cudaStream_t st);
 
 cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream_t st);
+// (cos, sin) table of gw_rope_cs: float32 [max_pos][rot_dim / 2][2].
+cudaError_t launch_rope_cs(float* out, double theta, int rot_dim, int head_dim, int max_pos, cudaStream_t st);
 cudaError_t launch_bw_probe(const void* buf, int64_t chunks, int32_t* status, cudaStream_t st);
+cudaError_t launch_wait_selftest(int32_t* status, int32_t* result, int64_t limit_ns, cudaStream_t st);
 // TMA descriptor of a bf16 LOCAL pool (rows of 256 elements in 4 chunks of 64;
 // row = ((page * kv_heads + head) * 2 + {K, V}) * 16 + token), box {64, 1, 16},
 // 128-byte swizzle.

@@ -1,9 +1,9 @@
 // Local decode attention for callers that cannot allocate device memory.
 //
 // Some callers of this library cannot call cudaMalloc at the point where they
-// run attention: code replayed inside an already-captured CUDA graph whose
-// memory plan is frozen, allocator-less embedding runtimes, or hosts that
-// forbid device allocation after start-up.  gw_decode_attn_local needs a
+// run attention: embedding runtimes that have no device allocator of their
+// own, and hosts that forbid device allocation once serving has started (a
+// fixed memory budget decided at start-up).  gw_decode_attn_local needs a
 // caller-supplied workspace for its split-KV partials; this entry point runs
 // the same computation with that workspace carved from a fixed, file-scope
 // device array instead, so the call itself allocates nothing.
@@ -13,6 +13,8 @@
 // requirement (gw_attn_workspace_bytes) exceeds it is rejected.
 #include <cstdio>
 #include <mutex>
+
+#include <cuda.h>
 
 #include "gw_internal.h"
 
@@ -25,27 +27,54 @@ constexpr size_t kStaticScratchBytes = static_cast<size_t>(32) << 20;
 // address: the address is obtained with cudaGetSymbolAddress below.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 
-// Device address of the scratch on the current device, resolved once per
-// device (with that device current) and cached.
+CtxGetCurrentFn resolve_ctx_get_current() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<CtxGetCurrentFn>(fn);
+}
+
+// Cached address of the scratch per device, tagged with the context it was
+// resolved in: after a device reset the module is loaded again, possibly at
+// another address, in a new context, and the address is looked up again.
+constexpr int kMaxDevices = 64;
+struct Cached {
+  CUcontext ctx;
+  void* addr;
+};
+std::mutex g_mu;
+Cached g_scratch[kMaxDevices] = {};
+
+// Device address of the scratch on the current device (with that device
+// current).
 gw_status scratch_for_current_device(const char* fn, void** out) {
+  static const CtxGetCurrentFn ctx_get_current = resolve_ctx_get_current();
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return gw::set_error(GW_ERR_CUDA, fn, "cudaGetDevice failed: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return gw::set_error(GW_ERR_UNSUPPORTED, fn, "device ordinal %d >= %d", dev, kMaxDevices);
+  if (!ctx_get_current) return gw::set_error(GW_ERR_CUDA, fn, "cuCtxGetCurrent is not available");
+  // Before the runtime's first call on this device no context may be current
+  // (ctx stays NULL); cudaGetSymbolAddress then initialises the device's
+  // primary context, which is read again afterwards.
+  CUcontext ctx = nullptr;
+  if (ctx_get_current(&ctx) != CUDA_SUCCESS) ctx = nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
+  if (!ctx || !g_scratch[dev].addr || g_scratch[dev].ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || !p)
       return gw::set_error(GW_ERR_CUDA, fn, "cudaGetSymbolAddress of the static scratch failed: %s",
                            cudaGetErrorString(e));
-    g_scratch_addr[dev] = p;
+    if (ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx)
+      return gw::set_error(GW_ERR_CUDA, fn, "cannot read the current CUDA context");
+    g_scratch[dev] = Cached{ctx, p};
   }
-  *out = g_scratch_addr[dev];
+  *out = g_scratch[dev].addr;
   return GW_OK;
 }
 
@@ -57,17 +86,15 @@ extern "C" gw_status gw_decode_attn_local_noalloc(const gw_kv_pool* pool, const 
                                                   int32_t max_pages_per_seq, int32_t max_q_rows, int32_t window,
                                                   float scale, int32_t* dev_status, void* stream) {
   const char* fn = "gw_decode_attn_local_noalloc";
-  if (batch > 0 && max_pages_per_seq > 0) {
-    const int64_t max_len64 = static_cast<int64_t>(max_pages_per_seq) * 16;
-    const int32_t max_len = max_len64 > 0x7fffffff ? 0x7fffffff : static_cast<int32_t>(max_len64);
-    const size_t need = gw_attn_workspace_bytes(pool, num_q_heads, batch, max_len, max_q_rows, window);
-    if (need > kStaticScratchBytes)
-      return gw::set_error(GW_ERR_WORKSPACE, fn,
-                           "this call needs %zu bytes of split-KV scratch; the static scratch holds %zu", need,
-                           kStaticScratchBytes);
-  }
+  // The same checks, in the same order, as gw_decode_attn_local, with the
+  // static scratch's size as the workspace size: an invalid call gets the
+  // same status as there, and a call needing more scratch GW_ERR_WORKSPACE.
+  gw_status s = gw::validate_local_call(fn, pool, q, out, num_q_heads, batch, cu_q_rows, seq_lens, block_table,
+                                        max_pages_per_seq, max_q_rows, window, scale, kStaticScratchBytes,
+                                        dev_status);
+  if (s != GW_OK || batch == 0) return s;
   void* scratch = nullptr;
-  gw_status s = scratch_for_current_device(fn, &scratch);
+  s = scratch_for_current_device(fn, &scratch);
   if (s != GW_OK) return s;
   s = gw_decode_attn_local(pool, q, out, num_q_heads, batch, cu_q_rows, seq_lens, block_table, max_pages_per_seq,
                            max_q_rows, window, scale, scratch, kStaticScratchBytes, dev_status, stream);

@@ -3,6 +3,7 @@
 import numpy as np
 import torch
 
+from oracle import rope
 from paged_hybrid_attention_gb300 import gw
 
 
@@ -14,8 +15,14 @@ def i32(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
 
 
+def oracle_table(theta, rot_dim, head_dim, max_pos):
+    """The oracle's own RoPE (cos, sin) table as a CPU float32 tensor.  Parity
+    tests hand these bytes to both gw_kv_append and the oracle's page writer."""
+    return torch.from_numpy(rope.rope_table(theta, rot_dim, head_dim, max_pos))
+
+
 def table_for(fam, max_pos):
-    return gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, max_pos).cuda()
+    return oracle_table(fam.theta, fam.rot_dim, fam.head_dim, max_pos).cuda()
 
 
 def new_pool(layer, fill=0):
@@ -62,3 +69,29 @@ def errors(got, want):
 
 
 MAX_ABS, REL_L2 = 1e-2, 5e-3
+
+
+def assert_oracle_rows(layer, got_rows, s, ref_pool, rows=None):
+    """The GPU rows of sequence s (float64 [n, HQ, D], in row order) against
+    the oracle on ref_pool, within the attention tolerance; `rows` restricts
+    the check to a sample of row indices."""
+    from tests import oracle_helpers as H
+    want = H.oracle_rows(layer, ref_pool, s)
+    if rows is not None:
+        got_rows, want = got_rows[rows], want[rows]
+    mx, rl = errors(got_rows, want)
+    assert mx <= MAX_ABS and rl <= REL_L2, (s, mx, rl)
+
+
+def check_layer_vs_oracle(layer, out, ref_pool, max_rows=8):
+    """Every sequence's rows of `out` (layer.cu_rows() order) against the
+    float64 oracle; prompt segments longer than max_rows are sampled at
+    max_rows evenly spaced rows, first and last included."""
+    got = to_f64(out)
+    cu = layer.cu_rows()
+    for s in range(layer.B):
+        n = int(cu[s + 1] - cu[s])
+        if n == 0:
+            continue
+        rows = None if n <= max_rows else np.unique(np.linspace(0, n - 1, max_rows).astype(int))
+        assert_oracle_rows(layer, got[cu[s]:cu[s + 1]], s, ref_pool, rows)

@@ -8,7 +8,6 @@ import re
 import numpy as np
 import pytest
 
-from oracle import rope
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -110,19 +109,17 @@ def test_workspace_size_grows_with_batch_and_length():
         L.gw_attn_workspace_bytes(ctypes.byref(g), 32, 8, 8192, 1, 0)
 
 
-@pytest.mark.parametrize("theta,R,D", [(1e4, 256, 256), (1e6, 128, 512), (1e4, 128, 512)])
-def test_rope_table_matches_oracle(theta, R, D):
-    """The library's table builder (torch float64) and the oracle's (NumPy
-    float64) agree to one float32 ulp (1e-10 absolute near zero, the float64 ulp of angles up to 1.4e5).  They are not always bit-identical: an
-    ulp of difference between two float64 pow/cos implementations moves the
-    float32 rounding of values that sit near a rounding boundary.  Parity
-    tests therefore hand both sides the same table bytes (the table is an
-    input of gw_kv_append)."""
-    mine = gw.rope_table(theta, R, D, 140000).numpy()
-    ref = rope.rope_table(theta, R, D, 140000)
-    tol = np.maximum(np.spacing(np.abs(ref)).astype(np.float64), 1e-10)
-    assert np.all(np.abs(mine.astype(np.float64) - ref) <= tol)
-    assert np.count_nonzero(mine.view(np.uint32) != ref.view(np.uint32)) < 1e-4 * ref.size
+def test_rope_cs_host_validation():
+    L = gw.lib()
+    f = _fake()
+    assert L.gw_rope_cs(None, 1e4, 256, 256, 10, None) == gw.GW_ERR_INVALID_ARG
+    assert gw.last_error().startswith("gw_rope_cs:")
+    assert L.gw_rope_cs(_fake((1 << 24) + 4), 1e4, 256, 256, 10, None) == gw.GW_ERR_INVALID_ARG  # misaligned
+    assert L.gw_rope_cs(f, 0.0, 256, 256, 10, None) == gw.GW_ERR_INVALID_ARG
+    assert L.gw_rope_cs(f, float("inf"), 256, 256, 10, None) == gw.GW_ERR_INVALID_ARG
+    assert L.gw_rope_cs(f, 1e6, 129, 512, 10, None) == gw.GW_ERR_INVALID_ARG                  # odd width
+    assert L.gw_rope_cs(f, 1e6, 1024, 512, 10, None) == gw.GW_ERR_INVALID_ARG                 # wider than the head
+    assert L.gw_rope_cs(f, 1e6, 128, 512, 0, None) == gw.GW_ERR_INVALID_ARG
 
 
 def test_bw_probe_host_validation():
@@ -144,3 +141,31 @@ def test_set_max_ctas_validation():
     assert L.gw_set_early_launch(1) == gw.GW_OK
     assert L.gw_set_early_inputs(1) == gw.GW_OK
     assert L.gw_set_early_inputs(0) == gw.GW_OK
+
+
+def test_wait_selftest_host_validation():
+    L = gw.lib()
+    f = _fake()
+    assert L.gw_wait_selftest(None, f, 1_000_000, None) == gw.GW_ERR_INVALID_ARG
+    assert gw.last_error().startswith("gw_wait_selftest:")
+    assert L.gw_wait_selftest(f, None, 1_000_000, None) == gw.GW_ERR_INVALID_ARG
+    assert L.gw_wait_selftest(f, f, 10, None) == gw.GW_ERR_INVALID_ARG               # below 1 us
+    assert L.gw_wait_selftest(f, f, 5_000_000_000, None) == gw.GW_ERR_INVALID_ARG    # above 1 s
+
+
+def test_noalloc_refusals_need_no_gpu():
+    """gw_decode_attn_local_noalloc checks its arguments, scratch size
+    included, before it touches the device: an oversized call is refused
+    with the scratch size in the message, and an invalid one with the status
+    gw_decode_attn_local gives."""
+    L = gw.lib()
+    d = _desc()
+    f = _fake()
+    rc = L.gw_decode_attn_local_noalloc(ctypes.byref(d), f, f, 32, 4096, f, f, f, 512, 1, 1024, 0.0625, None, None)
+    assert rc == gw.GW_ERR_WORKSPACE
+    msg = gw.last_error()
+    assert msg.startswith("gw_decode_attn_local_noalloc:") and str(L.gw_noalloc_scratch_bytes()) in msg
+    rc = L.gw_decode_attn_local_noalloc(ctypes.byref(d), f, f, 32, 5000, f, f, f, 512, 1, 1024, 0.0625, None, None)
+    assert rc == gw.GW_ERR_UNSUPPORTED and "4096" in gw.last_error()
+    assert L.gw_decode_attn_local_noalloc(ctypes.byref(d), f, f, 32, 0, f, f, f, 512, 1, 1024, 0.0625, None,
+                                          None) == gw.GW_OK

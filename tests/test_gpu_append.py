@@ -22,7 +22,7 @@ SENTINEL = 0x5A
 def _pools(layer, seqs=None, part="all"):
     fam = layer.fam
     max_pos = int(np.max(layer.spec.lens)) + 1
-    tab_t = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, max_pos)
+    tab_t = G.oracle_table(fam.theta, fam.rot_dim, fam.head_dim, max_pos)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     pool = G.new_pool(layer, fill=SENTINEL)
     G.append(layer, pool, tab_t.cuda(), part=part, status=status)
@@ -60,7 +60,7 @@ def test_append_e4m3_saturates_and_rounds_ties():
     vv = np.broadcast_to(v, (16, 1, 256)).copy()
     slot = layer.slots(0, np.arange(16))
     pos = np.zeros(16, np.int32)           # position 0: rotation is the identity
-    tab = gw.rope_table(1e4, 256, 256, 1)
+    tab = G.oracle_table(1e4, 256, 256, 1)
     pool = G.new_pool(layer, fill=SENTINEL)
     gw.kv_append(pool, G.bits_to_cuda_bf16(kk), G.bits_to_cuda_bf16(vv), G.i32(slot), G.i32(pos), tab.cuda())
     from oracle import pages
@@ -98,7 +98,7 @@ def test_append_out_of_range_rows_are_skipped_and_reported():
     pos = pos.copy()
     slot[3] = layer.num_pages * 16        # one past the end
     pos[5] = 100000                        # beyond the table
-    tab = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, 200)
+    tab = G.oracle_table(fam.theta, fam.rot_dim, fam.head_dim, 200)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     pool = G.new_pool(layer, fill=SENTINEL)
     gw.kv_append(pool, G.bits_to_cuda_bf16(k), G.bits_to_cuda_bf16(v), G.i32(slot), G.i32(pos), tab.cuda(), status)
@@ -109,3 +109,23 @@ def test_append_out_of_range_rows_are_skipped_and_reported():
     pages.write_local(ref, fam.kv_heads, "bf16", k[keep], v[keep], slot[keep], pos[keep], tab.numpy())
     assert np.array_equal(pool.data.cpu().numpy(), ref)
     assert int(status.item()) == (gw.GW_DEV_SLOT_RANGE | gw.GW_DEV_POS_RANGE)
+
+
+@pytest.mark.parametrize("theta,R,D", [(1e4, 256, 256), (1e6, 128, 512), (1e4, 128, 512)])
+def test_rope_cs_matches_oracle_table(theta, R, D):
+    """gw_rope_cs (float64 on the GPU, rounded once) against the oracle's
+    table (NumPy float64 with the host libm, rounded once), over 140000
+    positions.  Both round float64 values of the same definition, so they
+    agree to one float32 ulp (1e-10 absolute near zero, the float64 ulp of
+    angles up to 1.4e5); they are not bit-identical, because a float64 ulp of
+    difference between two pow/cos implementations moves the float32 rounding
+    of values near a rounding boundary.  The parity tests therefore give the
+    oracle's table to both sides."""
+    from oracle import rope
+    mine = gw.rope_cs(theta, R, D, 140000).cpu().numpy()
+    ref = rope.rope_table(theta, R, D, 140000)
+    tol = np.maximum(np.spacing(np.abs(ref)).astype(np.float64), 1e-10)
+    assert np.all(np.abs(mine.astype(np.float64) - ref) <= tol)
+    assert np.count_nonzero(mine.view(np.uint32) != ref.view(np.uint32)) < 1e-3 * ref.size
+    assert np.array_equal(mine[0, :, 0], np.ones(R // 2, np.float32))     # position 0: cos 1, sin 0
+    assert np.array_equal(mine[0, :, 1], np.zeros(R // 2, np.float32))

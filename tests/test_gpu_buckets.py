@@ -7,8 +7,10 @@ the kernels from the device-side row offsets and lengths, so a bucket needs
 no per-size plan: the unused slots get zero query rows (no units, no output)
 and their append rows write a sink page that no sequence reads.  The live
 rows of every replay must equal, bit for bit, unpadded eager calls over the
-live sequences alone (append + attention), and the pool bytes must match
-everywhere but the sink page.
+live sequences alone (append + attention), the pool bytes must match
+everywhere but the sink page, and the live rows must match the float64
+oracle (reading pools its own page writer filled) within the attention
+tolerance.
 """
 
 import numpy as np
@@ -17,6 +19,7 @@ import torch
 
 from paged_hybrid_attention_gb300 import gw, synth
 from tests import gpu_helpers as G
+from tests import oracle_helpers as H
 
 pytestmark = pytest.mark.gpu
 
@@ -109,7 +112,7 @@ def _eager(layer, snapshot, table, live):
 def test_one_bucket_graph_serves_smaller_batches_bitwise(key):
     layer = _layer(key)
     fam, sp = layer.fam, layer.spec
-    table = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sp.lens)) + 1).cuda()
+    table = G.oracle_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sp.lens)) + 1).cuda()
     pool = G.new_pool(layer)
     G.append(layer, pool, table, part="history")
     torch.cuda.synchronize()
@@ -125,6 +128,7 @@ def test_one_bucket_graph_serves_smaller_batches_bitwise(key):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         bs.step()
+    ref_pool = H.build_pool(layer, table.cpu().numpy())
     pb = pool.page_bytes
     keep = torch.ones(layer.num_pages, dtype=torch.bool, device="cuda")
     keep[bs.sink] = False
@@ -141,3 +145,6 @@ def test_one_bucket_graph_serves_smaller_batches_bitwise(key):
         got_pages = pool.data.view(layer.num_pages, pb)[keep]
         want_pages = want_pool.data.view(layer.num_pages, pb)[keep]
         assert torch.equal(got_pages, want_pages), live
+        got = G.to_f64(bs.out[:n])
+        for i, s in enumerate(live):
+            G.assert_oracle_rows(layer, got[i:i + 1], s, ref_pool)

@@ -43,7 +43,7 @@ def _attend_with_table(layer, pool, bt):
 
 def _check(layer, widths):
     fam = layer.fam
-    tab = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(layer.spec.lens)) + 1)
+    tab = G.oracle_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(layer.spec.lens)) + 1)
     pool = G.new_pool(layer)
     G.append(layer, pool, tab.cuda())
     outs = [_attend_with_table(layer, pool, _widened(layer.block_table, w)) for w in widths]

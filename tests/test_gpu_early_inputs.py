@@ -7,7 +7,8 @@ benchmark runs it: the append of this step's rows (which writes the pages the
 decode then reads), then the attention call, launched with programmatic
 dependent launch behind the append.  With early inputs on, the graph's
 outputs and pool bytes must equal, bit for bit, eager calls with the
-setting off.
+setting off; those pool bytes equal the oracle's page writer's, and those
+outputs match the float64 oracle within the attention tolerance.
 """
 
 import numpy as np
@@ -16,6 +17,7 @@ import torch
 
 from paged_hybrid_attention_gb300 import gw, synth
 from tests import gpu_helpers as G
+from tests import oracle_helpers as H
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +49,8 @@ def _attend(layer, pool, q, out, cu, lens, bt, ws, mq, status):
 def test_early_inputs_same_bits(kind, mixed):
     layer = _layer(kind, mixed)
     fam, sp = layer.fam, layer.spec
-    table = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sp.lens)) + 1).cuda()
+    table_np = G.oracle_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sp.lens)) + 1)
+    table = table_np.cuda()
     pool = G.new_pool(layer)
     G.append(layer, pool, table, part="history")
     torch.cuda.synchronize()
@@ -69,6 +72,9 @@ def test_early_inputs_same_bits(kind, mixed):
     step()
     torch.cuda.synchronize()
     want, want_pool = out.clone(), pool.data.clone()
+    ref_pool = H.build_pool(layer, table_np.numpy(), pool=np.zeros(pool.nbytes, np.uint8))
+    assert np.array_equal(want_pool.cpu().numpy(), ref_pool)
+    G.check_layer_vs_oracle(layer, want, ref_pool)
     try:
         gw.set_early_inputs(True)
         side = torch.cuda.Stream()
@@ -97,7 +103,7 @@ def test_early_inputs_bad_length_still_reported():
     too (the check moves after the wait) and is not read."""
     layer = _layer("local", False)
     fam, sp = layer.fam, layer.spec
-    table = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sp.lens)) + 1).cuda()
+    table = G.oracle_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sp.lens)) + 1).cuda()
     pool = G.new_pool(layer)
     G.append(layer, pool, table)
     lens = sp.lens.copy()

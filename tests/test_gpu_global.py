@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 def _run(layer, seqs_for_oracle=None, status_ok=True):
     fam = layer.fam
     max_pos = int(np.max(layer.spec.lens)) + 1
-    tab = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, max_pos)
+    tab = G.oracle_table(fam.theta, fam.rot_dim, fam.head_dim, max_pos)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     pool = G.new_pool(layer)
     G.append(layer, pool, tab.cuda(), status=status)
@@ -72,11 +72,11 @@ def test_global_serving_full():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("key", ["global", "global_full"])
-def test_global_long_context_sampled(key):
+@pytest.mark.parametrize("key,seqs", [("global", list(range(8))), ("global_full", [2, 7])])
+def test_global_long_context_sampled(key, seqs):
     layer = synth.Layer(synth.spec("long_global"), key)
-    out, ref, _ = _run(layer, [2, 7])
-    mx, rl = _compare(layer, out, ref, [2, 7])
+    out, ref, _ = _run(layer, seqs)
+    mx, rl = _compare(layer, out, ref, seqs)
     print("long_global %s worst max-abs %.3g rel-l2 %.3g" % (key, mx, rl))
 
 
@@ -100,7 +100,7 @@ def test_global_batch_invariance_bitwise():
     sub = synth.custom("ginv", sp.seed, 32, sp.lens[:5], sp.n_rows[:5], sp.families)
     layer = synth.Layer(sub, "global")
     fam = layer.fam
-    tab = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sub.lens)) + 1).cuda()
+    tab = G.oracle_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sub.lens)) + 1).cuda()
     pool = G.new_pool(layer)
     G.append(layer, pool, tab)
     full = G.attend(layer, pool)
@@ -118,7 +118,7 @@ def test_global_batch_invariance_bitwise():
 def test_global_page_permutation_bitwise():
     fam = synth.Family("global", "bf16", "folded", 1, 512, 128, 1e6, 0)
     layer = synth.Layer(synth.custom("gperm", 6, 32, [300, 1200, 45], [1, 1, 1], {"global": fam}), "global")
-    tab = gw.rope_table(1e6, 128, 512, 1201).cuda()
+    tab = G.oracle_table(1e6, 128, 512, 1201).cuda()
     pool = G.new_pool(layer)
     G.append(layer, pool, tab)
     base = G.attend(layer, pool)
@@ -139,7 +139,7 @@ def test_global_garbage_past_end_is_ignored():
     patterns) must not reach the output."""
     fam = synth.Family("global", "bf16", "folded", 1, 512, 128, 1e6, 0)
     layer = synth.Layer(synth.custom("gnan", 7, 32, [37, 100, 1001], [1, 1, 1], {"global": fam}), "global")
-    tab = gw.rope_table(1e6, 128, 512, 1002)
+    tab = G.oracle_table(1e6, 128, 512, 1002)
     pool = G.new_pool(layer, fill=0xFF)        # 0xFFFF is a bf16 NaN
     G.append(layer, pool, tab.cuda())
     out = G.attend(layer, pool)
@@ -152,7 +152,7 @@ def test_global_garbage_past_end_is_ignored():
 def test_global_bad_page_reported():
     fam = synth.Family("global", "bf16", "folded", 1, 512, 128, 1e6, 0)
     layer = synth.Layer(synth.custom("gbad", 8, 32, [500, 200], [1, 1], {"global": fam}), "global")
-    tab = gw.rope_table(1e6, 128, 512, 501).cuda()
+    tab = G.oracle_table(1e6, 128, 512, 501).cuda()
     pool = G.new_pool(layer)
     G.append(layer, pool, tab)
     good = G.attend(layer, pool)

@@ -1,6 +1,7 @@
 """The C-ABI calls captured in a CUDA graph (as the benchmark runs them)
 give the same bits as eager calls, replay after replay, for decode and
-mixed (prompt-row) steps on both families."""
+mixed (prompt-row) steps on both families; the eager results match the
+float64 oracle within the attention tolerance."""
 
 import numpy as np
 import pytest
@@ -8,6 +9,7 @@ import torch
 
 from paged_hybrid_attention_gb300 import gw, synth
 from tests import gpu_helpers as G
+from tests import oracle_helpers as H
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +31,8 @@ def _layer(key, mixed):
 def test_graph_replay_matches_eager_bitwise(key, mixed):
     layer = _layer(key, mixed)
     fam, sp = layer.fam, layer.spec
-    tab = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sp.lens)) + 1).cuda()
+    tab_np = G.oracle_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sp.lens)) + 1)
+    tab = tab_np.cuda()
     pool = G.new_pool(layer)
     G.append(layer, pool, tab)
     q = G.bits_to_cuda_bf16(layer.queries())
@@ -48,6 +51,7 @@ def test_graph_replay_matches_eager_bitwise(key, mixed):
     call()
     torch.cuda.synchronize()
     want = out.clone()
+    G.check_layer_vs_oracle(layer, want, H.build_pool(layer, tab_np.numpy()))
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):

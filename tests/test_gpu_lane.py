@@ -2,7 +2,8 @@
 any cap as with one CTA per SM (a work unit's arithmetic never depends on
 which CTA runs it), for decode rows and prompt rows on both families, and a
 capped prompt lane without early launch on a second stream beside a decode
-lane leaves both results unchanged."""
+lane leaves both results unchanged.  The uncapped results themselves are
+checked against the float64 oracle within the attention tolerance."""
 
 import numpy as np
 import pytest
@@ -10,6 +11,7 @@ import torch
 
 from paged_hybrid_attention_gb300 import gw, synth
 from tests import gpu_helpers as G
+from tests import oracle_helpers as H
 
 pytestmark = pytest.mark.gpu
 
@@ -27,10 +29,15 @@ def _layer(key, mixed, n=8):
 
 def _setup(layer):
     fam, sp = layer.fam, layer.spec
-    tab = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sp.lens)) + 1).cuda()
+    tab = G.oracle_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(sp.lens)) + 1)
     pool = G.new_pool(layer)
-    G.append(layer, pool, tab)
+    G.append(layer, pool, tab.cuda())
+    layer.ref_pool = H.build_pool(layer, tab.numpy())
     return pool
+
+
+def _check_oracle(layer, out):
+    G.check_layer_vs_oracle(layer, out, layer.ref_pool)
 
 
 @pytest.mark.parametrize("mixed", [False, True])
@@ -40,6 +47,8 @@ def test_cap_gives_same_bits(key, mixed):
     pool = _setup(layer)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     ref = G.attend(layer, pool, status=status).clone()
+    torch.cuda.synchronize()
+    _check_oracle(layer, ref)
     try:
         for cap in (1, 7, 53, 99):
             gw.set_max_ctas(cap)
@@ -59,6 +68,8 @@ def test_capped_lane_beside_decode_lane():
     ref_d = G.attend(dec, pool_d, status=status).clone()
     ref_p = G.attend(pre, pool_p, status=status).clone()
     torch.cuda.synchronize()
+    _check_oracle(dec, ref_d)
+    _check_oracle(pre, ref_p)
     sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
     sa.wait_stream(torch.cuda.current_stream())
     sb.wait_stream(torch.cuda.current_stream())

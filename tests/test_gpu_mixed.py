@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 def _build(layer):
     fam = layer.fam
-    tab = gw.rope_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(layer.spec.lens)) + 1)
+    tab = G.oracle_table(fam.theta, fam.rot_dim, fam.head_dim, int(np.max(layer.spec.lens)) + 1)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     pool = G.new_pool(layer, fill=0xFF)           # unwritten bytes are NaN patterns
     G.append(layer, pool, tab.cuda(), status=status)
@@ -57,6 +57,38 @@ def _check(layer, out, tab, seq_rows):
             mx, rl = G.errors(got[cu[s] + r], want)
             worst = (max(worst[0], mx), max(worst[1], rl))
             assert mx <= G.MAX_ABS and rl <= G.REL_L2, (s, r, mx, rl)
+    return worst
+
+
+def _check_whole_prompt(layer, out, tab, s):
+    """Every row of sequence s's prompt segment against the oracle.  The
+    segment's keys are read from the oracle pool once and each row attends
+    over its own key range, as attention.local_rows / global_rows define it
+    (they read the pool again for every row, which is too slow for 2048
+    rows)."""
+    fam, sp = layer.fam, layer.spec
+    L, n = int(sp.lens[s]), int(sp.n_rows[s])
+    scale = 1.0 / np.sqrt(fam.head_dim)
+    ref = H.build_pool(layer, tab.numpy(), seqs=[s])
+    q = bf16_bits_to_f64(layer.q(s))
+    got = G.to_f64(out)[layer.cu_rows()[s]:layer.cu_rows()[s] + n]
+    if fam.layout == "local":
+        first = max(0, L - n - fam.window + 1)
+        K, V = pages.read_local(ref, fam.kv_heads, fam.dtype, layer.block_table[s], np.arange(first, L))
+    else:
+        rows = pages.read_global_rows(ref, fam.layout, layer.block_table[s], np.arange(L))
+        K, V = attention.rebuild_global_k(rows) if fam.layout == "folded" else attention.split_full_rows(rows)
+        K, V, first = K[:, None], V[:, None], 0
+    worst = (0.0, 0.0)
+    for r in range(n):
+        p = L - n + r
+        J = (attention.local_keys(p, fam.window) if fam.layout == "local" else attention.global_keys(p)) - first
+        sl = slice(int(J[0]), int(J[-1]) + 1)        # J is contiguous: a view, not a copy
+        assert len(J) == sl.stop - sl.start
+        want = attention.attend(q[r], K[sl], V[sl], scale)
+        mx, rl = G.errors(got[r], want)
+        worst = (max(worst[0], mx), max(worst[1], rl))
+        assert mx <= G.MAX_ABS and rl <= G.REL_L2, (s, r, mx, rl)
     return worst
 
 
@@ -125,11 +157,12 @@ def test_mixed_full_size_sampled(key):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     rng = np.random.Generator(np.random.PCG64(3))
-    sample = {0: [0], 17: [0], 47: [0],
-              48: sorted(rng.choice(2048, 12, replace=False).tolist() + [0, 1023, 1024, 2047]),
-              51: sorted(rng.choice(2048, 6, replace=False).tolist() + [2047])}
+    sample = {s: [0] for s in range(48)}          # every decode row
+    sample[51] = sorted(rng.choice(2048, 6, replace=False).tolist() + [2047])
     mx, rl = _check(layer, out, tab, sample)
-    print("mixed %s sampled worst max-abs %.3g rel-l2 %.3g" % (key, mx, rl))
+    wm, wr = _check_whole_prompt(layer, out, tab, 48)   # one whole 2048-row prompt
+    print("mixed %s: decode rows + sampled worst max-abs %.3g rel-l2 %.3g; whole prompt 48 max-abs %.3g "
+          "rel-l2 %.3g" % (key, mx, rl, wm, wr))
 
 
 @pytest.mark.slow
@@ -143,10 +176,10 @@ def test_chunked_continuation_full_size_sampled(key):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     rng = np.random.Generator(np.random.PCG64(4))
-    sample = {0: [0], 31: [0],
-              32: sorted(rng.choice(1024, 6, replace=False).tolist() + [0, 1023]),
-              35: sorted(rng.choice(1024, 4, replace=False).tolist() + [511])}
+    sample = {s: [0] for s in range(32)}          # every decode row
+    sample[35] = sorted(rng.choice(1024, 4, replace=False).tolist() + [511])
     mx, rl = _check(layer, out, tab, sample)
+    _check_whole_prompt(layer, out, tab, 32)      # one whole 1024-row chunk
     print("chunked %s sampled worst max-abs %.3g rel-l2 %.3g" % (key, mx, rl))
 
 
