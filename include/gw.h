@@ -81,6 +81,7 @@ typedef int32_t gw_status;
 #define GW_LAYOUT_LOCAL 0         /* sliding-window layers                   */
 #define GW_LAYOUT_GLOBAL_FOLDED 1 /* global layers, V(512) + k_rot(128)     */
 #define GW_LAYOUT_GLOBAL_FULL 2   /* global layers, K(512) + V(512) control */
+#define GW_LAYOUT_GLOBAL_FOLDED_E4M3 3 /* opt-in: V(512) + k_rot(128) in e4m3 */
 
 /*
  * A paged KV pool: `num_pages` pages of 16 tokens at `base` (device, 256-byte
@@ -97,6 +98,14 @@ typedef int32_t gw_status;
  *   GLOBAL_FULL   (bf16, head_dim 512, rot_dim 128, kv_heads 1)
  *           a token row is K[0:512] || V[0:512], same 8x8 blocking with 128
  *           column blocks.  32768 B per page.
+ *   GLOBAL_FOLDED_E4M3 (e4m3, head_dim 512, rot_dim 128, kv_heads 1)
+ *           the folded row V[0:512] || k_rot[0:128] with every element
+ *           rounded once to e4m3, stored as [token block 2][column block
+ *           40][row 8][column 16]: token o = 8*tb + r, e = 16*cb + c.
+ *           10240 B per page (0.3125x of GLOBAL_FULL).  The pages serve e4m3
+ *           for the sliding family only and refuse it for global layers, so
+ *           this layout is an explicit opt-in: dtype e4m3 on GLOBAL_FOLDED
+ *           stays refused ("supports only local").
  *
  * In the folded layout the unrotated dims of K are not stored: attention uses
  * K = k_rot || V[128:512].  The caller folds the k_norm gain of those dims
@@ -138,15 +147,42 @@ size_t gw_pool_page_bytes(const gw_kv_pool* pool);
  * (binary32, no fused multiply-add), then rounded once to the pool type:
  * bf16 round-to-nearest-even, or e4m3 round-to-nearest-even saturating to
  * +-448.  V (and the unrotated K dims of a FULL pool) are copied (bf16) or
- * rounded once to e4m3.  Rows whose slot or pos is out of range are skipped
+ * rounded once to e4m3 (a GLOBAL_FOLDED_E4M3 pool rounds k_rot once from its
+ * float32 rotation and V once from bf16).  Rows whose slot or pos is out of
+ * range are skipped
  * (GW_DEV_SLOT_RANGE / GW_DEV_POS_RANGE).  num_rows == 0 is a no-op.
- * Alignment: k, v 16 B; slot, pos, rope_cs 4 B.
- * Errors: GW_ERR_INVALID_ARG, GW_ERR_UNSUPPORTED (e4m3 on a global pool:
- * "supports only local"), GW_ERR_CUDA.
+ * rope_cs is the table gw_rope_cs fills.
+ * Alignment: k, v, rope_cs 16 B; slot, pos 4 B.
+ * Errors: GW_ERR_INVALID_ARG, GW_ERR_UNSUPPORTED (e4m3 on a GLOBAL_FOLDED or
+ * GLOBAL_FULL pool: "supports only local"), GW_ERR_CUDA.
  */
 gw_status gw_kv_append(const gw_kv_pool* pool, const void* k, const void* v, int32_t num_rows,
                        const int32_t* slot, const int32_t* pos, const float* rope_cs, int32_t max_pos,
                        int32_t* dev_status, void* stream);
+
+/*
+ * gw_rope_cs - fill the (cos, sin) table that gw_kv_append takes as rope_cs.
+ *
+ * [pegainfer] "Architecture notes": local layers rotate all 256 dims of K
+ * with theta 10k; global layers use a proportional RoPE that rotates 128 of
+ * the 512 dims with theta 1M while the frequency denominator stays the full
+ * head dim.  So the table takes both the rotated width and the head dim:
+ *
+ *   inv_f_i = theta^((-2 i) / head_dim),      i in [0, rot_dim / 2)
+ *   rope_cs[p][i] = (cos(p * inv_f_i), sin(p * inv_f_i)),  p in [0, max_pos)
+ *
+ * computed on the GPU in float64 (frequency, angle, cosine and sine) and
+ * rounded once to float32.  Local pools take (theta 1e4, rot_dim 256,
+ * head_dim 256); global pools (theta 1e6, rot_dim 128, head_dim 512).
+ *
+ *   rope_cs   device float32 [max_pos][rot_dim / 2][2], caller-owned,
+ *             16-byte aligned; fully overwritten.
+ * Errors: GW_ERR_INVALID_ARG (NULL or misaligned rope_cs, theta not finite
+ * and positive, rot_dim odd or outside [2, head_dim], max_pos < 1),
+ * GW_ERR_CUDA.  Asynchronous on `stream`.
+ */
+gw_status gw_rope_cs(float* rope_cs, double theta, int32_t rot_dim, int32_t head_dim, int32_t max_pos,
+                     void* stream);
 
 /*
  * gw_decode_attn_local - sliding-window attention on a LOCAL pool.
@@ -187,14 +223,22 @@ gw_status gw_decode_attn_local(const gw_kv_pool* pool, const void* q, void* out,
                                int32_t* dev_status, void* stream);
 
 /*
- * gw_decode_attn_global - global attention on a GLOBAL_FOLDED or GLOBAL_FULL
- * pool: as gw_decode_attn_local with no window (j in [0, p]) and head dim 512.
+ * gw_decode_attn_global - global attention on a GLOBAL_FOLDED, GLOBAL_FULL or
+ * GLOBAL_FOLDED_E4M3 pool: as gw_decode_attn_local with no window
+ * (j in [0, p]) and head dim 512.
  *
- * [pegainfer] "Architecture notes"; [Gewell] "the Why".  On a FOLDED pool the
+ * [pegainfer] "Architecture notes"; [Gewell] "the Why".  On a folded pool the
  * kernel forms K_j = k_rot_j || V_j[128:512] on chip from the same page tile
  * that supplies V_j.  num_q_heads must be 8, 16 or 32 and batch at most
- * 4096.  Errors as above; GW_ERR_UNSUPPORTED for an e4m3 pool ("supports
- * only local").
+ * 4096.  Errors as above; GW_ERR_UNSUPPORTED for dtype e4m3 on a GLOBAL_FOLDED
+ * or GLOBAL_FULL pool ("supports only local"), and for prompt rows
+ * (max_q_rows > 1) on a GLOBAL_FOLDED_E4M3 pool.
+ *
+ * On a GLOBAL_FOLDED_E4M3 pool the contractions run on the e4m3 tiles as
+ * stored; q and the softmax weights enter them as sums of two e4m3 terms
+ * (q after an exact per-head power-of-two scaling), which carries them at
+ * about bf16 precision.  Output rows match attention over the stored e4m3
+ * values within the same tolerance as a bf16 pool.
  */
 gw_status gw_decode_attn_global(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,
                                 int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,
@@ -213,21 +257,24 @@ size_t gw_attn_workspace_bytes(const gw_kv_pool* pool, int32_t num_q_heads, int3
 /*
  * gw_decode_attn_local_noalloc - gw_decode_attn_local without a workspace
  * argument, for callers that cannot allocate device memory when they run
- * attention (a CUDA graph whose memory plan is already fixed, an embedding
- * runtime without a device allocator, a host that forbids allocation after
- * start-up).  The pages this library follows have no counterpart of this
- * entry point; it exists only for such callers.
+ * attention (an embedding runtime without a device allocator of its own, a
+ * host that forbids device allocation once serving has started).  The pages
+ * this library follows have no counterpart of this entry point; it exists
+ * only for such callers.
  *
  * Same arguments, semantics, results and errors as gw_decode_attn_local,
  * minus workspace/workspace_bytes.  The split-KV scratch is a file-scope
  * device array of gw_noalloc_scratch_bytes() = 32 MiB that every GPU loading
  * this library keeps until the process exits; the call allocates and frees
- * nothing.  A call whose gw_attn_workspace_bytes(...) (with max_seq_len =
- * max_pages_per_seq * 16) exceeds 32 MiB returns GW_ERR_WORKSPACE.
+ * nothing.  Arguments are checked as by gw_decode_attn_local (same statuses
+ * for the same faults); a call whose gw_attn_workspace_bytes(...) (with
+ * max_seq_len = max_pages_per_seq * 16) exceeds 32 MiB returns
+ * GW_ERR_WORKSPACE, before anything is launched.
  *
  * The first call on a device looks up the array's device address with that
- * device current (cudaGetSymbolAddress) and caches it; make that first call
- * before any stream capture.  All calls share the one array and it keeps the
+ * device current (cudaGetSymbolAddress) and caches it with the current CUDA
+ * context; a call in another context (after a device reset) looks it up
+ * again.  Make the first call on each device before any stream capture.  All calls share the one array and it keeps the
  * last call's contents (each call re-initialises what it needs), so calls
  * whose executions overlap on the GPU (different streams without ordering)
  * race on it.  Sequences with more than one query row (prompt rows of a mixed
@@ -308,6 +355,38 @@ gw_status gw_set_early_inputs(int32_t on);
  * GW_ERR_CUDA.  Asynchronous on `stream`.
  */
 gw_status gw_bw_probe(const void* buf, size_t bytes, int32_t* dev_status, void* stream);
+
+/*
+ * gw_bw_probe_tma - as gw_bw_probe, through the copy pipeline of the bf16
+ * local decode kernel instead: one CTA per SM, 6 warps, each with a 2-stage
+ * ring of 16 KiB shared-memory stages, a stage being one 16-token page head
+ * (K then V) brought by 8 tensor-map copies of 2 KiB (128-byte swizzled).
+ * The first floor(bytes / 16384) * 16384 bytes of `buf` are read as the
+ * pages of a LOCAL bf16 pool with one KV head, in page order, and discarded.
+ * A measurement aid with no counterpart in the pages.
+ *   buf          device memory, 256-byte aligned, caller-owned, only read.
+ *   bytes        in [16384, 2^36].
+ * Errors: GW_ERR_INVALID_ARG, GW_ERR_CUDA.  Asynchronous on `stream`.
+ */
+gw_status gw_bw_probe_tma(const void* buf, size_t bytes, int32_t* dev_status, void* stream);
+
+/*
+ * gw_wait_selftest - a test aid, not part of the method: runs the bounded
+ * mbarrier wait that every kernel of this library uses, on one warp, with a
+ * limit of `limit_ns` instead of the kernels' 2 s.  A phase that an arrival
+ * completes is waited on first (must succeed); then a phase that nothing
+ * ever completes, whose wait must give up after limit_ns, OR GW_DEV_TIMEOUT
+ * into *dev_status and return, so that the kernel ends normally and the
+ * context stays usable.  This is how the kernels' timeout path is tested
+ * without hanging a GPU.  The pages this library follows have no
+ * counterpart of this entry point.
+ *   dev_status  device int32, caller-zeroed.
+ *   result      device int32[3]: {first wait succeeded (1), second wait gave
+ *               up (1), microseconds spent in the second wait}.
+ *   limit_ns    in [1e3, 1e9].
+ * Errors: GW_ERR_INVALID_ARG, GW_ERR_CUDA.  Asynchronous on `stream`.
+ */
+gw_status gw_wait_selftest(int32_t* dev_status, int32_t* result, int64_t limit_ns, void* stream);
 
 /* Message of the calling thread's last failed call ("" if none). */
 const char* gw_last_error(void);

@@ -52,24 +52,44 @@ constexpr int kTilePages = 4;  // 64 tokens = UMMA M of QK^T
 constexpr int kRing = 4;       // tile descriptors in flight
 constexpr float kLazyThreshold = 8.f;
 
+// Page geometry per layout.  Every layout stores 8-token x 16-byte blocks
+// (8 bf16 or 16 e4m3 elements per block row); kBlk is the number of such
+// column blocks per 8-token block.  A QK^T K-step covers 16 dims (bf16) or
+// 32 dims (e4m3), i.e. two column blocks either way.
 template <int LAYOUT>
 struct GTraits;
 template <>
 struct GTraits<GW_LAYOUT_GLOBAL_FOLDED> {
+  static constexpr bool kE4 = false;
   static constexpr int kPageBytes = 20480;
-  static constexpr int kBlk = 80;   // 8-column blocks per 8-token block
+  static constexpr int kBlk = 80;   // 16-byte column blocks per 8-token block
   static constexpr int kNumBuf = 2;  // tile buffers
   static constexpr int kVcb = 0;    // column block of V dim 0
+  static constexpr int kKSteps = 32;
   // column block holding K dims [16 ks, 16 ks + 16)
   __device__ static int k_cb(int ks) { return ks < 8 ? 64 + 2 * ks : 2 * ks; }
 };
 template <>
 struct GTraits<GW_LAYOUT_GLOBAL_FULL> {
+  static constexpr bool kE4 = false;
   static constexpr int kPageBytes = 32768;
   static constexpr int kBlk = 128;
   static constexpr int kNumBuf = 1;
   static constexpr int kVcb = 64;
+  static constexpr int kKSteps = 32;
   __device__ static int k_cb(int ks) { return 2 * ks; }
+};
+template <>
+struct GTraits<GW_LAYOUT_GLOBAL_FOLDED_E4M3> {
+  static constexpr bool kE4 = true;
+  static constexpr int kPageBytes = 10240;
+  static constexpr int kBlk = 40;
+  static constexpr int kNumBuf = 2;
+  static constexpr int kVcb = 0;
+  static constexpr int kKSteps = 16;
+  // column block holding K dims [32 ks, 32 ks + 32): k_rot (elements
+  // 512..639, blocks 32..39) for dims 0..127, V for dims 128..511
+  __device__ static int k_cb(int ks) { return ks < 4 ? 32 + 2 * ks : 2 * ks; }
 };
 
 struct TileDesc {
@@ -84,20 +104,36 @@ template <int LAYOUT, int HQ>
 struct GSmem {
   using T = GTraits<LAYOUT>;
   static constexpr int kNP = HQ < 16 ? 16 : HQ;  // P.V N (M=128 needs N % 16 == 0)
+  // Q buffers: one for bf16 pools (written once the previous unit's last
+  // QK^T has completed); two for the e4m3 pool, whose q is converted on chip
+  // and so is prepared while the previous unit still runs.
+  static constexpr int kQBuf = T::kE4 ? 2 : 1;
+  // bf16: K-major Q [hb][cb 64][8 heads][8 dims].  e4m3: the hi term then
+  // the lo term, each K-major [hb][cb 32][8 heads][16 dims].
+  static constexpr int kQBytes = HQ * 512 * 2;
+  // bf16: MN-major P^T [tb 8][hb 8-head blocks][8 tokens][8 heads].  e4m3:
+  // the hi term then the lo term, each [tb 8][16-head blocks][8 tokens][16 heads].
+  static constexpr int kPBytes = 64 * kNP * 2;
   uint8_t tiles[T::kNumBuf][kTilePages][T::kPageBytes];
-  uint8_t q[HQ * 512 * 2];     // K-major Q: [hb][cb 64][8][8] bf16
-  uint8_t p[2][64 * kNP * 2];  // MN-major P^T: [tb 8][hb][8 tokens][8 heads] bf16
+  uint8_t q[kQBuf][kQBytes];
+  uint8_t p[2][kPBytes];
   float red[4][32];            // per-warp head reductions
   float mvec[32];              // reference max per head (log2 units)
+  float qscale[4][32];         // e4m3: per unit (mod 4), per head: 2^-e of q's scaling
+  // e4m3: the unit's bf16 q rows staged for conversion, rows padded by 16 B
+  // so that the 8 heads a conversion step reads sit in different banks
+  static constexpr int kStageRow = 1040;
+  uint8_t qstage[T::kE4 ? HQ * kStageRow : 16];
   TileDesc ring[kRing];
   uint64_t full[T::kNumBuf], slot_empty[T::kNumBuf][kTilePages];
-  uint64_t s_ready[2], p_ready[2], pfree[2], o_done[2], o_free[2], q_ready, q_free;
+  uint64_t s_ready[2], p_ready[2], pfree[2], o_done[2], o_free[2], q_ready[2], q_free[2], qs_ready[4];
   uint32_t tmem_base;
   int32_t flag[2];  // per tile parity: index + 1 of the last tile that asked for a new max
   int32_t ub[kMaxBatch + 1 + 32];  // split plan (+ scan scratch)
 };
 static_assert(sizeof(GSmem<GW_LAYOUT_GLOBAL_FOLDED, 32>) <= 232448, "shared memory of one CTA");
 static_assert(sizeof(GSmem<GW_LAYOUT_GLOBAL_FULL, 32>) <= 232448, "shared memory of one CTA");
+static_assert(sizeof(GSmem<GW_LAYOUT_GLOBAL_FOLDED_E4M3, 32>) <= 232448, "shared memory of one CTA");
 
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -154,6 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
   using SM = GSmem<LAYOUT, HQ>;
   constexpr int NB = T::kNumBuf;
   constexpr int NP = SM::kNP;
+  constexpr bool kE4 = T::kE4;
+  constexpr int QB = SM::kQBuf;
   constexpr uint32_t kTileBytes = kTilePages * T::kPageBytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   SM& sm = *reinterpret_cast<SM*>(smem_raw);
@@ -181,8 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       mbar_init(&sm.o_free[b], 128);
       sm.flag[b] = 0;
     }
-    mbar_init(&sm.q_ready, 1);
-    mbar_init(&sm.q_free, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.q_ready[b], 1);
+      mbar_init(&sm.q_free[b], 1);
+    }
+    for (int b = 0; b < 4; ++b) mbar_init(&sm.qs_ready[b], 1);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -291,12 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     wait_prev();
     // The whole warp runs this loop with warp-uniform values; elect.sync
     // picks the issuing lane inside mma_bf16_warp / commit_warp.
-    const uint32_t id_qk = tc::idesc_bf16(64, HQ, false, false);
+    const uint32_t id_qk = kE4 ? tc::idesc_e4m3(64, HQ, false, false) : tc::idesc_bf16(64, HQ, false, false);
     // descriptor bases; the start-address field is addr >> 4 in the low bits,
-    // so a byte offset o is added as o >> 4 (all addresses stay below 256 KiB)
+    // so a byte offset o is added as o >> 4 (all addresses stay below 256 KiB).
+    // Q: 16-byte block rows, the next 8 heads (kQBytes / 2 / (HQ / 8)) apart
+    // within a term.
     const uint64_t qk_a0 = tc::smem_desc(smem_u32(sm.tiles[0]), 128, T::kBlk * 128);
-    const uint64_t qk_b0 = tc::smem_desc(smem_u32(sm.q), 128, 64 * 128);
-    int uidx = -1;
+    const uint64_t qk_b0 = tc::smem_desc(smem_u32(sm.q[0]), 128, kE4 ? 32 * 128 : 64 * 128);
+    int uidx = -1, qb = 0;
     for (uint32_t n = 0;; ++n) {
       const int b = n % NB;
       if (!warp_wait(&sm.full[b], (n / NB) & 1, st)) break;
@@ -304,28 +347,37 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       if (d.flags & kEnd) break;
       if (d.flags & kFirst) {
         ++uidx;
-        if (!warp_wait(&sm.q_ready, uidx & 1, st)) break;
+        qb = uidx % QB;
+        if (!warp_wait(&sm.q_ready[qb], (uidx / QB) & 1, st)) break;
       }
       // S^T buffer n & 1 is free once the softmax of tile n - 2 has read it
       if (n >= 2 && !warp_wait(&sm.p_ready[n & 1], ((n >> 1) - 1) & 1, st)) break;
       tc::fence_after();
       const uint64_t a_tile = qk_a0 + ((b * kTileBytes) >> 4);
+      const uint64_t q_base = qk_b0 + ((qb * SM::kQBytes) >> 4);
       const uint32_t d_s = tmem + 32 * (n & 1);
 #pragma unroll
-      for (int ks = 0; ks < 32; ++ks) {
+      for (int ks = 0; ks < T::kKSteps; ++ks) {
         const uint64_t ad = a_tile + ((T::k_cb(ks) * 128) >> 4);
-        const uint64_t bd = qk_b0 + ((2 * ks * 128) >> 4);
-        tc::mma_bf16_warp(d_s, ad, bd, id_qk, ks > 0);
+        const uint64_t bd = q_base + ((2 * ks * 128) >> 4);
+        if constexpr (kE4) {
+          // S = K . (q_hi + q_lo): two MMAs into one accumulator
+          tc::mma_e4m3_warp(d_s, ad, bd, id_qk, ks > 0);
+          tc::mma_e4m3_warp(d_s, ad, bd + ((HQ * 512) >> 4), id_qk, true);
+        } else {
+          tc::mma_bf16_warp(d_s, ad, bd, id_qk, ks > 0);
+        }
       }
       tc::commit_warp(&sm.s_ready[n & 1]);
-      if (d.flags & kLast) tc::commit_warp(&sm.q_free);  // Q may be replaced once this completes
+      if (d.flags & kLast) tc::commit_warp(&sm.q_free[qb]);  // Q buffer qb may be replaced once this completes
     }
   } else if (warp == 7) {
     // ------------------------------------------------------------ P.V issue
     wait_prev();
-    const uint32_t id_pv = tc::idesc_bf16(128, NP, true, true);
+    const uint32_t id_pv = kE4 ? tc::idesc_e4m3(128, NP, true, true) : tc::idesc_bf16(128, NP, true, true);
     const uint64_t pv_a0 = tc::smem_desc(smem_u32(sm.tiles[0]), T::kBlk * 128, 128);
-    const uint64_t pv_b0 = tc::smem_desc(smem_u32(sm.p[0]), (NP / 8) * 128, 128);
+    // P^T: 8-token block rows (NP / 8 or NP / 16 head blocks of 16 bytes) apart
+    const uint64_t pv_b0 = tc::smem_desc(smem_u32(sm.p[0]), (kE4 ? NP / 16 : NP / 8) * 128, 128);
     int ui = -1;
     for (uint32_t n = 0;; ++n) {
       const int b = n % NB;
@@ -338,19 +390,126 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       if ((d.flags & kFirst) && ui >= 2 && !warp_wait(&sm.o_free[ob], ((ui >> 1) - 1) & 1, st)) break;
       tc::fence_after();
       const uint64_t a_tile = pv_a0 + ((b * kTileBytes) >> 4);
-      const uint64_t b_p = pv_b0 + (((n & 1) * sizeof(sm.p[0])) >> 4);
+      const uint64_t b_p = pv_b0 + (((n & 1) * SM::kPBytes) >> 4);
+      if constexpr (kE4) {
+        // K = 32 tokens per MMA: pages 2j and 2j + 1; O^T += V^T (P_hi + P_lo)^T
 #pragma unroll
-      for (int j = 0; j < kTilePages; ++j) {
-        const uint64_t bd = b_p + ((2 * j * (NP / 8) * 128) >> 4);
+        for (int j = 0; j < kTilePages / 2; ++j) {
+          const uint64_t bd = b_p + ((4 * j * (NP / 16) * 128) >> 4);
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          const uint64_t ad = a_tile + ((j * T::kPageBytes + (T::kVcb + 16 * blk) * 128) >> 4);
-          tc::mma_bf16_warp(tmem + 64 + 128 * ob + 32 * blk, ad, bd, id_pv, !((d.flags & kFirst) && j == 0));
+          for (int blk = 0; blk < 4; ++blk) {
+            const uint64_t ad = a_tile + ((2 * j * T::kPageBytes + (T::kVcb + 8 * blk) * 128) >> 4);
+            const uint32_t d_o = tmem + 64 + 128 * ob + 32 * blk;
+            tc::mma_e4m3_warp(d_o, ad, bd, id_pv, !((d.flags & kFirst) && j == 0));
+            tc::mma_e4m3_warp(d_o, ad, bd + ((64 * NP) >> 4), id_pv, true);
+          }
+          tc::commit_warp(&sm.slot_empty[b][2 * j]);  // the producer may refill these page slots
+          tc::commit_warp(&sm.slot_empty[b][2 * j + 1]);
         }
-        tc::commit_warp(&sm.slot_empty[b][j]);  // the producer may refill this page slot
+      } else {
+#pragma unroll
+        for (int j = 0; j < kTilePages; ++j) {
+          const uint64_t bd = b_p + ((2 * j * (NP / 8) * 128) >> 4);
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+            const uint64_t ad = a_tile + ((j * T::kPageBytes + (T::kVcb + 16 * blk) * 128) >> 4);
+            tc::mma_bf16_warp(tmem + 64 + 128 * ob + 32 * blk, ad, bd, id_pv, !((d.flags & kFirst) && j == 0));
+          }
+          tc::commit_warp(&sm.slot_empty[b][j]);  // the producer may refill this page slot
+        }
       }
       tc::commit_warp(&sm.pfree[n & 1]);
       if (d.flags & kLast) tc::commit_warp(&sm.o_done[ob]);
+    }
+  } else if (warp == 6 && kE4) {
+    // ------------------------------------------------- q loader, e4m3 pool
+    wait_prev();
+    // Unit k's q goes to Q buffer k & 1 once the last QK^T of unit k - 2 has
+    // completed.  Each head is scaled by an exact power of two 2^e, chosen so
+    // that its largest |q| lands in [128, 256), and split into two e4m3
+    // terms, hi = e4m3(q 2^e) and lo = e4m3(q 2^e - hi); 2^-e goes to the
+    // softmax, which scales the logits back.
+    int k = 0;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++k) {
+      const int q_row = a.cu_q_rows[plan_seq(sm.ub, a.batch, u)];
+      const int qb = k & 1;
+      if (k >= 2 && !warp_wait(&sm.q_free[qb], ((k >> 1) - 1) & 1, st)) break;
+      // stage the bf16 rows in shared memory: all copies in flight at once
+      const uint16_t* gsrc = a.q + static_cast<int64_t>(q_row) * HQ * 512;
+      __syncwarp();  // the previous unit's reads of the stage are done
+      for (int c = lane; c < HQ * 64; c += 32) {
+        const int h = c >> 6, c8 = c & 63;
+        cp_async16(sm.qstage + h * SM::kStageRow + c8 * 16, gsrc + h * 512 + c8 * 8);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      __syncwarp();
+      auto srow = [&](int h) { return reinterpret_cast<const uint16_t*>(sm.qstage + h * SM::kStageRow); };
+      // pass 1: largest |q| of each head (lane h keeps head h's)
+      float my_scale = 1.f;
+#pragma unroll 4
+      for (int h = 0; h < HQ; ++h) {
+        float x[8], y[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(srow(h) + 16 * lane), x);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(srow(h) + 16 * lane + 8), y);
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fmaxf(fabsf(x[i]), fabsf(y[i])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == h) {
+          // e = 7 - floor(log2 m), clamped so that 2^e and 2^-e are normal floats
+          const int ex = m > 0.f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xFF) - 127 : 7;
+          const int e = min(125, max(-125, 7 - ex));
+          my_scale = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+          sm.qscale[k & 3][h] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+        }
+      }
+      // pass 2: lane (h & 7, cb >> 2 ... ) converts 16 dims of one head; the 8
+      // heads of a block go to 8 different 16-byte bank groups
+      uint8_t* qhi = sm.q[qb];
+      uint8_t* qlo = sm.q[qb] + HQ * 512;
+#pragma unroll 1
+      for (int hb = 0; hb < HQ / 8; ++hb) {
+        const int h = 8 * hb + (lane & 7);
+        const float sc = __shfl_sync(0xffffffffu, my_scale, h);
+#pragma unroll 2
+        for (int j = 0; j < 8; ++j) {
+          const int cb = 4 * j + (lane >> 3);
+          float x[16];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(srow(h) + 16 * cb), *reinterpret_cast<float(*)[8]>(x));
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(srow(h) + 16 * cb + 8), *reinterpret_cast<float(*)[8]>(x + 8));
+          uint32_t whi[4], wlo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t hw = 0, lw = 0;
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const float a0 = x[4 * i + 2 * jj] * sc, a1 = x[4 * i + 2 * jj + 1] * sc;
+              const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+              const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E4M3)));
+              const __nv_fp8x2_storage_t lo2 =
+                  __nv_cvt_float2_to_fp8x2(make_float2(a0 - hf.x, a1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+              hw |= static_cast<uint32_t>(hi2) << (16 * jj);
+              lw |= static_cast<uint32_t>(lo2) << (16 * jj);
+            }
+            whi[i] = hw;
+            wlo[i] = lw;
+          }
+          const int off = ((h >> 3) * 32 + cb) * 128 + (h & 7) * 16;
+          *reinterpret_cast<uint4*>(qhi + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+          *reinterpret_cast<uint4*>(qlo + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.q_ready[qb]);
+        mbar_arrive(&sm.qs_ready[k & 3]);
+        const int un = u + gridDim.x;
+        if (un < total_units)
+          prefetch_l2(a.q + static_cast<int64_t>(a.cu_q_rows[plan_seq(sm.ub, a.batch, un)]) * HQ * 512, HQ * 1024);
+      }
     }
   } else if (warp == 6) {
     // -------------------------------------------------------------- q loader
@@ -360,18 +519,18 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     int k = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++k) {
       const int q_row = a.cu_q_rows[plan_seq(sm.ub, a.batch, u)];
-      if (k > 0 && !warp_wait(&sm.q_free, (k - 1) & 1, st)) break;
+      if (k > 0 && !warp_wait(&sm.q_free[0], (k - 1) & 1, st)) break;
       const uint16_t* src = a.q + static_cast<int64_t>(q_row) * HQ * 512;
       for (int c = lane; c < HQ * 64; c += 32) {
         const int h = c >> 6, cb = c & 63;
-        cp_async16(sm.q + (((h >> 3) * 64 + cb) * 128 + (h & 7) * 16), src + h * 512 + cb * 8);
+        cp_async16(sm.q[0] + (((h >> 3) * 64 + cb) * 128 + (h & 7) * 16), src + h * 512 + cb * 8);
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
       asm volatile("cp.async.wait_group 0;" ::: "memory");
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&sm.q_ready);
+        mbar_arrive(&sm.q_ready[0]);
         const int un = u + gridDim.x;
         if (un < total_units)
           prefetch_l2(a.q + static_cast<int64_t>(a.cu_q_rows[plan_seq(sm.ub, a.batch, un)]) * HQ * 512, HQ * 1024);
@@ -398,6 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       if (d.flags & kEnd) break;
       const bool first = d.flags & kFirst;
       if (first) ++uidx;
+      // e4m3: the unit's per-head descale of q is published with qs_ready
+      if (kE4 && first && !mbar_wait(&sm.qs_ready[uidx & 3], (uidx >> 2) & 1, st)) break;
       if (!mbar_wait(&sm.s_ready[n & 1], (n >> 1) & 1, st)) break;
       tc::fence_after();
       uint32_t r[32];
@@ -410,7 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       bool need = false;
 #pragma unroll
       for (int h = 0; h < HQ; ++h) {
-        s[h] = valid ? __uint_as_float(r[h]) * a.scale_log2 : -INFINITY;
+        const float sc = kE4 ? sm.qscale[uidx & 3][h] * a.scale_log2 : a.scale_log2;
+        s[h] = valid ? __uint_as_float(r[h]) * sc : -INFINITY;
         need |= s[h] > m_run[h] + kLazyThreshold;
       }
       // A thread asking for a new max tags the flag of this tile's parity
@@ -464,7 +626,44 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       }
       // ---- P^T (bf16) for this tile; wait until P.V two tiles back released the buffer
       if (n >= 2 && !mbar_wait(&sm.pfree[n & 1], ((n >> 1) - 1) & 1, st)) break;
-      if (active) {
+      if (active && kE4) {
+        // P = P_hi + P_lo, two e4m3 terms (P <= 2^8 under the lazy max); l
+        // sums exactly the weights the contraction uses
+        uint8_t* phi = sm.p[n & 1] + ((t >> 3) * (NP / 16)) * 128 + (t & 7) * 16;
+        uint8_t* plo = phi + 64 * NP;
+#pragma unroll
+        for (int hb = 0; hb < NP / 16; ++hb) {
+          uint32_t whi[4], wlo[4];
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            uint32_t hw = 0, lw = 0;
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const int h0 = hb * 16 + 4 * k4 + 2 * jj;
+              const int i0 = h0 < HQ ? h0 : 0, i1 = h0 + 1 < HQ ? h0 + 1 : 0;
+              const float p0 = (valid && h0 < HQ) ? ex2(s[i0] - m_run[i0]) : 0.f;
+              const float p1 = (valid && h0 + 1 < HQ) ? ex2(s[i1] - m_run[i1]) : 0.f;
+              const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
+              const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi2, __NV_E4M3)));
+              const __nv_fp8x2_storage_t lo2 =
+                  __nv_cvt_float2_to_fp8x2(make_float2(p0 - hf.x, p1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+              const float2 lf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo2, __NV_E4M3)));
+              if (h0 < HQ) l_acc[i0] += hf.x + lf.x;
+              if (h0 + 1 < HQ) l_acc[i1] += hf.y + lf.y;
+              hw |= static_cast<uint32_t>(hi2) << (16 * jj);
+              lw |= static_cast<uint32_t>(lo2) << (16 * jj);
+            }
+            whi[k4] = hw;
+            wlo[k4] = lw;
+          }
+          *reinterpret_cast<uint4*>(phi + hb * 128) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+          *reinterpret_cast<uint4*>(plo + hb * 128) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+        }
+        if (pvalid && tabs >= d.L) {
+          uint8_t* row = sm.tiles[b][j] + (lane >> 3) * T::kBlk * 128 + (lane & 7) * 16;
+          for (int cb = 0; cb < T::kBlk; ++cb) *reinterpret_cast<uint4*>(row + cb * 128) = make_uint4(0, 0, 0, 0);
+        }
+      } else if (active) {
         uint8_t* pdst = sm.p[n & 1] + ((t >> 3) * (NP / 8)) * 128 + (t & 7) * 16;
 #pragma unroll
         for (int hb = 0; hb < HQ / 8; ++hb) {
@@ -543,7 +742,7 @@ cudaError_t launch_layout(const LocalArgs& a, cudaStream_t stream) {
   // Dropping the merged partials from L2 unwritten pays for the folded pool
   // (24.7 vs 26.9 us per serving call) but not for the full control (427 vs
   // 415 us per long-context call), measured.
-  return launch_combine(a, HQ, 512, global_max_chunks(a.max_pages), LAYOUT == GW_LAYOUT_GLOBAL_FOLDED, stream);
+  return launch_combine(a, HQ, 512, global_max_chunks(a.max_pages), LAYOUT != GW_LAYOUT_GLOBAL_FULL, stream);
 }
 
 template <int LAYOUT>
@@ -559,6 +758,7 @@ cudaError_t launch_hq(const LocalArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_global_decode(int layout, const LocalArgs& a, cudaStream_t stream) {
+  if (layout == GW_LAYOUT_GLOBAL_FOLDED_E4M3) return launch_hq<GW_LAYOUT_GLOBAL_FOLDED_E4M3>(a, stream);
   return layout == GW_LAYOUT_GLOBAL_FOLDED ? launch_hq<GW_LAYOUT_GLOBAL_FOLDED>(a, stream)
                                            : launch_hq<GW_LAYOUT_GLOBAL_FULL>(a, stream);
 }

@@ -43,12 +43,19 @@ gw_status check_pool(const gw_kv_pool* p, const char* fn, bool need_base = true)
     if (p->head_dim != 256 || p->rot_dim != 256)
       return fail(GW_ERR_INVALID_ARG, fn, "local pool needs head_dim 256 and rot_dim 256");
     if (p->kv_heads < 1 || p->kv_heads > 64) return fail(GW_ERR_INVALID_ARG, fn, "kv_heads must be in [1, 64]");
-  } else if (p->layout == GW_LAYOUT_GLOBAL_FOLDED || p->layout == GW_LAYOUT_GLOBAL_FULL) {
+  } else if (p->layout == GW_LAYOUT_GLOBAL_FOLDED || p->layout == GW_LAYOUT_GLOBAL_FULL ||
+             p->layout == GW_LAYOUT_GLOBAL_FOLDED_E4M3) {
     if (p->head_dim != 512 || p->rot_dim != 128)
       return fail(GW_ERR_INVALID_ARG, fn, "global pool needs head_dim 512 and rot_dim 128");
     if (p->kv_heads != 1) return fail(GW_ERR_INVALID_ARG, fn, "global pool has exactly one KV head");
-    if (p->dtype != GW_KV_BF16)
-      return fail(GW_ERR_UNSUPPORTED, fn, "e4m3 KV supports only local (sliding) layers");
+    if (p->layout == GW_LAYOUT_GLOBAL_FOLDED_E4M3) {
+      if (p->dtype != GW_KV_E4M3)
+        return fail(GW_ERR_INVALID_ARG, fn, "layout GLOBAL_FOLDED_E4M3 needs dtype e4m3");
+    } else if (p->dtype != GW_KV_BF16) {
+      return fail(GW_ERR_UNSUPPORTED, fn,
+                  "e4m3 KV supports only local (sliding) layers; the opt-in e4m3 global pool is layout "
+                  "GLOBAL_FOLDED_E4M3");
+    }
   } else {
     return fail(GW_ERR_INVALID_ARG, fn, "unknown layout %d", p->layout);
   }
@@ -57,6 +64,7 @@ gw_status check_pool(const gw_kv_pool* p, const char* fn, bool need_base = true)
 
 size_t page_bytes(const gw_kv_pool* p) {
   if (p->layout == GW_LAYOUT_LOCAL) return static_cast<size_t>(p->kv_heads) * 2 * 16 * 256 * (p->dtype == GW_KV_BF16 ? 2 : 1);
+  if (p->layout == GW_LAYOUT_GLOBAL_FOLDED_E4M3) return 16 * 640;
   return p->layout == GW_LAYOUT_GLOBAL_FOLDED ? 16 * 640 * 2 : 16 * 1024 * 2;
 }
 
@@ -175,6 +183,20 @@ gw_status gw_kv_append(const gw_kv_pool* pool, const void* k, const void* v, int
   return cuda_status(launch_append(pool->layout, pool->dtype, a, static_cast<cudaStream_t>(stream)), fn);
 }
 
+gw_status gw_rope_cs(float* rope_cs, double theta, int32_t rot_dim, int32_t head_dim, int32_t max_pos,
+                     void* stream) {
+  const char* fn = "gw_rope_cs";
+  g_err[0] = 0;
+  if (!rope_cs || !aligned(rope_cs, 16)) return fail(GW_ERR_INVALID_ARG, fn, "rope_cs NULL or not 16-byte aligned");
+  if (!(theta > 0.0) || !std::isfinite(theta)) return fail(GW_ERR_INVALID_ARG, fn, "theta must be finite and > 0");
+  if (head_dim < 2 || rot_dim < 2 || rot_dim > head_dim || rot_dim % 2)
+    return fail(GW_ERR_INVALID_ARG, fn, "need an even rot_dim in [2, head_dim] (rot_dim %d, head_dim %d)", rot_dim,
+                head_dim);
+  if (max_pos < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_pos must be >= 1");
+  return cuda_status(launch_rope_cs(rope_cs, theta, rot_dim, head_dim, max_pos, static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
 size_t gw_attn_workspace_bytes(const gw_kv_pool* pool, int32_t num_q_heads, int32_t batch, int32_t max_seq_len,
                                int32_t max_q_rows, int32_t window) {
   (void)max_q_rows;
@@ -192,7 +214,7 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
                              int32_t num_q_heads, int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,
                              const int32_t* block_table, int32_t max_pages_per_seq, int32_t max_q_rows,
                              int32_t window, float scale, void* workspace, size_t workspace_bytes,
-                             int32_t* dev_status, void* stream) {
+                             int32_t* dev_status, void* stream, bool validate_only = false) {
   g_err[0] = 0;
   gw_status s = check_pool(pool, fn);
   if (s != GW_OK) return s;
@@ -214,7 +236,7 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(GW_ERR_INVALID_ARG, fn, "scale must be finite and > 0");
   if (max_pages_per_seq < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_pages_per_seq must be >= 1");
   if (max_q_rows < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_q_rows must be >= 1");
-  if (local && pool->dtype == GW_KV_E4M3 && max_q_rows > 1)
+  if (pool->dtype == GW_KV_E4M3 && max_q_rows > 1)
     return fail(GW_ERR_UNSUPPORTED, fn, "prompt rows (max_q_rows %d > 1) on an e4m3 pool: the prompt-row kernel "
                 "reads bf16 pages only", max_q_rows);
   if (!q || !out || !aligned(q, 16) || !aligned(out, 16)) return fail(GW_ERR_INVALID_ARG, fn, "q/out NULL or not 16-byte aligned");
@@ -229,6 +251,7 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
                                local ? window : 0);
   if (workspace_bytes < w.total)
     return fail(GW_ERR_WORKSPACE, fn, "workspace_bytes %zu < %zu needed", workspace_bytes, w.total);
+  if (validate_only) return GW_OK;
 
   LocalArgs a{};
   a.pool = static_cast<const uint8_t*>(pool->base);
@@ -272,6 +295,23 @@ gw_status gw_decode_attn_local(const gw_kv_pool* pool, const void* q, void* out,
                      max_pages_per_seq, max_q_rows, window, scale, workspace, workspace_bytes, dev_status, stream);
 }
 
+}  // extern "C"
+
+namespace gw {
+gw_status validate_local_call(const char* fn, const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,
+                              int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,
+                              const int32_t* block_table, int32_t max_pages_per_seq, int32_t max_q_rows,
+                              int32_t window, float scale, size_t workspace_bytes, int32_t* dev_status) {
+  // Any 256-byte aligned non-null address stands in for the workspace: only
+  // its size is checked, and nothing is launched.
+  return attn_common(fn, true, pool, q, out, num_q_heads, batch, cu_q_rows, seq_lens, block_table, max_pages_per_seq,
+                     max_q_rows, window, scale, reinterpret_cast<void*>(static_cast<uintptr_t>(256)), workspace_bytes,
+                     dev_status, nullptr, true);
+}
+}  // namespace gw
+
+extern "C" {
+
 gw_status gw_decode_attn_global(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads, int32_t batch,
                                 const int32_t* cu_q_rows, const int32_t* seq_lens, const int32_t* block_table,
                                 int32_t max_pages_per_seq, int32_t max_q_rows, float scale, void* workspace,
@@ -309,6 +349,29 @@ gw_status gw_bw_probe(const void* buf, size_t bytes, int32_t* dev_status, void* 
   return cuda_status(launch_bw_probe(buf, static_cast<int64_t>(bytes / 8192), dev_status,
                                      static_cast<cudaStream_t>(stream)),
                      fn);
+}
+
+gw_status gw_bw_probe_tma(const void* buf, size_t bytes, int32_t* dev_status, void* stream) {
+  const char* fn = "gw_bw_probe_tma";
+  g_err[0] = 0;
+  if (!buf || !aligned(buf, 256)) return fail(GW_ERR_INVALID_ARG, fn, "buf NULL or not 256-byte aligned");
+  if (bytes < 16384) return fail(GW_ERR_INVALID_ARG, fn, "bytes (%zu) < 16384", bytes);
+  if (bytes / 16384 > (static_cast<size_t>(1) << 22))  // tensor-map rows stay below 2^31
+    return fail(GW_ERR_INVALID_ARG, fn, "bytes (%zu) above 2^36", bytes);
+  if (dev_status && !aligned(dev_status, 4)) return fail(GW_ERR_INVALID_ARG, fn, "dev_status misaligned");
+  return cuda_status(launch_bw_probe_tma(buf, static_cast<int64_t>(bytes / 16384), dev_status,
+                                         static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+gw_status gw_wait_selftest(int32_t* dev_status, int32_t* result, int64_t limit_ns, void* stream) {
+  const char* fn = "gw_wait_selftest";
+  g_err[0] = 0;
+  if (!dev_status || !aligned(dev_status, 4)) return fail(GW_ERR_INVALID_ARG, fn, "dev_status NULL or misaligned");
+  if (!result || !aligned(result, 4)) return fail(GW_ERR_INVALID_ARG, fn, "result NULL or misaligned");
+  if (limit_ns < 1000 || limit_ns > 1000000000)
+    return fail(GW_ERR_INVALID_ARG, fn, "limit_ns (%lld) outside [1e3, 1e9]", static_cast<long long>(limit_ns));
+  return cuda_status(launch_wait_selftest(dev_status, result, limit_ns, static_cast<cudaStream_t>(stream)), fn);
 }
 
 }  // extern "C"

@@ -144,6 +144,7 @@ cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream
 // (cos, sin) table of gw_rope_cs: float32 [max_pos][rot_dim / 2][2].
 cudaError_t launch_rope_cs(float* out, double theta, int rot_dim, int head_dim, int max_pos, cudaStream_t st);
 cudaError_t launch_bw_probe(const void* buf, int64_t chunks, int32_t* status, cudaStream_t st);
+cudaError_t launch_bw_probe_tma(const void* buf, int64_t pages, int32_t* status, cudaStream_t st);
 cudaError_t launch_wait_selftest(int32_t* status, int32_t* result, int64_t limit_ns, cudaStream_t st);
 // TMA descriptor of a bf16 LOCAL pool (rows of 256 elements in 4 chunks of 64;
 // row = ((page * kv_heads + head) * 2 + {K, V}) * 16 + token), box {64, 1, 16},

@@ -165,13 +165,21 @@ __device__ __forceinline__ int64_t tiled(int64_t page, int o, int e) {
   return page * (kPage * kRow) + ((static_cast<int64_t>(o / 8) * kBlk + e / 8) * 8 + (o % 8)) * 8 + (e % 8);
 }
 
+// Byte offset of (page, token o, row element e) in a GLOBAL_FOLDED_E4M3 page:
+// rows of 640 one-byte elements, blocked 8 tokens x 16 elements.
+__device__ __forceinline__ int64_t tiled_e4m3(int64_t page, int o, int e) {
+  return page * (kPage * 640) + ((static_cast<int64_t>(o / 8) * 40 + e / 16) * 8 + (o % 8)) * 16 + (e % 16);
+}
+
 // GLOBAL FOLDED: row = V[0:512] || k_rot[0:128]; items per row: 64 V chunks
-// + 8 rotation items (pairs 8t..8t+7 and 64+8t..).
+// + 8 rotation items (pairs 8t..8t+7 and 64+8t..).  The e4m3 folded pool has
+// the same items, each rounding its 8 elements once to e4m3 (8-byte stores).
 // GLOBAL FULL:   row = K[0:512] || V[0:512]; items per row: 8 rotation items,
 // 48 copies of k[128:512], 64 V chunks.
 template <int LAYOUT>
 __global__ void append_global_kernel(const AppendArgs a) {
-  constexpr bool kFolded = LAYOUT == GW_LAYOUT_GLOBAL_FOLDED;
+  constexpr bool kE4 = LAYOUT == GW_LAYOUT_GLOBAL_FOLDED_E4M3;
+  constexpr bool kFolded = LAYOUT == GW_LAYOUT_GLOBAL_FOLDED || kE4;
   constexpr int kRow = kFolded ? 640 : 1024;
   constexpr int kItems = kFolded ? 72 : 120;
   PdlGate gate(a);
@@ -203,8 +211,17 @@ __global__ void append_global_kernel(const AppendArgs a) {
       load_bf16x8(krow + 64 + 8 * t, x1);
       rotate8(x0, x1, cs);
       const int e0 = kFolded ? 512 + 8 * t : 8 * t;
-      *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, e0)) = f32x8_to_bf16(x0);
-      *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, e0 + 64)) = f32x8_to_bf16(x1);
+      if constexpr (kE4) {
+        *reinterpret_cast<uint2*>(a.pool + tiled_e4m3(page, off, e0)) = f32x8_to_e4m3(x0);
+        *reinterpret_cast<uint2*>(a.pool + tiled_e4m3(page, off, e0 + 64)) = f32x8_to_e4m3(x1);
+      } else {
+        *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, e0)) = f32x8_to_bf16(x0);
+        *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, e0 + 64)) = f32x8_to_bf16(x1);
+      }
+    } else if (kE4) {  // V chunk it in [0, 64), rounded to e4m3
+      float x[8];
+      load_bf16x8(vrow + 8 * it, x);
+      *reinterpret_cast<uint2*>(a.pool + tiled_e4m3(page, off, 8 * it)) = f32x8_to_e4m3(x);
     } else if (kFolded) {  // V chunk it in [0, 64)
       *reinterpret_cast<uint4*>(pool + tiled<kRow>(page, off, 8 * it)) =
           *reinterpret_cast<const uint4*>(vrow + 8 * it);
@@ -219,6 +236,22 @@ __global__ void append_global_kernel(const AppendArgs a) {
   }
 }
 
+// One (cos, sin) entry per item: item w = pos * half + i.  The frequency,
+// the angle and both trigonometric values are float64; each value is rounded
+// once to float32.
+__global__ void rope_cs_kernel(float2* out, double theta, int half, int head_dim, int64_t total) {
+  for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
+       w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(w % half);
+    const int64_t p = w / half;
+    const double inv_f = pow(theta, (-2.0 * static_cast<double>(i)) / static_cast<double>(head_dim));
+    const double ang = static_cast<double>(p) * inv_f;
+    double s, c;
+    sincos(ang, &s, &c);
+    out[w] = make_float2(__double2float_rn(c), __double2float_rn(s));
+  }
+}
+
 int grid_for(int64_t items, int block) {
   int64_t blocks = (items + block - 1) / block;
   const int64_t cap = static_cast<int64_t>(grid_ctas()) * 16;
@@ -227,6 +260,13 @@ int grid_for(int64_t items, int block) {
 
 }  // namespace
 
+cudaError_t launch_rope_cs(float* out, double theta, int rot_dim, int head_dim, int max_pos, cudaStream_t st) {
+  constexpr int kBlock = 256;
+  const int64_t total = static_cast<int64_t>(max_pos) * (rot_dim / 2);
+  return launch_pdl(rope_cs_kernel, dim3(grid_for(total, kBlock)), dim3(kBlock), 0, st, reinterpret_cast<float2*>(out),
+                    theta, rot_dim / 2, head_dim, total);
+}
+
 cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream_t st) {
   constexpr int kBlock = 256;
   if (layout == GW_LAYOUT_LOCAL) {
@@ -234,6 +274,9 @@ cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream
     if (dtype == GW_KV_BF16) return launch_pdl(append_local_kernel<GW_KV_BF16>, dim3(grid), dim3(kBlock), 0, st, a);
     return launch_pdl(append_local_kernel<GW_KV_E4M3>, dim3(grid), dim3(kBlock), 0, st, a);
   }
+  if (layout == GW_LAYOUT_GLOBAL_FOLDED_E4M3)
+    return launch_pdl(append_global_kernel<GW_LAYOUT_GLOBAL_FOLDED_E4M3>,
+                      dim3(grid_for(static_cast<int64_t>(a.num_rows) * 72, kBlock)), dim3(kBlock), 0, st, a);
   if (layout == GW_LAYOUT_GLOBAL_FOLDED)
     return launch_pdl(append_global_kernel<GW_LAYOUT_GLOBAL_FOLDED>,
                       dim3(grid_for(static_cast<int64_t>(a.num_rows) * 72, kBlock)), dim3(kBlock), 0, st, a);

@@ -24,13 +24,14 @@ GW_OK, GW_ERR_INVALID_ARG, GW_ERR_UNSUPPORTED, GW_ERR_WORKSPACE, GW_ERR_CUDA = 0
 GW_DEV_SLOT_RANGE, GW_DEV_POS_RANGE, GW_DEV_PAGE_RANGE, GW_DEV_LEN_RANGE = 1, 2, 4, 8
 GW_DEV_TIMEOUT, GW_DEV_WORKSPACE = 16, 32
 KV_BF16, KV_E4M3 = 0, 1
-LAYOUT_LOCAL, LAYOUT_GLOBAL_FOLDED, LAYOUT_GLOBAL_FULL = 0, 1, 2
-LAYOUTS = {"local": LAYOUT_LOCAL, "folded": LAYOUT_GLOBAL_FOLDED, "full": LAYOUT_GLOBAL_FULL}
+LAYOUT_LOCAL, LAYOUT_GLOBAL_FOLDED, LAYOUT_GLOBAL_FULL, LAYOUT_GLOBAL_FOLDED_E4M3 = 0, 1, 2, 3
+LAYOUTS = {"local": LAYOUT_LOCAL, "folded": LAYOUT_GLOBAL_FOLDED, "full": LAYOUT_GLOBAL_FULL,
+           "folded_e4m3": LAYOUT_GLOBAL_FOLDED_E4M3}
 DTYPES = {"bf16": KV_BF16, "e4m3": KV_E4M3}
 EXPORTS = ["gw_pool_page_bytes", "gw_kv_append", "gw_decode_attn_local", "gw_decode_attn_global",
            "gw_attn_workspace_bytes", "gw_last_error", "gw_version", "gw_decode_attn_local_noalloc",
            "gw_noalloc_scratch_bytes", "gw_bw_probe", "gw_set_max_ctas", "gw_set_early_launch",
-           "gw_set_early_inputs"]
+           "gw_set_early_inputs", "gw_rope_cs", "gw_wait_selftest", "gw_bw_probe_tma"]
 
 
 class GwError(RuntimeError):
@@ -57,6 +58,8 @@ _lib.gw_decode_attn_local.restype = _i32
 _lib.gw_decode_attn_global.argtypes = [_P, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _sz,
                                        _vp, _vp]
 _lib.gw_decode_attn_global.restype = _i32
+_lib.gw_rope_cs.argtypes = [_vp, ctypes.c_double, _i32, _i32, _i32, _vp]
+_lib.gw_rope_cs.restype = _i32
 _lib.gw_attn_workspace_bytes.argtypes = [_P, _i32, _i32, _i32, _i32, _i32]
 _lib.gw_attn_workspace_bytes.restype = _sz
 _lib.gw_decode_attn_local_noalloc.argtypes = [_P, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _f32,
@@ -66,6 +69,10 @@ _lib.gw_noalloc_scratch_bytes.argtypes = []
 _lib.gw_noalloc_scratch_bytes.restype = _sz
 _lib.gw_bw_probe.argtypes = [_vp, _sz, _vp, _vp]
 _lib.gw_bw_probe.restype = _i32
+_lib.gw_bw_probe_tma.argtypes = [_vp, _sz, _vp, _vp]
+_lib.gw_bw_probe_tma.restype = _i32
+_lib.gw_wait_selftest.argtypes = [_vp, _vp, _i64, _vp]
+_lib.gw_wait_selftest.restype = _i32
 _lib.gw_set_max_ctas.argtypes = [_i32]
 _lib.gw_set_max_ctas.restype = _i32
 _lib.gw_set_early_launch.argtypes = [_i32]
@@ -131,16 +138,13 @@ class KVPool:
         return self.num_pages * self.page_bytes
 
 
-def rope_table(theta, rot_dim, head_dim, max_pos):
-    """float32 [max_pos, rot_dim/2, 2] (cos, sin) table, float64 math rounded once.
-
-    inv_f_i = theta^(-2 i / head_dim) for i < rot_dim/2 (the full head dim is the
-    frequency denominator also when only a slice rotates); angle = pos * inv_f_i.
-    """
-    i = torch.arange(rot_dim // 2, dtype=torch.float64)
-    inv_f = torch.pow(torch.tensor(float(theta), dtype=torch.float64), -2.0 * i / float(head_dim))
-    ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * inv_f[None, :]
-    return torch.stack([torch.cos(ang), torch.sin(ang)], dim=-1).to(torch.float32).contiguous()
+def rope_cs(theta, rot_dim, head_dim, max_pos, out=None, device="cuda", stream=None):
+    """gw_rope_cs: the float32 [max_pos, rot_dim/2, 2] (cos, sin) table of
+    gw_kv_append, computed by the library on the GPU (into `out` if given)."""
+    if out is None:
+        out = torch.empty((max_pos, rot_dim // 2, 2), dtype=torch.float32, device=device)
+    _check(_lib.gw_rope_cs(_ptr(out), float(theta), int(rot_dim), int(head_dim), int(max_pos), _stream(stream)))
+    return out
 
 
 # ---- entry points ------------------------------------------------------------------
@@ -220,3 +224,16 @@ def set_early_inputs(on):
 def bw_probe(buf, dev_status=None, stream=None):
     """gw_bw_probe: stream `buf` (a CUDA tensor) through the decode kernels' copy pipeline."""
     _check(_lib.gw_bw_probe(_ptr(buf), int(buf.numel() * buf.element_size()), _ptr(dev_status), _stream(stream)))
+
+
+def bw_probe_tma(buf, dev_status=None, stream=None):
+    """gw_bw_probe_tma: stream `buf` through the bf16 decode kernel's tensor-map copy pipeline."""
+    _check(_lib.gw_bw_probe_tma(_ptr(buf), int(buf.numel() * buf.element_size()), _ptr(dev_status),
+                                _stream(stream)))
+
+
+def wait_selftest(dev_status, result, limit_ns, stream=None):
+    """gw_wait_selftest: run the kernels' bounded wait on a phase nothing
+    completes, with a limit of limit_ns; result (int32[3] on the device)
+    receives {first wait ok, second wait gave up, microseconds waited}."""
+    _check(_lib.gw_wait_selftest(_ptr(dev_status), _ptr(result), int(limit_ns), _stream(stream)))

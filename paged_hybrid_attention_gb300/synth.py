@@ -15,7 +15,8 @@ layers per global layer):
               heads, window 1024, bf16; global folded; 5 local + 1 global.
   fp8_local   64 sequences, L ~ U[4096, 32768], local only, e4m3 pool, values
               N(0, 0.5) (the clip at +-448 never binds); bf16 control.
-  long_global 8 slots at L = 131072, global only, folded vs full control.
+  long_global 8 slots at L = 131072, global only, folded vs full control,
+              and the opt-in e4m3 folded pool of the same tokens.
   mixed       48 decode streams, L ~ U[1024, 16384], plus 4 new prompts of 2048
               rows appended and attended in the same step; both families.
   chunked     32 decode streams, L ~ U[1024, 16384], plus 4 prompts continuing
@@ -78,7 +79,7 @@ def spec(name):
         loc = Family("local", "bf16", "local", 4, 256, 256, 1e4, 32)
         glo = Family("global", "bf16", "folded", 1, 512, 128, 1e4, 0)
         return Spec(name, 1001, 8, np.array([37, 100], np.int32), np.ones(2, np.int32),
-                    {"local": loc, "global": glo, "global_full": _full(glo)}, 1, 1)
+                    {"local": loc, "global": glo, "global_full": _full(glo), "global_e4m3": _e4m3(glo)}, 1, 1)
     if name == "serving":
         lens = _draw_lens(1002, 16, 512, 8192)
         loc = Family("local", "bf16", "local", 16, 256, 256, 1e4, 1024)
@@ -95,7 +96,7 @@ def spec(name):
         lens = np.full(8, 131072, np.int32)
         glo = Family("global", "bf16", "folded", 1, 512, 128, 1e6, 0)
         return Spec(name, 1004, 32, lens, np.ones(8, np.int32),
-                    {"global": glo, "global_full": _full(glo)}, 0, 1)
+                    {"global": glo, "global_full": _full(glo), "global_e4m3": _e4m3(glo)}, 0, 1)
     if name == "mixed":
         dec = _draw_lens(1005, 48, 1024, 16384)
         lens = np.concatenate([dec, np.full(4, 2048, np.int32)]).astype(np.int32)
@@ -123,6 +124,12 @@ def spec(name):
 
 def _full(fam):
     return Family(fam.kind, fam.dtype, "full", fam.kv_heads, fam.head_dim, fam.rot_dim,
+                  fam.theta, fam.window, fam.sigma)
+
+
+def _e4m3(fam):
+    """The opt-in e4m3 folded pool of a global family (same tokens)."""
+    return Family(fam.kind, "e4m3", "folded_e4m3", fam.kv_heads, fam.head_dim, fam.rot_dim,
                   fam.theta, fam.window, fam.sigma)
 
 
@@ -252,4 +259,4 @@ class Layer:
 
 
 def _fam_id(key):
-    return {"local": 1, "global": 2, "global_full": 2, "local_bf16": 1}[key]
+    return {"local": 1, "global": 2, "global_full": 2, "local_bf16": 1, "global_e4m3": 2}[key]

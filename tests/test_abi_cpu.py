@@ -43,6 +43,24 @@ def test_page_bytes_and_bad_descriptions():
     assert L.gw_pool_page_bytes(ctypes.byref(_desc(base=0))) == 16 * 16384   # size query before allocation
     assert L.gw_pool_page_bytes(ctypes.byref(_desc(gw.LAYOUT_GLOBAL_FOLDED, gw.KV_E4M3, kvh=1, hd=512, rd=128))) == 0
     assert "supports only local" in gw.last_error()
+    # the opt-in e4m3 folded layout: 16 x 640 bytes, and only with dtype e4m3
+    e8 = _desc(gw.LAYOUT_GLOBAL_FOLDED_E4M3, gw.KV_E4M3, kvh=1, hd=512, rd=128)
+    assert L.gw_pool_page_bytes(ctypes.byref(e8)) == 10240
+    assert L.gw_pool_page_bytes(ctypes.byref(_desc(gw.LAYOUT_GLOBAL_FOLDED_E4M3, kvh=1, hd=512, rd=128))) == 0
+    assert "needs dtype e4m3" in gw.last_error()
+
+
+def test_e4m3_global_opt_in_validation():
+    L = gw.lib()
+    f = _fake()
+    e8 = _desc(gw.LAYOUT_GLOBAL_FOLDED_E4M3, gw.KV_E4M3, kvh=1, hd=512, rd=128)
+    call = lambda mq: L.gw_decode_attn_global(ctypes.byref(e8), f, f, 32, 2, f, f, f, 64, mq, 0.04,
+                                              _fake(1 << 28), 1 << 30, None, None)
+    assert call(2) == gw.GW_ERR_UNSUPPORTED and "prompt rows" in gw.last_error()
+    assert L.gw_attn_workspace_bytes(ctypes.byref(e8), 32, 8, 131072, 1, 0) == \
+        L.gw_attn_workspace_bytes(ctypes.byref(_desc(gw.LAYOUT_GLOBAL_FOLDED, kvh=1, hd=512, rd=128)), 32, 8,
+                                  131072, 1, 0)
+    assert _local_call(e8) == gw.GW_ERR_INVALID_ARG               # a global pool on the local entry
 
 
 def _fake(n=1 << 24):
@@ -169,3 +187,11 @@ def test_noalloc_refusals_need_no_gpu():
     assert rc == gw.GW_ERR_UNSUPPORTED and "4096" in gw.last_error()
     assert L.gw_decode_attn_local_noalloc(ctypes.byref(d), f, f, 32, 0, f, f, f, 512, 1, 1024, 0.0625, None,
                                           None) == gw.GW_OK
+
+
+def test_bw_probe_tma_host_validation():
+    L = gw.lib()
+    assert L.gw_bw_probe_tma(None, 1 << 20, None, None) == gw.GW_ERR_INVALID_ARG
+    assert gw.last_error().startswith("gw_bw_probe_tma:")
+    assert L.gw_bw_probe_tma(_fake((1 << 24) + 16), 1 << 20, None, None) == gw.GW_ERR_INVALID_ARG  # not 256-aligned
+    assert L.gw_bw_probe_tma(_fake(), 8192, None, None) == gw.GW_ERR_INVALID_ARG                   # < one stage

@@ -33,7 +33,7 @@ def _pools(layer, seqs=None, part="all"):
     return pool.data.cpu().numpy(), ref
 
 
-@pytest.mark.parametrize("key", ["local", "global", "global_full"])
+@pytest.mark.parametrize("key", ["local", "global", "global_full", "global_e4m3"])
 def test_append_tiny_bit_exact(key):
     layer = synth.Layer(synth.spec("tiny"), key)
     got, ref = _pools(layer)
@@ -75,7 +75,7 @@ def test_append_e4m3_saturates_and_rounds_ties():
 @pytest.mark.parametrize("name,key,sample", [
     ("serving", "local", None), ("serving", "global", None),
     ("fp8_local", "local", [0, 17, 40, 63]), ("fp8_local", "local_bf16", [5, 33]),
-    ("long_global", "global", [3]), ("long_global", "global_full", [6]),
+    ("long_global", "global", [3]), ("long_global", "global_full", [6]), ("long_global", "global_e4m3", [1]),
     ("mixed", "local", list(range(44, 52))), ("mixed", "global", [0, 48, 51]),
 ])
 def test_append_full_size_bit_exact(name, key, sample):

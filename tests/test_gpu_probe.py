@@ -25,3 +25,13 @@ def test_bw_probe_rejects_bad_arguments():
     assert e.value.code == gw.GW_ERR_INVALID_ARG and "8192" in str(e.value)
     with pytest.raises(gw.GwError):
         gw.bw_probe(buf[1:9000])
+
+
+def test_bw_probe_tma_runs_and_reports_no_timeout():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    buf = torch.zeros((1 << 24) + 256, dtype=torch.uint8, device="cuda")
+    off = (-buf.data_ptr()) % 256
+    gw.bw_probe_tma(buf[off:off + (1 << 24)], status)
+    gw.bw_probe_tma(buf[off:off + 16384 * 5 + 300], status)   # a ragged tail is ignored
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
