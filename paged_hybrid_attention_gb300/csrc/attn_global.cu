@@ -21,7 +21,14 @@
 // commits each page's MMAs to that slot's barrier and the producer refills
 // the slot at once.  The folded layout double-buffers its tiles, so one tile
 // streams in while the other is computed; the full K+V control layout, whose
-// pages are 1.6x larger, has room for one tile only.  (One 128-token tile of
+// pages are 1.6x larger, has room for one tile only; the e4m3 folded layout,
+// whose pages are half the size, keeps three tiles in flight.
+//
+// On the e4m3 folded pool the same contractions run as kind::f8f6f4 MMAs
+// straight on the stored tiles (K = 32 per MMA): q enters as two e4m3 terms
+// [q_hi; q_lo] stacked along N (one MMA of N = 2 HQ per K-step, the softmax
+// adds the two logit columns), and P as two e4m3 terms accumulated into O by
+// two MMAs per K-step.  (One 128-token tile of
 // eight slots halves the MMAs per byte but leaves nothing streaming during
 // QK^T and the softmax, and was slower.)
 //
@@ -84,7 +91,7 @@ struct GTraits<GW_LAYOUT_GLOBAL_FOLDED_E4M3> {
   static constexpr bool kE4 = true;
   static constexpr int kPageBytes = 10240;
   static constexpr int kBlk = 40;
-  static constexpr int kNumBuf = 2;
+  static constexpr int kNumBuf = 3;
   static constexpr int kVcb = 0;
   static constexpr int kKSteps = 16;
   // column block holding K dims [32 ks, 32 ks + 32): k_rot (elements
@@ -104,10 +111,11 @@ template <int LAYOUT, int HQ>
 struct GSmem {
   using T = GTraits<LAYOUT>;
   static constexpr int kNP = HQ < 16 ? 16 : HQ;  // P.V N (M=128 needs N % 16 == 0)
-  // Q buffers: one for bf16 pools (written once the previous unit's last
-  // QK^T has completed); two for the e4m3 pool, whose q is converted on chip
-  // and so is prepared while the previous unit still runs.
-  static constexpr int kQBuf = T::kE4 ? 2 : 1;
+  // One Q buffer, written once the previous unit's last QK^T has completed.
+  // (The e4m3 pool spends the room a second buffer would take on a third
+  // tile buffer: 198 vs 216 us per 8 x 131072-token call.  Its loader stages
+  // and scales the next unit's q before waiting for the buffer.)
+  static constexpr int kQBuf = 1;
   // bf16: K-major Q [hb][cb 64][8 heads][8 dims].  e4m3: the hi term then
   // the lo term, each K-major [hb][cb 32][8 heads][16 dims].
   static constexpr int kQBytes = HQ * 512 * 2;
@@ -251,7 +259,11 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = sm.tmem_base;
-  // TMEM columns: S^T buffers at 0 and 32; O^T buffers at 64 and 192 (4 blocks of 32).
+  // TMEM columns: S^T buffers at 0 and kSCols; O^T buffers at kOBase and
+  // kOBase + 128 (4 blocks of 32).  bf16: S^T is 64 x HQ (kSCols 32).  e4m3:
+  // S^T is 64 x 2HQ, the logits against q_hi then against q_lo (kSCols 64).
+  constexpr uint32_t kSCols = kE4 ? 64 : 32;
+  constexpr uint32_t kOBase = 2 * kSCols;
   if (total_units > a.max_units) {  // uniform
     wait_prev();
     if (blockIdx.x == 0 && tid == 0) set_status(st, GW_DEV_WORKSPACE);
@@ -280,6 +292,17 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     if (!end) unit_info();
     bool in_unit = false;
     int32_t pg = end ? -1 : fetch_page(in_unit);
+    if (early && !end) {
+      // Warm L2 with the first two tiles' pages while the previous kernel
+      // finishes.  A prefetch only fills L2, which the previous kernel's
+      // writes (the append of the sequence's last row) keep coherent, so it
+      // may run before the wait; the copies to shared memory come after it.
+      const int lp = p0 + lane;
+      if (lane < 2 * kTilePages && lp < p1) {
+        const int32_t pp = a.block_table[static_cast<int64_t>(s) * a.max_pages + lp];
+        if (pp >= 0 && pp < a.num_pages) prefetch_l2(a.pool + static_cast<int64_t>(pp) * T::kPageBytes, T::kPageBytes);
+      }
+    }
     wait_prev();
     for (uint32_t n = 0;; ++n) {
       const int b = n % NB;
@@ -332,7 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     wait_prev();
     // The whole warp runs this loop with warp-uniform values; elect.sync
     // picks the issuing lane inside mma_bf16_warp / commit_warp.
-    const uint32_t id_qk = kE4 ? tc::idesc_e4m3(64, HQ, false, false) : tc::idesc_bf16(64, HQ, false, false);
+    // e4m3: one MMA per K-step against [q_hi; q_lo] (N = 2 HQ: the lo term's
+    // head blocks follow the hi term's at the same 8-head stride)
+    const uint32_t id_qk = kE4 ? tc::idesc_e4m3(64, 2 * HQ, false, false) : tc::idesc_bf16(64, HQ, false, false);
     // descriptor bases; the start-address field is addr >> 4 in the low bits,
     // so a byte offset o is added as o >> 4 (all addresses stay below 256 KiB).
     // Q: 16-byte block rows, the next 8 heads (kQBytes / 2 / (HQ / 8)) apart
@@ -355,15 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       tc::fence_after();
       const uint64_t a_tile = qk_a0 + ((b * kTileBytes) >> 4);
       const uint64_t q_base = qk_b0 + ((qb * SM::kQBytes) >> 4);
-      const uint32_t d_s = tmem + 32 * (n & 1);
+      const uint32_t d_s = tmem + kSCols * (n & 1);
 #pragma unroll
       for (int ks = 0; ks < T::kKSteps; ++ks) {
         const uint64_t ad = a_tile + ((T::k_cb(ks) * 128) >> 4);
         const uint64_t bd = q_base + ((2 * ks * 128) >> 4);
         if constexpr (kE4) {
-          // S = K . (q_hi + q_lo): two MMAs into one accumulator
           tc::mma_e4m3_warp(d_s, ad, bd, id_qk, ks > 0);
-          tc::mma_e4m3_warp(d_s, ad, bd + ((HQ * 512) >> 4), id_qk, true);
         } else {
           tc::mma_bf16_warp(d_s, ad, bd, id_qk, ks > 0);
         }
@@ -399,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
 #pragma unroll
           for (int blk = 0; blk < 4; ++blk) {
             const uint64_t ad = a_tile + ((2 * j * T::kPageBytes + (T::kVcb + 8 * blk) * 128) >> 4);
-            const uint32_t d_o = tmem + 64 + 128 * ob + 32 * blk;
+            const uint32_t d_o = tmem + kOBase + 128 * ob + 32 * blk;
             tc::mma_e4m3_warp(d_o, ad, bd, id_pv, !((d.flags & kFirst) && j == 0));
             tc::mma_e4m3_warp(d_o, ad, bd + ((64 * NP) >> 4), id_pv, true);
           }
@@ -413,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
 #pragma unroll
           for (int blk = 0; blk < 4; ++blk) {
             const uint64_t ad = a_tile + ((j * T::kPageBytes + (T::kVcb + 16 * blk) * 128) >> 4);
-            tc::mma_bf16_warp(tmem + 64 + 128 * ob + 32 * blk, ad, bd, id_pv, !((d.flags & kFirst) && j == 0));
+            tc::mma_bf16_warp(tmem + kOBase + 128 * ob + 32 * blk, ad, bd, id_pv, !((d.flags & kFirst) && j == 0));
           }
           tc::commit_warp(&sm.slot_empty[b][j]);  // the producer may refill this page slot
         }
@@ -424,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
   } else if (warp == 6 && kE4) {
     // ------------------------------------------------- q loader, e4m3 pool
     wait_prev();
-    // Unit k's q goes to Q buffer k & 1 once the last QK^T of unit k - 2 has
+    // Unit k's q goes to the Q buffer once the last QK^T of unit k - 1 has
     // completed.  Each head is scaled by an exact power of two 2^e, chosen so
     // that its largest |q| lands in [128, 256), and split into two e4m3
     // terms, hi = e4m3(q 2^e) and lo = e4m3(q 2^e - hi); 2^-e goes to the
@@ -432,8 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
     int k = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++k) {
       const int q_row = a.cu_q_rows[plan_seq(sm.ub, a.batch, u)];
-      const int qb = k & 1;
-      if (k >= 2 && !warp_wait(&sm.q_free[qb], ((k >> 1) - 1) & 1, st)) break;
+      const int qb = k % SM::kQBuf;
       // stage the bf16 rows in shared memory: all copies in flight at once
       const uint16_t* gsrc = a.q + static_cast<int64_t>(q_row) * HQ * 512;
       __syncwarp();  // the previous unit's reads of the stage are done
@@ -465,6 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
           sm.qscale[k & 3][h] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
         }
       }
+      // the Q buffer is free once the last QK^T that read it has completed
+      if (k >= SM::kQBuf && !warp_wait(&sm.q_free[qb], ((k / SM::kQBuf) - 1) & 1, st)) break;
       // pass 2: lane (h & 7, cb >> 2 ... ) converts 16 dims of one head; the 8
       // heads of a block go to 8 different 16-byte bank groups
       uint8_t* qhi = sm.q[qb];
@@ -562,8 +586,24 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       if (!mbar_wait(&sm.s_ready[n & 1], (n >> 1) & 1, st)) break;
       tc::fence_after();
       uint32_t r[32];
-      tc::ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * (n & 1), r);
-      tc::wait_ld();
+      const uint32_t s_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16) + kSCols * (n & 1);
+      tc::ld32(s_addr, r);
+      if constexpr (kE4) {
+        // logit = S(q_hi) + S(q_lo): columns h and HQ + h
+        if constexpr (HQ == 32) {
+          uint32_t r2[32];
+          tc::ld32(s_addr + 32, r2);
+          tc::wait_ld();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) + __uint_as_float(r2[h]));
+        } else {
+          tc::wait_ld();
+#pragma unroll
+          for (int h = 0; h < HQ; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) + __uint_as_float(r[HQ + h]));
+        }
+      } else {
+        tc::wait_ld();
+      }
       const int tabs = d.tok0 + t;
       const bool pvalid = (d.flags >> (8 + j)) & 1;
       const bool valid = active && pvalid && tabs < d.L;
@@ -613,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
           const uint32_t ob = uidx & 1;
 #pragma unroll 1
           for (int blk = 0; blk < 4; ++blk) {
-            const uint32_t ad = tmem + (static_cast<uint32_t>(32 * warp) << 16) + 64 + 128 * ob + 32 * blk;
+            const uint32_t ad = tmem + (static_cast<uint32_t>(32 * warp) << 16) + kOBase + 128 * ob + 32 * blk;
             uint32_t o[32];
             tc::ld32(ad, o);
             tc::wait_ld();
@@ -700,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
 #pragma unroll 1
         for (int blk = 0; blk < 4; ++blk) {
           uint32_t o[32];
-          tc::ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 64 + 128 * ob + 32 * blk, o);
+          tc::ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + kOBase + 128 * ob + 32 * blk, o);
           tc::wait_ld();
           const int dim = 128 * blk + 32 * warp + lane;
 #pragma unroll
