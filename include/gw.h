@@ -247,6 +247,50 @@ gw_status gw_decode_attn_global(const gw_kv_pool* pool, const void* q, void* out
                                 void* stream);
 
 /*
+ * gw_decode_attn_global_lse - gw_decode_attn_global for decode rows
+ * (max_q_rows 1) that also writes each row's log-sum-exp:
+ *
+ *   lse[row][h] = ln( sum_j exp(scale * q_h . K_j) )      over the row's keys
+ *
+ * (-inf for a row without keys), float32 [total_rows][num_q_heads],
+ * 4-byte aligned, caller-owned.  With it, attention over a long sequence
+ * whose keys are spread over several pools (one per rank of a
+ * context-parallel split, each pool holding a contiguous range of the
+ * sequence's pages, renumbered from 0) is the gw_merge_lse of the per-range
+ * results: the split-KV combine applied across ranks.  The pages run one GPU
+ * per sequence; this is the multi-GPU extension of the same split.
+ * Errors as gw_decode_attn_global; GW_ERR_INVALID_ARG for a NULL lse.
+ */
+gw_status gw_decode_attn_global_lse(const gw_kv_pool* pool, const void* q, void* out, float* lse,
+                                    int32_t num_q_heads, int32_t batch, const int32_t* cu_q_rows,
+                                    const int32_t* seq_lens, const int32_t* block_table, int32_t max_pages_per_seq,
+                                    float scale, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                    void* stream);
+
+/*
+ * gw_merge_lse - merge n_parts attention results of the same rows computed
+ * over disjoint key sets (the ranks of a context-parallel split), by their
+ * log-sum-exp:
+ *
+ *   M = max_r lse_r,  w_r = exp(lse_r - M),
+ *   out = (sum_r w_r o_r) / (sum_r w_r),   lse_out = M + ln(sum_r w_r),
+ *
+ * in float32 with the parts added in order r = 0, 1, ... (a part whose lse
+ * is -inf contributes nothing and its o is not read; a row whose parts are
+ * all -inf is written as zeros).
+ *   o_parts     host array of n_parts device pointers, each bf16
+ *               [rows][num_heads][head_dim], 16-byte aligned.
+ *   lse_parts   host array of n_parts device pointers, each float32
+ *               [rows][num_heads], 4-byte aligned.
+ *   out         bf16 [rows][num_heads][head_dim], 16-byte aligned.
+ *   lse_out     float32 [rows][num_heads] or NULL.
+ *   n_parts in [1, 16]; head_dim 256 or 512.
+ * Errors: GW_ERR_INVALID_ARG, GW_ERR_CUDA.  Asynchronous on `stream`.
+ */
+gw_status gw_merge_lse(int32_t n_parts, const void* const* o_parts, const float* const* lse_parts, void* out,
+                       float* lse_out, int32_t rows, int32_t num_heads, int32_t head_dim, void* stream);
+
+/*
  * Workspace bytes an attention call on `pool` needs for `batch` sequences of
  * at most `max_seq_len` tokens and `max_q_rows` rows each (window ignored for
  * global pools).  0 on an invalid description.

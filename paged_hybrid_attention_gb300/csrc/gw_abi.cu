@@ -214,7 +214,8 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
                              int32_t num_q_heads, int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,
                              const int32_t* block_table, int32_t max_pages_per_seq, int32_t max_q_rows,
                              int32_t window, float scale, void* workspace, size_t workspace_bytes,
-                             int32_t* dev_status, void* stream, bool validate_only = false) {
+                             int32_t* dev_status, void* stream, bool validate_only = false,
+                             float* lse = nullptr) {
   g_err[0] = 0;
   gw_status s = check_pool(pool, fn);
   if (s != GW_OK) return s;
@@ -275,6 +276,7 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
   a.max_units = w.max_units;
   a.status = dev_status;
   a.early_inputs = g_early_inputs ? 1 : 0;
+  a.lse = lse;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (local) {
@@ -319,6 +321,48 @@ gw_status gw_decode_attn_global(const gw_kv_pool* pool, const void* q, void* out
   return attn_common("gw_decode_attn_global", false, pool, q, out, num_q_heads, batch, cu_q_rows, seq_lens,
                      block_table, max_pages_per_seq, max_q_rows, 0, scale, workspace, workspace_bytes, dev_status,
                      stream);
+}
+
+gw_status gw_decode_attn_global_lse(const gw_kv_pool* pool, const void* q, void* out, float* lse,
+                                    int32_t num_q_heads, int32_t batch, const int32_t* cu_q_rows,
+                                    const int32_t* seq_lens, const int32_t* block_table, int32_t max_pages_per_seq,
+                                    float scale, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                    void* stream) {
+  const char* fn = "gw_decode_attn_global_lse";
+  if (!lse || !aligned(lse, 4)) {
+    g_err[0] = 0;
+    return fail(GW_ERR_INVALID_ARG, fn, "lse NULL or misaligned");
+  }
+  return attn_common(fn, false, pool, q, out, num_q_heads, batch, cu_q_rows, seq_lens, block_table,
+                     max_pages_per_seq, 1, 0, scale, workspace, workspace_bytes, dev_status, stream, false, lse);
+}
+
+gw_status gw_merge_lse(int32_t n_parts, const void* const* o_parts, const float* const* lse_parts, void* out,
+                       float* lse_out, int32_t rows, int32_t num_heads, int32_t head_dim, void* stream) {
+  const char* fn = "gw_merge_lse";
+  g_err[0] = 0;
+  if (n_parts < 1 || n_parts > kMaxMergeParts)
+    return fail(GW_ERR_INVALID_ARG, fn, "n_parts (%d) outside [1, %d]", n_parts, kMaxMergeParts);
+  if (rows < 0 || num_heads < 1) return fail(GW_ERR_INVALID_ARG, fn, "rows < 0 or num_heads < 1");
+  if (head_dim != 256 && head_dim != 512) return fail(GW_ERR_INVALID_ARG, fn, "head_dim must be 256 or 512");
+  if (!o_parts || !lse_parts) return fail(GW_ERR_INVALID_ARG, fn, "o_parts/lse_parts NULL");
+  if (!out || !aligned(out, 16)) return fail(GW_ERR_INVALID_ARG, fn, "out NULL or not 16-byte aligned");
+  if (lse_out && !aligned(lse_out, 4)) return fail(GW_ERR_INVALID_ARG, fn, "lse_out misaligned");
+  MergeArgs m{};
+  for (int r = 0; r < n_parts; ++r) {
+    if (!o_parts[r] || !aligned(o_parts[r], 16) || !lse_parts[r] || !aligned(lse_parts[r], 4))
+      return fail(GW_ERR_INVALID_ARG, fn, "part %d: o NULL or not 16-byte aligned, or lse NULL or misaligned", r);
+    m.o[r] = static_cast<const uint16_t*>(o_parts[r]);
+    m.lse[r] = lse_parts[r];
+  }
+  if (rows == 0) return GW_OK;
+  m.n_parts = n_parts;
+  m.rows = rows;
+  m.heads = num_heads;
+  m.head_dim = head_dim;
+  m.out = static_cast<uint16_t*>(out);
+  m.lse_out = lse_out;
+  return cuda_status(launch_merge_lse(m, static_cast<cudaStream_t>(stream)), fn);
 }
 
 gw_status gw_set_max_ctas(int32_t max_ctas) {

@@ -93,6 +93,7 @@ struct LocalArgs {
   int64_t max_units;
   int32_t* status;
   int32_t* prompt_base;  // tile offsets of the prompt-row kernels
+  float* lse;            // optional: natural-log log-sum-exp per (decode row, q head)
   int32_t early_inputs;  // gw_set_early_inputs: plan before the wait on the previous kernel
 };
 
@@ -141,6 +142,18 @@ cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim,
                            cudaStream_t st);
 
 cudaError_t launch_append(int layout, int dtype, const AppendArgs& a, cudaStream_t st);
+
+// Up to kMaxMergeParts attention results of the same rows over disjoint key
+// sets, merged by their log-sum-exp (gw_merge_lse).
+constexpr int kMaxMergeParts = 16;
+struct MergeArgs {
+  const uint16_t* o[kMaxMergeParts];  // bf16 [rows][heads][head_dim]
+  const float* lse[kMaxMergeParts];   // [rows][heads], natural log
+  int32_t n_parts, rows, heads, head_dim;
+  uint16_t* out;
+  float* lse_out;
+};
+cudaError_t launch_merge_lse(const MergeArgs& m, cudaStream_t st);
 // (cos, sin) table of gw_rope_cs: float32 [max_pos][rot_dim / 2][2].
 cudaError_t launch_rope_cs(float* out, double theta, int rot_dim, int head_dim, int max_pos, cudaStream_t st);
 cudaError_t launch_bw_probe(const void* buf, int64_t chunks, int32_t* status, cudaStream_t st);

@@ -145,9 +145,55 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const LocalArgs a, int 
   w.x = *reinterpret_cast<uint32_t*>(&lo);
   w.y = *reinterpret_cast<uint32_t*>(&hi);
   *reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(row0) * a.num_q_heads + h) * D + dim0) = w;
+  // log-sum-exp of the row's logits, natural log (the partials are in base-2
+  // units of the scaled logits): ln(sum_j e^{scale q.k_j}) = ln2 (M + log2 den)
+  if (a.lse && slice == 0 && lane == 0)
+    a.lse[static_cast<int64_t>(row0) * a.num_q_heads + h] = den > 0.f ? 0.6931471805599453f * (M + log2f(den)) : -INFINITY;
+}
+
+// gw_merge_lse: one warp per (row, head); lane l owns dims [8 l', ...) in
+// 16-byte chunks.  Parts are added in part order.
+__global__ void __launch_bounds__(256) merge_lse_kernel(const MergeArgs m) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t task = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (task >= static_cast<int64_t>(m.rows) * m.heads) return;
+  float M = -INFINITY;
+  for (int r = 0; r < m.n_parts; ++r) M = fmaxf(M, m.lse[r][task]);
+  float w[kMaxMergeParts];
+  float den = 0.f;
+  for (int r = 0; r < m.n_parts; ++r) {
+    w[r] = M == -INFINITY ? 0.f : __expf(m.lse[r][task] - M);
+    den += w[r];
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  for (int c = lane; c < m.head_dim / 8; c += 32) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < m.n_parts; ++r) {
+      if (w[r] == 0.f) continue;  // a part without keys: its bytes may be anything
+      float x[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(m.o[r] + task * m.head_dim + 8 * c), x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(w[r], x[i], acc[i]);
+    }
+    uint32_t pk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+      pk[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(m.out + task * m.head_dim + 8 * c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+  if (m.lse_out && lane == 0) m.lse_out[task] = den > 0.f ? M + logf(den) : -INFINITY;
 }
 
 }  // namespace
+
+cudaError_t launch_merge_lse(const MergeArgs& m, cudaStream_t st) {
+  const int64_t tasks = static_cast<int64_t>(m.rows) * m.heads;
+  return launch_pdl(merge_lse_kernel, dim3(static_cast<unsigned>((tasks + 7) / 8)), dim3(256), 0, st, m);
+}
 
 cudaError_t launch_combine(const LocalArgs& a, int heads_per_unit, int head_dim, int max_chunks, bool discard,
                            cudaStream_t st) {

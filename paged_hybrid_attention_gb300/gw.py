@@ -31,7 +31,8 @@ DTYPES = {"bf16": KV_BF16, "e4m3": KV_E4M3}
 EXPORTS = ["gw_pool_page_bytes", "gw_kv_append", "gw_decode_attn_local", "gw_decode_attn_global",
            "gw_attn_workspace_bytes", "gw_last_error", "gw_version", "gw_decode_attn_local_noalloc",
            "gw_noalloc_scratch_bytes", "gw_bw_probe", "gw_set_max_ctas", "gw_set_early_launch",
-           "gw_set_early_inputs", "gw_rope_cs", "gw_wait_selftest", "gw_bw_probe_tma"]
+           "gw_set_early_inputs", "gw_rope_cs", "gw_wait_selftest", "gw_bw_probe_tma",
+           "gw_decode_attn_global_lse", "gw_merge_lse"]
 
 
 class GwError(RuntimeError):
@@ -58,6 +59,11 @@ _lib.gw_decode_attn_local.restype = _i32
 _lib.gw_decode_attn_global.argtypes = [_P, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _sz,
                                        _vp, _vp]
 _lib.gw_decode_attn_global.restype = _i32
+_lib.gw_decode_attn_global_lse.argtypes = [_P, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _f32, _vp, _sz,
+                                           _vp, _vp]
+_lib.gw_decode_attn_global_lse.restype = _i32
+_lib.gw_merge_lse.argtypes = [_i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp]
+_lib.gw_merge_lse.restype = _i32
 _lib.gw_rope_cs.argtypes = [_vp, ctypes.c_double, _i32, _i32, _i32, _vp]
 _lib.gw_rope_cs.restype = _i32
 _lib.gw_attn_workspace_bytes.argtypes = [_P, _i32, _i32, _i32, _i32, _i32]
@@ -188,6 +194,27 @@ def decode_attn_global(pool, q, out, cu_q_rows, seq_lens, block_table, workspace
                                       _ptr(cu_q_rows), _ptr(seq_lens), _ptr(block_table), int(block_table.shape[1]),
                                       int(max_q_rows), float(scale), _ptr(workspace), int(workspace.numel()),
                                       _ptr(dev_status), _stream(stream)))
+
+
+def decode_attn_global_lse(pool, q, out, lse, cu_q_rows, seq_lens, block_table, workspace, scale=None,
+                           dev_status=None, stream=None):
+    """gw_decode_attn_global_lse: decode rows, plus each row's log-sum-exp (float32 [rows, heads])."""
+    hq = int(q.shape[1])
+    scale = 1.0 / math.sqrt(512) if scale is None else scale
+    _check(_lib.gw_decode_attn_global_lse(ctypes.byref(pool.desc), _ptr(q), _ptr(out), _ptr(lse), hq,
+                                          int(seq_lens.numel()), _ptr(cu_q_rows), _ptr(seq_lens), _ptr(block_table),
+                                          int(block_table.shape[1]), float(scale), _ptr(workspace),
+                                          int(workspace.numel()), _ptr(dev_status), _stream(stream)))
+
+
+def merge_lse(outs, lses, out, lse_out=None, stream=None):
+    """gw_merge_lse: merge the parts (bf16 [rows, heads, D] outputs and their
+    float32 [rows, heads] log-sum-exps) into `out`."""
+    n = len(outs)
+    o_arr = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    l_arr = (ctypes.c_void_p * n)(*[l.data_ptr() for l in lses])
+    rows, heads, dim = (int(x) for x in out.shape)
+    _check(_lib.gw_merge_lse(n, o_arr, l_arr, _ptr(out), _ptr(lse_out), rows, heads, dim, _stream(stream)))
 
 
 def decode_attn_local_noalloc(pool, q, out, cu_q_rows, seq_lens, block_table, window, scale=None, max_q_rows=1,

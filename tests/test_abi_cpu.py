@@ -195,3 +195,20 @@ def test_bw_probe_tma_host_validation():
     assert gw.last_error().startswith("gw_bw_probe_tma:")
     assert L.gw_bw_probe_tma(_fake((1 << 24) + 16), 1 << 20, None, None) == gw.GW_ERR_INVALID_ARG  # not 256-aligned
     assert L.gw_bw_probe_tma(_fake(), 8192, None, None) == gw.GW_ERR_INVALID_ARG                   # < one stage
+
+
+def test_cp_entry_points_host_validation():
+    L = gw.lib()
+    f = _fake()
+    g = _desc(gw.LAYOUT_GLOBAL_FOLDED, kvh=1, hd=512, rd=128)
+    st = L.gw_decode_attn_global_lse(ctypes.byref(g), f, f, None, 32, 2, f, f, f, 64, 0.04, _fake(1 << 28), 1 << 30,
+                                     None, None)
+    assert st == gw.GW_ERR_INVALID_ARG and gw.last_error().startswith("gw_decode_attn_global_lse:")
+    arr = (ctypes.c_void_p * 2)(1 << 24, 1 << 25)
+    assert L.gw_merge_lse(0, arr, arr, f, None, 4, 8, 512, None) == gw.GW_ERR_INVALID_ARG      # no parts
+    assert L.gw_merge_lse(17, arr, arr, f, None, 4, 8, 512, None) == gw.GW_ERR_INVALID_ARG     # above 16
+    assert L.gw_merge_lse(2, arr, arr, f, None, 4, 8, 128, None) == gw.GW_ERR_INVALID_ARG      # head dim
+    bad = (ctypes.c_void_p * 2)(1 << 24, (1 << 25) + 8)
+    assert L.gw_merge_lse(2, bad, arr, f, None, 4, 8, 512, None) == gw.GW_ERR_INVALID_ARG      # misaligned part
+    assert "part 1" in gw.last_error()
+    assert L.gw_merge_lse(2, arr, arr, f, None, 0, 8, 512, None) == gw.GW_OK                   # no rows
