@@ -210,10 +210,16 @@ gw_status gw_rope_cs(float* rope_cs, double theta, int32_t rot_dim, int32_t head
  *   window       >= 1 (1024 for the served model).
  *   workspace    device scratch of at least gw_attn_workspace_bytes(...),
  *                256-byte aligned; contents need no initialisation.
+ * On an e4m3 pool ([PR1012] "Description", "Verification": the sliding
+ * family's fp8 pool serves decode and mixed steps alike) the prompt-row
+ * contractions run on the e4m3 tiles as stored; each q row and softmax
+ * weight enters as a sum of two e4m3 terms (q after an exact power-of-two
+ * scaling), which carries it at about bf16 precision.  Decode rows on e4m3
+ * pools round q to f16 once per unit: |q| must stay below 65504.
+ *
  * Errors: GW_ERR_INVALID_ARG, GW_ERR_WORKSPACE, GW_ERR_UNSUPPORTED
  * (num_q_heads / kv_heads not in {1,2,4,8}; batch > 4096, since the decode
- * kernel keeps the batch's split plan in shared memory; max_q_rows > 1 on an
- * e4m3 pool, since the prompt-row kernel reads bf16 pages only), GW_ERR_CUDA.
+ * kernel keeps the batch's split plan in shared memory), GW_ERR_CUDA.
  * Every error but GW_ERR_CUDA is returned before anything is launched.
  */
 gw_status gw_decode_attn_local(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads,

@@ -67,10 +67,10 @@ __global__ void plan_prompt_kernel(const LocalArgs a, int heads_factor, int quer
 }
 
 template <int G>
-cudaError_t launch_local_g(const LocalArgs& a, cudaStream_t st) {
+cudaError_t launch_local_g(int dtype, const LocalArgs& a, cudaStream_t st) {
   cudaError_t e = launch_pdl(plan_prompt_kernel, dim3(1), dim3(1024), 0, st, a, a.kv_heads, 128 / G);
   if (e != cudaSuccess) return e;
-  return launch_local_prompt_tc(G, a, st);
+  return launch_local_prompt_tc(dtype, G, a, st);
 }
 
 template <int HQ>
@@ -84,12 +84,11 @@ cudaError_t launch_global_hq(int layout, const LocalArgs& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_local_prompt(int dtype, int group, const LocalArgs& a, int /*max_q_rows*/, cudaStream_t st) {
-  if (dtype != GW_KV_BF16) return cudaErrorNotSupported;
   switch (group) {
-    case 1: return launch_local_g<1>(a, st);
-    case 2: return launch_local_g<2>(a, st);
-    case 4: return launch_local_g<4>(a, st);
-    case 8: return launch_local_g<8>(a, st);
+    case 1: return launch_local_g<1>(dtype, a, st);
+    case 2: return launch_local_g<2>(dtype, a, st);
+    case 4: return launch_local_g<4>(dtype, a, st);
+    case 8: return launch_local_g<8>(dtype, a, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -47,12 +47,18 @@ constexpr int kTcThreads = 256;
 constexpr float kTcLazy = 8.f;
 // TMEM columns: S buffers at 0 and 64, Q at 128..255, O at 256..511
 constexpr uint32_t kColS = 0, kColQ = 128, kColO = 256;
-constexpr uint32_t kPlane = kTN * 128;  // one 64-dim chunk of a K/V tile: 64 rows x 128 B
+constexpr uint32_t kPlane = kTN * 128;  // one 128-byte chunk column of a K/V tile: 64 rows x 128 B
 constexpr int kKS = 3, kVS = 3;         // K and V stages
 
+// 128-byte chunks per 256-element row: 4 of 64 bf16, 2 of 128 e4m3
+template <int DT>
+constexpr int chunks_of() { return DT == GW_KV_BF16 ? 4 : 2; }
+
+template <int DT>
 struct TcSmem {
-  uint8_t k[kKS][4 * kPlane];    // [dim chunk 4][64 keys][128 B], 128-byte swizzled
-  uint8_t v[kVS][4 * kPlane];    // same layout
+  static constexpr int kC = chunks_of<DT>();
+  uint8_t k[kKS][kC * kPlane];    // [chunk][64 keys][128 B], 128-byte swizzled
+  uint8_t v[kVS][kC * kPlane];    // same layout
   uint64_t kfull[kKS], kempty[kKS], vfull[kVS], vempty[kVS];
   uint64_t s_ready[2], p_ready[2], pfree[2];
   uint64_t q_full, q_free, o_done, o_free;
@@ -62,6 +68,33 @@ struct TcSmem {
 
 __device__ __forceinline__ void zero16(uint32_t dst) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0) : "memory");
+}
+
+// Zero key rows of a K/V stage (every 16-byte unit of the row's chunks);
+// `want(r)` selects rows r in [0, 64).  The warp's lanes share the units.
+template <int DT, class Want>
+__device__ __forceinline__ void zero_rows(uint32_t base, int lane, Want want) {
+  constexpr int kU = chunks_of<DT>() * 8;  // 16-byte units per row
+  for (int idx = lane; idx < kTN * kU; idx += 32) {
+    const int r = idx / kU, u = idx % kU;
+    if (want(r)) zero16(base + (u >> 3) * kPlane + r * 128 + (u & 7) * 16);
+  }
+}
+
+// q (or a weight) x as two e4m3 terms: hi = e4m3(x), lo = e4m3(x - hi); the
+// pair (x0, x1) gives one 16-bit word of each (x0 in the low byte).  With
+// `sum`, the value hi + lo the contraction will use.
+__device__ __forceinline__ void split_e4m3(float x0, float x1, uint32_t& hi, uint32_t& lo, float2* sum = nullptr) {
+  const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+  const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+  const __nv_fp8x2_storage_t l2 =
+      __nv_cvt_float2_to_fp8x2(make_float2(x0 - hf.x, x1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+  hi = h2;
+  lo = l2;
+  if (sum) {
+    const float2 lf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(l2, __NV_E4M3)));
+    *sum = make_float2(hf.x + lf.x, hf.y + lf.y);
+  }
 }
 
 // Shared-memory descriptor of a 128-byte-swizzled operand (atoms of 8 rows x
@@ -106,12 +139,14 @@ __device__ __forceinline__ WorkTile work_tile(const LocalArgs& a, int tile) {
   return w;
 }
 
-template <int G>
+template <int DT, int G>
 __global__ void __launch_bounds__(kTcThreads, 1)
     local_prompt_tc_kernel(const LocalArgs a, const __grid_constant__ CUtensorMap kv_map) {
   constexpr int BQ = kTM / G;
+  constexpr bool kE4 = DT == GW_KV_E4M3;
+  constexpr int kC = chunks_of<DT>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw);
+  TcSmem<DT>& sm = *reinterpret_cast<TcSmem<DT>*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   int32_t* st = a.status;
 
@@ -149,13 +184,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 4 || warp == 6) {
     // ------------------------------------------------------ TMA producers
-    // warp 4 loads K tiles, warp 6 V tiles; lane l < 16 issues the copy of
-    // page l / 4, 64-dim chunk l % 4 (the 16 copies of a tile go out together)
+    // warp 4 loads K tiles, warp 6 V tiles; lane l < 4 kC issues the copy of
+    // page l / kC, 128-byte chunk l % kC (a tile's copies go out together)
     const bool is_v = warp == 6;
     // every K/V tile is read again by the neighbouring query blocks (a window
     // of W keys is shared by W / 64 of them): keep it in L2 (evict last)
     const uint64_t pol = policy_evict_last();
-    const int j = lane >> 2, c = lane & 3;
+    const int j = lane / kC, c = lane % kC;
     uint32_t gi = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
@@ -167,7 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t ph = gi / ns;  // use of this stage
         // page j of the tile: loaded if it overlaps [lo, hi] and is valid
         int32_t row = -1;
-        if (lane < 16) {
+        if (lane < 4 * kC) {
           const int k0 = t * kTN + j * kPage;
           if (k0 + kPage - 1 >= w.lo && k0 <= w.hi) {
             const int32_t pg = bt[k0 / kPage];
@@ -178,16 +213,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         }
-        const uint32_t loaded = __ballot_sync(0xffffffffu, row >= 0 && c == 0);  // bit 4j: page j
+        const uint32_t loaded = __ballot_sync(0xffffffffu, row >= 0 && c == 0);  // bit kC j: page j
         int mask = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) mask |= ((loaded >> (4 * q)) & 1) << q;
+        for (int q = 0; q < 4; ++q) mask |= ((loaded >> (kC * q)) & 1) << q;
         uint64_t* full = is_v ? &sm.vfull[b] : &sm.kfull[b];
         uint64_t* empty = is_v ? &sm.vempty[b] : &sm.kempty[b];
         if (ph >= 1 && !__all_sync(0xffffffffu, mbar_wait(empty, (ph - 1) & 1, st))) { ok = false; break; }
         if (lane == 0) {
           if (is_v) sm.vmask[b] = mask; else sm.kmask[b] = mask;
-          mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(mask)) * 4 * 2048);
+          mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(mask)) * kC * 2048);
         }
         __syncwarp();
         if (row >= 0)
@@ -196,7 +231,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 5) {
     // ---------------------------------------------------- Q.K^T issue
-    const uint32_t id_s = tc::idesc_bf16(kTM, kTN, false, false);
+    const uint32_t id_s = kE4 ? tc::idesc_e4m3(kTM, kTN, false, false) : tc::idesc_bf16(kTM, kTN, false, false);
     uint32_t gi = 0;
     int wt = 0;
     bool ok = true;
@@ -217,19 +252,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (kmask != 0xF) {
           // pages not loaded (outside the range or invalid): finite zeros, so no
           // stale bytes can turn into NaN logits
-          for (int pg = 0; pg < 4; ++pg) {
-            if ((kmask >> pg) & 1) continue;
-            for (int kr = 0; kr < kPage; ++kr)
-              zero16(ka + (lane >> 3) * kPlane + (pg * kPage + kr) * 128 + (lane & 7) * 16);
-          }
+          zero_rows<DT>(ka, lane, [&](int r) { return ((kmask >> (r / kPage)) & 1) == 0; });
           fence_proxy_async_smem();
           __syncwarp();
         }
         tc::fence_after();
+        // a K-step is 32 bytes of each key row: 16 bf16 or 32 e4m3 dims
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks)
-          tc::mma_bf16_ts_warp(tmem + kColS + 64 * sb, tmem + kColQ + 8 * ks,
-                               sw128_desc(ka + (ks >> 2) * kPlane + (ks & 3) * 32, 16), id_s, ks > 0);
+        for (int ks = 0; ks < 16 / (kE4 ? 2 : 1); ++ks) {
+          const uint64_t bd = sw128_desc(ka + (ks >> 2) * kPlane + (ks & 3) * 32, 16);
+          if constexpr (kE4) {
+            // S = (q_hi + q_lo) . K^T: q_hi at Q columns 0..63, q_lo at 64..127
+            tc::mma_e4m3_ts_warp(tmem + kColS + 64 * sb, tmem + kColQ + 8 * ks, bd, id_s, ks > 0);
+            tc::mma_e4m3_ts_warp(tmem + kColS + 64 * sb, tmem + kColQ + 64 + 8 * ks, bd, id_s, true);
+          } else {
+            tc::mma_bf16_ts_warp(tmem + kColS + 64 * sb, tmem + kColQ + 8 * ks, bd, id_s, ks > 0);
+          }
+        }
         tc::commit_warp(&sm.kempty[b]);
         tc::commit_warp(&sm.s_ready[sb]);
         if (j == nt - 1) tc::commit_warp(&sm.q_free);
@@ -237,7 +276,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 7) {
     // ------------------------------------------------------- P.V issue
-    const uint32_t id_o = tc::idesc_bf16(kTM, 256, false, true);
+    const uint32_t id_o = kE4 ? tc::idesc_e4m3(kTM, 256, false, true) : tc::idesc_bf16(kTM, 256, false, true);
     uint32_t gi = 0;
     int wt = 0;
     bool ok = true;
@@ -255,22 +294,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int key0 = (w.t_lo + j) * kTN;
         const int mask = sm.vmask[b];
         if (mask != 0xF || key0 < w.lo || key0 + kTN - 1 > w.hi) {
-          const uint32_t vb = smem_u32(sm.v[b]);
-          for (int kr = 0; kr < kTN; ++kr) {
+          zero_rows<DT>(smem_u32(sm.v[b]), lane, [&](int kr) {
             const int key = key0 + kr;
-            if (((mask >> (kr >> 4)) & 1) && key >= w.lo && key <= w.hi) continue;
-            zero16(vb + (lane >> 3) * kPlane + kr * 128 + (lane & 7) * 16);
-          }
+            return !(((mask >> (kr >> 4)) & 1) && key >= w.lo && key <= w.hi);
+          });
           fence_proxy_async_smem();
           __syncwarp();
         }
         if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_ready[sb], (gi >> 1) & 1, st))) { ok = false; break; }
         tc::fence_after();
         const uint32_t va = smem_u32(sm.v[b]);
+        if constexpr (kE4) {
+          // K-steps of 32 keys (4 swizzle atoms of 8 rows); O += (P_hi + P_lo) . V,
+          // P_hi at S columns 0..15, P_lo at 16..31
 #pragma unroll
-        for (int kk = 0; kk < kTN / 16; ++kk)
-          tc::mma_bf16_ts_warp(tmem + kColO, tmem + kColS + 64 * sb + 8 * kk, sw128_desc(va + kk * 2048, kPlane),
-                               id_o, !(j == 0 && kk == 0));
+          for (int kk = 0; kk < kTN / 32; ++kk) {
+            const uint64_t bd = sw128_desc(va + kk * 4096, kPlane);
+            tc::mma_e4m3_ts_warp(tmem + kColO, tmem + kColS + 64 * sb + 8 * kk, bd, id_o, !(j == 0 && kk == 0));
+            tc::mma_e4m3_ts_warp(tmem + kColO, tmem + kColS + 64 * sb + 16 + 8 * kk, bd, id_o, true);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kTN / 16; ++kk)
+            tc::mma_bf16_ts_warp(tmem + kColO, tmem + kColS + 64 * sb + 8 * kk, sw128_desc(va + kk * 2048, kPlane),
+                                 id_o, !(j == 0 && kk == 0));
+        }
         tc::commit_warp(&sm.vempty[b]);
         tc::commit_warp(&sm.pfree[sb]);
         if (j == nt - 1) tc::commit_warp(&sm.o_done);
@@ -283,22 +331,66 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
     // Q row of a work tile -> tensor memory (128 columns of bf16 pairs), then
     // signal the MMA warp; rows past the prompt are zeros
+    // e4m3 pools: the row is scaled by an exact power of two 2^e that puts its
+    // largest |q| in [128, 256) and split into two e4m3 terms; sc_q = 2^-e
+    // scales the logits back (1 for bf16 pools)
+    float sc_q = 1.f;
     auto load_q = [&](const WorkTile& w) {
       const bool ok_row = qi < w.nq;
       const uint4* src = reinterpret_cast<const uint4*>(
           a.q + (static_cast<int64_t>(w.row0 + w.q0 + (ok_row ? qi : 0)) * a.num_q_heads + w.g * G + hh) * 256);
-      uint32_t qv[128];
+      if constexpr (kE4) {
+        // pass 1: the row's largest |q|; pass 2 reads the row again (from L1)
+        // a quarter at a time
+        float mq = 0.f;
+#pragma unroll 8
+        for (int c = 0; c < 32; ++c) {
+          const uint4 x = ok_row ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t u4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const uint4 x = ok_row ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-        qv[4 * c] = x.x;
-        qv[4 * c + 1] = x.y;
-        qv[4 * c + 2] = x.z;
-        qv[4 * c + 3] = x.w;
+          for (int i = 0; i < 4; ++i)
+            mq = fmaxf(mq, fmaxf(fabsf(__uint_as_float(u4[i] << 16)), fabsf(__uint_as_float(u4[i] & 0xFFFF0000u))));
+        }
+        const int ex = mq > 0.f ? static_cast<int>((__float_as_uint(mq) >> 23) & 0xFF) - 127 : 7;
+        const int e = min(125, max(-125, 7 - ex));
+        const float up = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+        sc_q = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+        // 4 dims per 32-bit column: q_hi at columns 0..63, q_lo at 64..127,
+        // a quarter (64 dims: 16 columns of each) at a time
+#pragma unroll 1
+        for (int qtr = 0; qtr < 4; ++qtr) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const uint4 x = ok_row ? src[8 * qtr + c8] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t u4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int hv = 0; hv < 2; ++hv) {
+              const uint32_t w0 = u4[2 * hv], w1 = u4[2 * hv + 1];
+              uint32_t h0, l0, h1, l1;
+              split_e4m3(__uint_as_float(w0 << 16) * up, __uint_as_float(w0 & 0xFFFF0000u) * up, h0, l0);
+              split_e4m3(__uint_as_float(w1 << 16) * up, __uint_as_float(w1 & 0xFFFF0000u) * up, h1, l1);
+              hi[2 * c8 + hv] = h0 | (h1 << 16);
+              lo[2 * c8 + hv] = l0 | (l1 << 16);
+            }
+          }
+          tc::st16(tmem + lane_base + kColQ + 16 * qtr, hi);
+          tc::st16(tmem + lane_base + kColQ + 64 + 16 * qtr, lo);
+        }
+      } else {
+        uint32_t qv[128];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const uint4 x = ok_row ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+          qv[4 * c] = x.x;
+          qv[4 * c + 1] = x.y;
+          qv[4 * c + 2] = x.z;
+          qv[4 * c + 3] = x.w;
+        }
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk)
+          tc::st32(tmem + lane_base + kColQ + 32 * blk, *reinterpret_cast<uint32_t(*)[32]>(&qv[32 * blk]));
       }
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk)
-        tc::st32(tmem + lane_base + kColQ + 32 * blk, *reinterpret_cast<uint32_t(*)[32]>(&qv[32 * blk]));
       tc::wait_st();
       tc::fence_before();
       mbar_arrive(&sm.q_full);
@@ -338,7 +430,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mg[g8] = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
         }
         const float mraw = fmaxf(fmaxf(fmaxf(mg[0], mg[1]), fmaxf(mg[2], mg[3])), fmaxf(fmaxf(mg[4], mg[5]), fmaxf(mg[6], mg[7])));
-        const float mx = mraw * a.scale_log2;  // -inf stays -inf (scale > 0)
+        const float sc = a.scale_log2 * sc_q;  // sc_q: the row's q descale (e4m3 pools)
+        const float mx = mraw * sc;            // -inf stays -inf (scale > 0)
         const bool raise = mx > m_ref + kTcLazy;  // false while the row has no key
         if (__any_sync(0xffffffffu, raise)) {
           const float m_new = raise ? mx : m_ref;
@@ -376,13 +469,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // key yet uses m = 0 so that no inf - inf arises
         const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
         uint32_t pw[32];
+        if constexpr (kE4) {
+          // P = P_hi + P_lo, two e4m3 terms (p <= 2^8 under the lazy max), 4
+          // keys per column: P_hi at columns 0..15, P_lo at 16..31
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float p0 = ex2(fmaf(__uint_as_float(sv[2 * u]), a.scale_log2, neg_m));
-          const float p1 = ex2(fmaf(__uint_as_float(sv[2 * u + 1]), a.scale_log2, neg_m));
-          __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          lp[u & 3] += __low2float(pb) + __high2float(pb);
-          pw[u] = *reinterpret_cast<uint32_t*>(&pb);
+          for (int u = 0; u < 16; ++u) {
+            uint32_t h[2], l[2];
+#pragma unroll
+            for (int hv = 0; hv < 2; ++hv) {
+              const float p0 = ex2(fmaf(__uint_as_float(sv[4 * u + 2 * hv]), sc, neg_m));
+              const float p1 = ex2(fmaf(__uint_as_float(sv[4 * u + 2 * hv + 1]), sc, neg_m));
+              float2 used;
+              split_e4m3(p0, p1, h[hv], l[hv], &used);
+              lp[u & 3] += used.x + used.y;
+            }
+            pw[u] = h[0] | (h[1] << 16);
+            pw[16 + u] = l[0] | (l[1] << 16);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const float p0 = ex2(fmaf(__uint_as_float(sv[2 * u]), sc, neg_m));
+            const float p1 = ex2(fmaf(__uint_as_float(sv[2 * u + 1]), sc, neg_m));
+            __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            lp[u & 3] += __low2float(pb) + __high2float(pb);
+            pw[u] = *reinterpret_cast<uint32_t*>(&pb);
+          }
         }
         tc::st32(tmem + lane_base + kColS + 64 * b, pw);
         tc::wait_st();
@@ -437,28 +549,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-template <int G>
+template <int DT, int G>
 cudaError_t launch_g(const LocalArgs& a, cudaStream_t st) {
   CUtensorMap map;
-  cudaError_t e = make_local_kv_map(a, &map);
+  cudaError_t e = make_local_kv_map(a, &map, DT);
   if (e != cudaSuccess) return e;
-  auto kern = local_prompt_tc_kernel<G>;
-  const size_t smem = sizeof(TcSmem);
+  auto kern = local_prompt_tc_kernel<DT, G>;
+  const size_t smem = sizeof(TcSmem<DT>);
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid_ctas()), dim3(kTcThreads), smem, st, a, map);
 }
 
-}  // namespace
 
-cudaError_t launch_local_prompt_tc(int group, const LocalArgs& a, cudaStream_t st) {
+template <int DT>
+cudaError_t launch_dt(int group, const LocalArgs& a, cudaStream_t st) {
   switch (group) {
-    case 1: return launch_g<1>(a, st);
-    case 2: return launch_g<2>(a, st);
-    case 4: return launch_g<4>(a, st);
-    case 8: return launch_g<8>(a, st);
+    case 1: return launch_g<DT, 1>(a, st);
+    case 2: return launch_g<DT, 2>(a, st);
+    case 4: return launch_g<DT, 4>(a, st);
+    case 8: return launch_g<DT, 8>(a, st);
   }
   return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_local_prompt_tc(int dtype, int group, const LocalArgs& a, cudaStream_t st) {
+  return dtype == GW_KV_E4M3 ? launch_dt<GW_KV_E4M3>(group, a, st) : launch_dt<GW_KV_BF16>(group, a, st);
 }
 
 }  // namespace gw

@@ -237,9 +237,9 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(GW_ERR_INVALID_ARG, fn, "scale must be finite and > 0");
   if (max_pages_per_seq < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_pages_per_seq must be >= 1");
   if (max_q_rows < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_q_rows must be >= 1");
-  if (pool->dtype == GW_KV_E4M3 && max_q_rows > 1)
-    return fail(GW_ERR_UNSUPPORTED, fn, "prompt rows (max_q_rows %d > 1) on an e4m3 pool: the prompt-row kernel "
-                "reads bf16 pages only", max_q_rows);
+  if (!local && pool->dtype == GW_KV_E4M3 && max_q_rows > 1)
+    return fail(GW_ERR_UNSUPPORTED, fn, "prompt rows (max_q_rows %d > 1) on an e4m3 global pool: the global "
+                "prompt-row kernel reads bf16 pages only", max_q_rows);
   if (!q || !out || !aligned(q, 16) || !aligned(out, 16)) return fail(GW_ERR_INVALID_ARG, fn, "q/out NULL or not 16-byte aligned");
   if (!cu_q_rows || !seq_lens || !block_table || !aligned(cu_q_rows, 4) || !aligned(seq_lens, 4) ||
       !aligned(block_table, 4))

@@ -159,17 +159,18 @@ cudaError_t launch_rope_cs(float* out, double theta, int rot_dim, int head_dim, 
 cudaError_t launch_bw_probe(const void* buf, int64_t chunks, int32_t* status, cudaStream_t st);
 cudaError_t launch_bw_probe_tma(const void* buf, int64_t pages, int32_t* status, cudaStream_t st);
 cudaError_t launch_wait_selftest(int32_t* status, int32_t* result, int64_t limit_ns, cudaStream_t st);
-// TMA descriptor of a bf16 LOCAL pool (rows of 256 elements in 4 chunks of 64;
-// row = ((page * kv_heads + head) * 2 + {K, V}) * 16 + token), box {64, 1, 16},
-// 128-byte swizzle.
+// TMA descriptor of a LOCAL pool: rows of 256 elements in 128-byte chunks
+// (4 chunks of 64 bf16, or 2 chunks of 128 e4m3); row = ((page * kv_heads +
+// head) * 2 + {K, V}) * 16 + token; box {one chunk, 1, 16 rows}, 128-byte
+// swizzle.
 constexpr int kPageTokens = 16;
-cudaError_t make_local_kv_map(const LocalArgs& a, CUtensorMap* map);
+cudaError_t make_local_kv_map(const LocalArgs& a, CUtensorMap* map, int dtype = GW_KV_BF16);
 cudaError_t launch_local_decode(int dtype, int group, const LocalArgs& a, cudaStream_t st);
 cudaError_t launch_global_decode(int layout, const LocalArgs& a, cudaStream_t st);
 cudaError_t launch_local_prompt(int dtype, int group, const LocalArgs& a, int max_q_rows, cudaStream_t st);
-// tcgen05 prompt-row kernel for local layers (bf16 pools); expects a.prompt_base
-// planned with 128 / group queries per tile
-cudaError_t launch_local_prompt_tc(int group, const LocalArgs& a, cudaStream_t st);
+// tcgen05 prompt-row kernel for local layers (bf16 or e4m3 pools); expects
+// a.prompt_base planned with 128 / group queries per tile
+cudaError_t launch_local_prompt_tc(int dtype, int group, const LocalArgs& a, cudaStream_t st);
 // tcgen05 prompt-row kernel for global layers; expects a.prompt_base planned
 // with 2 tiles (output-dim halves) per block of 128 / num_q_heads queries
 cudaError_t launch_global_prompt_tc(int layout, const LocalArgs& a, cudaStream_t st);

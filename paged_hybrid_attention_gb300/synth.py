@@ -19,6 +19,7 @@ layers per global layer):
               and the opt-in e4m3 folded pool of the same tokens.
   mixed       48 decode streams, L ~ U[1024, 16384], plus 4 new prompts of 2048
               rows appended and attended in the same step; both families.
+  mixed_e4m3  the mixed step with the local family on an e4m3 pool (N(0, 0.5)).
   chunked     32 decode streams, L ~ U[1024, 16384], plus 4 prompts continuing
               with a 1024-row chunk over U[4096, 16384] cached tokens (the
               chunked walk); both families.
@@ -104,6 +105,12 @@ def spec(name):
         loc = Family("local", "bf16", "local", 16, 256, 256, 1e4, 1024)
         glo = Family("global", "bf16", "folded", 1, 512, 128, 1e6, 0)
         return Spec(name, 1005, 32, lens, rows, {"local": loc, "global": glo}, 5, 1)
+    if name == "mixed_e4m3":
+        # the mixed step with the sliding family on its opt-in e4m3 pool
+        base = spec("mixed")
+        loc = Family("local", "e4m3", "local", 16, 256, 256, 1e4, 1024, sigma=0.5)
+        return Spec(name, base.seed, base.num_q_heads, base.lens, base.n_rows,
+                    {"local": loc, "global": base.families["global"]}, 5, 1)
     if name == "chunked":
         dec = _draw_lens(1006, 32, 1024, 16384)
         hist = _draw_lens(1106, 4, 4096, 16384)

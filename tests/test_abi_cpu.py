@@ -105,8 +105,7 @@ def test_attention_host_validation():
     assert "4096" in gw.last_error()
     e8 = _desc(dtype=gw.KV_E4M3)
     assert _local_call(e8, mq=1) != gw.GW_ERR_UNSUPPORTED
-    assert _local_call(e8, mq=2) == gw.GW_ERR_UNSUPPORTED             # prompt rows read bf16 pages only
-    assert "e4m3" in gw.last_error()
+    assert _local_call(e8, mq=2, ws_bytes=100) == gw.GW_ERR_WORKSPACE  # prompt rows on e4m3 local pools are served
     g = _desc(gw.LAYOUT_GLOBAL_FOLDED, kvh=1, hd=512, rd=128)
     assert _local_call(g) == gw.GW_ERR_INVALID_ARG                    # global pool on the local entry
     L = gw.lib()

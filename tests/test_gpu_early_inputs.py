@@ -43,9 +43,8 @@ def _attend(layer, pool, q, out, cu, lens, bt, ws, mq, status):
         gw.decode_attn_global(pool, q, out, cu, lens, bt, ws, max_q_rows=mq, dev_status=status)
 
 
-# prompt rows on an e4m3 pool are refused (GW_ERR_UNSUPPORTED), so e4m3 runs decode rows only
-@pytest.mark.parametrize("kind,mixed", [("local", False), ("local", True), ("e4m3", False), ("global", False),
-                                        ("global", True), ("full", False), ("full", True)])
+@pytest.mark.parametrize("kind,mixed", [("local", False), ("local", True), ("e4m3", False), ("e4m3", True),
+                                        ("global", False), ("global", True), ("full", False), ("full", True)])
 def test_early_inputs_same_bits(kind, mixed):
     layer = _layer(kind, mixed)
     fam, sp = layer.fam, layer.spec

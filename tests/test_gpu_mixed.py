@@ -96,12 +96,15 @@ def _all_rows(sp):
     return {s: list(range(int(n))) for s, n in enumerate(sp.n_rows) if n > 0}
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
 @pytest.mark.parametrize("kvh,hq", [(4, 4), (4, 8), (2, 8), (1, 8)])
 @pytest.mark.parametrize("window", [24, 1024])
-def test_local_prompt_rows(kvh, hq, window):
+def test_local_prompt_rows(kvh, hq, window, dtype):
+    """Prompt rows on bf16 and on e4m3 local pools (the e4m3 leg against the
+    oracle reading the same e4m3 bytes)."""
     lens = [40, 100, 300, 70, 9, 1]
     rows = [40, 1, 64, 5, 9, 1]          # new prompt, decode, continuation, short, new, decode
-    fam = synth.Family("local", "bf16", "local", kvh, 256, 256, 1e4, window)
+    fam = synth.Family("local", dtype, "local", kvh, 256, 256, 1e4, window, sigma=0.5 if dtype == "e4m3" else 1.0)
     layer = synth.Layer(synth.custom("lp", 61 + kvh + hq, hq, lens, rows, {"local": fam}), "local")
     pool, tab, status = _build(layer)
     out = G.attend(layer, pool, status=status)
@@ -126,20 +129,27 @@ def test_global_prompt_rows(layout, hq):
     _check(layer, out, tab, _all_rows(layer.spec))
 
 
-@pytest.mark.parametrize("key", ["local", "global"])
+@pytest.mark.parametrize("key", ["local", "global", "local_e4m3"])
 def test_decode_rows_of_mixed_call_equal_decode_only_bitwise(key):
+    """The mixed-step-against-serial gate: decode rows computed beside prompt
+    rows are bit-identical to a decode-only call, on bf16 pools and on the
+    e4m3 local pool."""
     sp = synth.spec("mixed")
+    fams = dict(sp.families)
+    if key == "local_e4m3":
+        fams["local"] = synth.Family("local", "e4m3", "local", 16, 256, 256, 1e4, 1024, sigma=0.5)
+        key = "local"
     # keep it small: 6 decode streams + 2 prompts of 300 rows
     lens = np.concatenate([sp.lens[:6], [300, 500]]).astype(np.int32)
     rows = np.concatenate([np.ones(6, np.int32), [300, 100]]).astype(np.int32)
-    mixed = synth.custom("mx", sp.seed, 32, lens, rows, sp.families)
+    mixed = synth.custom("mx", sp.seed, 32, lens, rows, fams)
     layer = synth.Layer(mixed, key)
     pool, tab, _ = _build(layer)
     out_mixed = G.attend(layer, pool)
     # the same decode rows, prompts dropped (zero rows)
     dec_rows = rows.copy()
     dec_rows[6:] = 0
-    dec = synth.custom("mx", sp.seed, 32, lens, dec_rows, sp.families)
+    dec = synth.custom("mx", sp.seed, 32, lens, dec_rows, fams)
     layer_d = synth.Layer(dec, key)
     layer_d.block_table = layer.block_table          # same pool, same pages
     q = G.bits_to_cuda_bf16(np.concatenate([layer.q(s) for s in range(6)]))
@@ -149,9 +159,10 @@ def test_decode_rows_of_mixed_call_equal_decode_only_bitwise(key):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("key", ["local", "global"])
+@pytest.mark.parametrize("key", ["local", "global", "local_e4m3"])
 def test_mixed_full_size_sampled(key):
-    layer = synth.Layer(synth.spec("mixed"), key)
+    layer = synth.Layer(synth.spec("mixed_e4m3" if key == "local_e4m3" else "mixed"),
+                        "local" if key == "local_e4m3" else key)
     pool, tab, status = _build(layer)
     out = G.attend(layer, pool, status=status)
     torch.cuda.synchronize()
