@@ -287,18 +287,24 @@ __global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kerne
     const Unit d = sm.ring[c_slot];
     if (c_i == 0) {
       const uint16_t* qrow = a.q + (static_cast<int64_t>(d.row) * a.num_q_heads + d.g * G) * 256 + lane * 8;
+      // a q value f16 cannot hold: bf16 magnitudes from 65536 (0x4780) up
+      // round to inf; the largest below, 65280, is exact in f16
+      bool q_big = false;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const uint4 qv = *reinterpret_cast<const uint4*>(qrow + h * 256);
         const uint32_t u[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i) {
           q16[h][i] = static_cast<uint32_t>(X::from_bf16(lo16(u[i]))) | (static_cast<uint32_t>(X::from_bf16(hi16(u[i]))) << 16);
+          q_big |= ((u[i] & 0x7FFFu) >= 0x4780u) || ((u[i] & 0x7FFF0000u) >= 0x47800000u);
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
         m[h] = -INFINITY;
         lsum[h] = 0.f;
       }
+      if (q_big) set_status(a.status, GW_DEV_Q_RANGE);
     }
     const int st = consumed % kStages;
     if (!mbar_wait(&sm.bar[st], (consumed / kStages) & 1, a.status)) {
