@@ -53,7 +53,7 @@ UNIT = "GB/s"
 # workload: (bytes, source file under csrc/, sha256)
 NCU_TRAFFIC = {
     "serving": (275542528, "attn_local.cu", "db9fb085d8075f8b289ad1d35df850b9606686f187eccb4dee26c40c180e501d"),
-    "fp8_local": (552907520, "attn_local.cu", "db9fb085d8075f8b289ad1d35df850b9606686f187eccb4dee26c40c180e501d"),
+    "fp8_local": (552973312, "attn_local_e4m3_tc.cu", "e348365c2bf236e2255d66c87103cc92c1406a3e1dab7e39b6f6144676afb399"),
     "long_global": (1354496512, "attn_global.cu", "f6add234ef69883f75cd07c7c8ad98348d3192bd7b1e56001c15c1040c3ccc69"),
 }
 

@@ -73,10 +73,6 @@ typedef int32_t gw_status;
 #define GW_DEV_TIMEOUT 16    /* a bounded wait gave up (work abandoned)       */
 #define GW_DEV_WORKSPACE 32  /* the step needs more split-KV partials than the
                                 workspace was sized for (nothing computed)    */
-#define GW_DEV_Q_RANGE 64    /* a decode row's q on an e4m3 local pool holds a
-                                bf16 value of magnitude >= 65536, which f16
-                                (the multiplicand format there) cannot hold:
-                                the row's output is not reliable          */
 
 /* ---- pool description --------------------------------------------------- */
 #define GW_KV_BF16 0
@@ -215,12 +211,11 @@ gw_status gw_rope_cs(float* rope_cs, double theta, int32_t rot_dim, int32_t head
  *   workspace    device scratch of at least gw_attn_workspace_bytes(...),
  *                256-byte aligned; contents need no initialisation.
  * On an e4m3 pool ([PR1012] "Description", "Verification": the sliding
- * family's fp8 pool serves decode and mixed steps alike) the prompt-row
- * contractions run on the e4m3 tiles as stored; each q row and softmax
- * weight enters as a sum of two e4m3 terms (q after an exact power-of-two
- * scaling), which carries it at about bf16 precision.  Decode rows on e4m3
- * pools round q to f16 once per unit: |q| must stay below 65536 (f16's
- * range), and a q outside it is reported as GW_DEV_Q_RANGE.
+ * family's fp8 pool serves decode and mixed steps alike) the contractions of
+ * decode and prompt rows run on the e4m3 tiles as stored; each q row and
+ * softmax weight enters as a sum of two e4m3 terms (q after an exact
+ * power-of-two scaling per head or row), which carries it at about bf16
+ * precision for any q whose logits are finite in fp32.
  *
  * Errors: GW_ERR_INVALID_ARG, GW_ERR_WORKSPACE, GW_ERR_UNSUPPORTED
  * (num_q_heads / kv_heads not in {1,2,4,8}; batch > 4096, since the decode

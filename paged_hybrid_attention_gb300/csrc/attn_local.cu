@@ -5,9 +5,11 @@
 // grouped KV heads, each in its own pool of 16-token pages; every active
 // request advances one token per batched step.  "feat(gemma4): the sliding
 // family serves an opt in fp8 KV pool", "Description": the pool may hold
-// e4m3 at scale 1.0; here it is widened to fp32 on the load path.
+// e4m3 at scale 1.0; those pools are served by the tcgen05 kernel of
+// attn_local_e4m3_tc.cu, this file holds the bf16 kernel.
 //
-// Split-KV flash decoding, common to both pool types:
+// Split-KV flash decoding (the plan, the partials and the combine are also
+// the e4m3 kernel's):
 //   * Work unit = (sequence, KV head, chunk of up to 8 pages of the window).
 //     The split depends on the sequence's own length only.
 //   * Persistent CTAs, one per SM, of independent warps.  Every CTA computes
@@ -26,50 +28,14 @@
 // head (K and V, 16 KB) brought by 8 TMA tensor copies into 128-byte-swizzled
 // shared memory; q.K^T and P.V run on warp-level tensor cores (mma.sync
 // m16n8k16, the G heads of the group as rows) with P kept in registers.
-//
-// e4m3 pools (local_decode_kernel, 12 warps for G <= 4): 8 KiB stages of 16
-// tokens with cp.async.bulk; lane l owns head dims [8l, 8l+8); products use
-// the mixed-precision fma.rn.f32.f16 after one paired e4m3x2 -> f16x2
-// conversion (no widening to fp32); q.K partial dot products are reduced
-// across lanes with a transpose-reduction whose token order is permuted by
-// lane bits (one shuffle + add per value and level).  The conversions double
-// the instructions per byte, so the kernel is bound by issue latency and runs
-// more warps than the HBM stream alone would need.
 #include "plan.cuh"
 #include "tma.cuh"
 
 namespace gw {
 namespace {
 
-// warps per CTA of the e4m3 kernel: 12 where the register budget allows
-template <int DT, int G>
-constexpr int warps_for() { return G <= 4 ? 12 : 8; }
-constexpr int kStageBytes = 8192;
-
 struct Unit {
   int32_t s, g, hp_lo, n, tok_lo, tok_hi, unit, row;
-};
-
-template <int kStages>
-struct __align__(128) WarpSmem {
-  static constexpr int kRing = kStages + 2;
-  uint8_t stage[kStages][kStageBytes];
-  uint64_t bar[kStages];
-  int32_t valid[kStages];
-  int32_t pad_;
-  Unit ring[kRing];
-  uint16_t pbuf[16 * 8];  // p of (token, head) in the 16-bit multiplicand format
-};
-
-template <int DT>
-struct Traits {
-  static constexpr int kEs = DT == GW_KV_BF16 ? 2 : 1;
-  static constexpr int kTok = kStageBytes / (2 * 256 * kEs);  // tokens per stage: 8 / 16
-  static constexpr int kSpp = kPage / kTok;                   // stages per page: 2 / 1
-  static constexpr int kLevels = kTok == 16 ? 4 : 3;          // halving levels of the reduction
-  static constexpr int kChunk = DT == GW_KV_BF16 ? kLocalChunkPagesBf16 : kLocalChunkPagesE4m3;
-  static constexpr int kStages = 2;  // copy-ring depth per warp
-  using Smem = WarpSmem<kStages>;
 };
 
 template <class T>
@@ -93,61 +59,6 @@ __device__ __forceinline__ Unit decode_unit(const LocalArgs& a, const int32_t* u
   d.unit = u;
   d.row = a.cu_q_rows[lo];
   return d;
-}
-
-// Mixed-precision multiply-add with fp32 accumulation (sm_100+): d = a * b + c
-// with 16-bit a, b taken straight from the halves of packed registers.  The
-// product of two 16-bit floats is exact in fp32, so this equals an fp32 FMA on
-// the widened values, without spending an instruction on the widening.
-// e4m3 pages are widened to f16 by the paired e4m3x2 -> f16x2 conversion and
-// multiply in f16 (q is rounded to f16 once per unit, exact for |q| in the
-// f16 normal range).
-template <int DT>
-struct Mix;
-template <>
-struct Mix<GW_KV_E4M3> {
-  __device__ __forceinline__ static float fma(uint16_t a, uint16_t b, float c) {
-    float d;
-    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
-    return d;
-  }
-  __device__ __forceinline__ static uint16_t from_f32(float x) { return __half_as_ushort(__float2half_rn(x)); }
-  __device__ __forceinline__ static float to_f32(uint16_t x) { return __half2float(__ushort_as_half(x)); }
-  __device__ __forceinline__ static uint16_t from_bf16(uint16_t x) {
-    return __half_as_ushort(__float2half_rn(__uint_as_float(static_cast<uint32_t>(x) << 16)));
-  }
-  __device__ __forceinline__ static void row(const uint8_t* base, int lane, uint32_t (&w)[4]) {
-    const uint2 v = *reinterpret_cast<const uint2*>(base + lane * 8);
-    const uint32_t u[2] = {v.x, v.y};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[i] & 0xFFFFu), __NV_E4M3);
-      __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u[i] >> 16), __NV_E4M3);
-      w[2 * i] = *reinterpret_cast<uint32_t*>(&lo);
-      w[2 * i + 1] = *reinterpret_cast<uint32_t*>(&hi);
-    }
-  }
-};
-
-__device__ __forceinline__ uint16_t lo16(uint32_t w) { return static_cast<uint16_t>(w & 0xFFFFu); }
-__device__ __forceinline__ uint16_t hi16(uint32_t w) { return static_cast<uint16_t>(w >> 16); }
-
-// Transpose-reduction over the 32 lanes of x[N] (N = tokens per stage) whose
-// entry j holds token j ^ perm(lane).  Each halving level keeps the lower half
-// and adds the partner's upper half; afterwards x[0] is the full sum for token
-// perm(lane), replicated over the remaining butterfly lanes.
-template <int N, int O>
-__device__ __forceinline__ void xreduce(float* x) {
-  if constexpr (O >= 1) {
-    if constexpr (N > 1) {
-#pragma unroll
-      for (int i = 0; i < N / 2; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i + N / 2], O);
-      xreduce<N / 2, O / 2>(x);
-    } else {
-      x[0] += __shfl_xor_sync(0xffffffffu, x[0], O);
-      xreduce<1, O / 2>(x);
-    }
-  }
 }
 
 // Warps per CTA that take units.  Units are dealt in rounds of warps x CTAs
@@ -176,227 +87,6 @@ template <int kChunk>
 __device__ __forceinline__ void local_plan(const LocalArgs& a, int32_t* ub, bool publish) {
   plan_in_smem(a, ub, ub + kMaxBatch + 1, [&](int L) { return a.kv_heads * local_chunks(L, a.window, kChunk); },
                publish);
-}
-
-template <int DT, int G>
-__global__ void __launch_bounds__(warps_for<DT, G>() * 32, 1) local_decode_kernel(const LocalArgs a) {
-  constexpr int kWarps = warps_for<DT, G>();
-  using T = Traits<DT>;
-  constexpr int kTok = T::kTok;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kStages = T::kStages, kRing = T::Smem::kRing;
-  typename T::Smem& sm = reinterpret_cast<typename T::Smem*>(smem_raw)[warp];
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < kStages; ++i) mbar_init(&sm.bar[i], 1);
-    fence_mbar_init();
-  }
-  int32_t* ub = reinterpret_cast<int32_t*>(smem_raw + sizeof(typename T::Smem) * kWarps);
-  // With early inputs the plan and the first units' page numbers are read
-  // before the wait on the previous kernel (gw_set_early_inputs).
-  const bool early = a.early_inputs != 0;
-  if (!early) {
-    pdl_wait();
-    pdl_trigger();
-  }
-  local_plan<T::kChunk>(a, ub, !early);
-  const int total_units = ub[a.batch];
-  if (total_units > a.max_units) {
-    if (early) pdl_wait();
-    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.status, GW_DEV_WORKSPACE);
-    return;
-  }
-  // units are dealt round-robin over the warps, SM-minor, so every SM gets
-  // an equal share of each round
-  const int n_active = active_warps(total_units, kWarps);
-  if (warp >= n_active) return;
-  const uint64_t pol = policy_evict_first();
-  const int n_warps = gridDim.x * n_active;
-  int next_u = warp * gridDim.x + blockIdx.x;
-  const int64_t head_bytes = 2LL * kPage * 256 * T::kEs;  // K + V of one KV head in one page
-  const int perm = (lane >> (5 - T::kLevels)) & (kTok - 1);
-  const bool canon = (lane & ((1 << (5 - T::kLevels)) - 1)) == 0;
-
-  int f_slot = 0, f_i = 0;
-  bool f_done = false, have_next = false;
-  uint32_t issued = 0, consumed = 0;
-  // Lane i holds the physical page of page i of the unit being issued (cur)
-  // and of the unit after it (nxt), loaded when the unit before starts
-  // issuing, so no stage issue waits for a block-table load.
-  int32_t pg_cur = -1, pg_nxt = -1;
-
-  auto grab = [&](int slot, int32_t& pg) -> bool {
-    const int u = next_u;
-    next_u += n_warps;
-    if (u >= total_units) return false;
-    const Unit d = decode_unit<T>(a, ub, u);
-    if (lane == 0) sm.ring[slot] = d;
-    const int lp0 = d.hp_lo / T::kSpp, np = (d.hp_lo + d.n - 1) / T::kSpp + 1 - lp0;
-    pg = lane < np ? a.block_table[static_cast<int64_t>(d.s) * a.max_pages + lp0 + lane] : -1;
-    __syncwarp();
-    return true;
-  };
-
-  auto issue = [&]() {
-    const Unit d = sm.ring[f_slot];
-    const int st = issued % kStages;
-    const int hp = d.hp_lo + f_i;
-    const int lp = hp / T::kSpp, half = hp % T::kSpp;
-    const int32_t phys = __shfl_sync(0xffffffffu, pg_cur, lp - d.hp_lo / T::kSpp);
-    if (lane == 0) {
-      if (phys < 0 || phys >= a.num_pages) {
-        sm.valid[st] = 0;
-        set_status(a.status, GW_DEV_PAGE_RANGE);
-        mbar_arrive(&sm.bar[st]);
-      } else {
-        sm.valid[st] = 1;
-        const uint8_t* kb = a.pool + (static_cast<int64_t>(phys) * a.kv_heads + d.g) * head_bytes +
-                            static_cast<int64_t>(half) * kTok * 256 * T::kEs;
-        mbar_arrive_expect_tx(&sm.bar[st], kStageBytes);
-        bulk_g2s(sm.stage[st], kb, kStageBytes / 2, &sm.bar[st], pol);
-        bulk_g2s(sm.stage[st] + kStageBytes / 2, kb + kPage * 256 * T::kEs, kStageBytes / 2, &sm.bar[st], pol);
-      }
-    }
-    ++issued;
-    if (++f_i == d.n) {
-      f_i = 0;
-      f_slot = (f_slot + 1) % kRing;
-      f_done = !have_next;
-      if (have_next) {
-        pg_cur = pg_nxt;
-        have_next = grab((f_slot + 1) % kRing, pg_nxt);
-      }
-    }
-  };
-
-  f_done = !grab(0, pg_cur);
-  if (!f_done) have_next = grab(1, pg_nxt);
-  if (early) {
-    pdl_wait();
-    pdl_trigger();
-    publish_plan(a, ub, threadIdx.x, n_active * 32);
-  }
-  while (!f_done && issued - consumed < kStages) issue();
-
-  using X = Mix<DT>;
-  uint32_t q16[G][4];  // this lane's 8 q dims per head, packed 16-bit pairs
-  float o[G][8], m[G], lsum[G];
-  int c_slot = 0, c_i = 0;
-  while (consumed < issued) {
-    const Unit d = sm.ring[c_slot];
-    if (c_i == 0) {
-      const uint16_t* qrow = a.q + (static_cast<int64_t>(d.row) * a.num_q_heads + d.g * G) * 256 + lane * 8;
-      // a q value f16 cannot hold: bf16 magnitudes from 65536 (0x4780) up
-      // round to inf; the largest below, 65280, is exact in f16
-      bool q_big = false;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const uint4 qv = *reinterpret_cast<const uint4*>(qrow + h * 256);
-        const uint32_t u[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          q16[h][i] = static_cast<uint32_t>(X::from_bf16(lo16(u[i]))) | (static_cast<uint32_t>(X::from_bf16(hi16(u[i]))) << 16);
-          q_big |= ((u[i] & 0x7FFFu) >= 0x4780u) || ((u[i] & 0x7FFF0000u) >= 0x47800000u);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
-        m[h] = -INFINITY;
-        lsum[h] = 0.f;
-      }
-      if (q_big) set_status(a.status, GW_DEV_Q_RANGE);
-    }
-    const int st = consumed % kStages;
-    if (!mbar_wait(&sm.bar[st], (consumed / kStages) & 1, a.status)) {
-      // abandon: drain whatever is still in flight (bounded) and leave
-      for (uint32_t k = consumed + 1; k < issued; ++k) mbar_wait(&sm.bar[k % kStages], (k / kStages) & 1, nullptr);
-      return;
-    }
-    const uint8_t* Ks = sm.stage[st];
-    const uint8_t* Vs = Ks + kStageBytes / 2;
-    const int t0 = (d.hp_lo + c_i) * kTok;
-
-    // ---- logits: x[h][j] = q_h . K[j ^ perm] over this lane's 8 dims
-    float x[G][kTok];
-#pragma unroll
-    for (int j = 0; j < kTok; ++j) {
-      uint32_t w[4];
-      X::row(Ks + (j ^ perm) * 256 * T::kEs, lane, w);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc = X::fma(lo16(q16[h][i]), lo16(w[i]), acc);
-          acc = X::fma(hi16(q16[h][i]), hi16(w[i]), acc);
-        }
-        x[h][j] = acc;
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) xreduce<kTok, 16>(x[h]);
-
-    const int tabs = t0 + perm;
-    const bool valid = sm.valid[st] && tabs >= d.tok_lo && tabs < d.tok_hi;
-    uint16_t p16[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float s = valid ? x[h][0] * a.scale_log2 : -INFINITY;
-      float mx = s;
-#pragma unroll
-      for (int O = 1 << (5 - T::kLevels); O < 32; O <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, O));
-      const float mnew = fmaxf(m[h], mx);
-      const float alpha = mnew == -INFINITY ? 1.f : ex2(m[h] - mnew);
-      p16[h] = X::from_f32(valid ? ex2(s - mnew) : 0.f);
-      m[h] = mnew;
-      // l sums the rounded weights P.V multiplies by
-      lsum[h] = lsum[h] * alpha + (canon ? X::to_f32(p16[h]) : 0.f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[h][i] *= alpha;
-    }
-    if (canon) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) sm.pbuf[perm * G + h] = p16[h];
-    }
-    __syncwarp();
-
-    // ---- o += p[t] * V[t]; masked tokens are skipped, not multiplied by
-    // zero: their bytes may be anything the pool held (even NaN patterns)
-    const bool stage_ok = sm.valid[st] != 0;
-#pragma unroll
-    for (int t = 0; t < kTok; ++t) {
-      if (!stage_ok || t0 + t < d.tok_lo || t0 + t >= d.tok_hi) continue;
-      uint32_t w[4];
-      X::row(Vs + t * 256 * T::kEs, lane, w);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const uint16_t ph = sm.pbuf[t * G + h];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          o[h][2 * i] = X::fma(ph, lo16(w[i]), o[h][2 * i]);
-          o[h][2 * i + 1] = X::fma(ph, hi16(w[i]), o[h][2 * i + 1]);
-        }
-      }
-    }
-    __syncwarp();
-    ++consumed;
-    if (++c_i == d.n) {
-      // ---- unit done: write the unnormalised partial
-      float* po = a.part_o + static_cast<int64_t>(d.unit) * G * 256 + lane * 8;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float l = lsum[h];
-#pragma unroll
-        for (int O = 1; O < 32; O <<= 1) l += __shfl_xor_sync(0xffffffffu, l, O);
-        *reinterpret_cast<float4*>(po + h * 256) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-        *reinterpret_cast<float4*>(po + h * 256 + 4) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
-        if (lane == h) a.part_ml[static_cast<int64_t>(d.unit) * G + h] = make_float2(m[h], l);
-      }
-      c_i = 0;
-      c_slot = (c_slot + 1) % kRing;
-    }
-    while (!f_done && issued - consumed < kStages) issue();
-  }
 }
 
 
@@ -705,45 +395,17 @@ cudaError_t launch_tc(const LocalArgs& a, cudaStream_t st) {
   return launch_combine(a, G, 256, local_max_chunks(a.max_pages, a.window, TcTraits::kChunk), true, st);
 }
 
-template <int DT, int G>
-cudaError_t launch_typed(const LocalArgs& a, cudaStream_t st) {
-  using T = Traits<DT>;
-  cudaError_t e;
-  constexpr int kWarps = warps_for<DT, G>();
-  const size_t smem = sizeof(typename T::Smem) * kWarps + sizeof(int32_t) * (kMaxBatch + 1 + 32);
-  auto kern = local_decode_kernel<DT, G>;
-  e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kWarps * 32), smem, st, a);
-  if (e != cudaSuccess) return e;
-  return launch_combine(a, G, 256, local_max_chunks(a.max_pages, a.window, T::kChunk), true, st);
-}
-
-template <int DT>
-cudaError_t launch_dt(int group, const LocalArgs& a, cudaStream_t st) {
-  if constexpr (DT == GW_KV_BF16) {
-    switch (group) {
-      case 1: return launch_tc<1>(a, st);
-      case 2: return launch_tc<2>(a, st);
-      case 4: return launch_tc<4>(a, st);
-      case 8: return launch_tc<8>(a, st);
-    }
-    return cudaErrorInvalidValue;
-  } else {
-    switch (group) {
-      case 1: return launch_typed<DT, 1>(a, st);
-      case 2: return launch_typed<DT, 2>(a, st);
-      case 4: return launch_typed<DT, 4>(a, st);
-      case 8: return launch_typed<DT, 8>(a, st);
-    }
-    return cudaErrorInvalidValue;
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_local_decode(int dtype, int group, const LocalArgs& a, cudaStream_t st) {
-  return dtype == GW_KV_BF16 ? launch_dt<GW_KV_BF16>(group, a, st) : launch_dt<GW_KV_E4M3>(group, a, st);
+  if (dtype != GW_KV_BF16) return launch_local_decode_e4m3_tc(group, a, st);
+  switch (group) {
+    case 1: return launch_tc<1>(a, st);
+    case 2: return launch_tc<2>(a, st);
+    case 4: return launch_tc<4>(a, st);
+    case 8: return launch_tc<8>(a, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace gw

@@ -97,12 +97,6 @@ __device__ __forceinline__ void split_e4m3(float x0, float x1, uint32_t& hi, uin
   }
 }
 
-// Shared-memory descriptor of a 128-byte-swizzled operand (atoms of 8 rows x
-// 128 B, 1024 B apart along the 8-row direction).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo) {
-  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
 
 __device__ __forceinline__ int prompt_seq(const int32_t* base, int batch, int t) {
   int lo = 0, hi = batch;
@@ -260,7 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // a K-step is 32 bytes of each key row: 16 bf16 or 32 e4m3 dims
 #pragma unroll
         for (int ks = 0; ks < 16 / (kE4 ? 2 : 1); ++ks) {
-          const uint64_t bd = sw128_desc(ka + (ks >> 2) * kPlane + (ks & 3) * 32, 16);
+          const uint64_t bd = tc::smem_desc_sw128(ka + (ks >> 2) * kPlane + (ks & 3) * 32, 16);
           if constexpr (kE4) {
             // S = (q_hi + q_lo) . K^T: q_hi at Q columns 0..63, q_lo at 64..127
             tc::mma_e4m3_ts_warp(tmem + kColS + 64 * sb, tmem + kColQ + 8 * ks, bd, id_s, ks > 0);
@@ -309,14 +303,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // P_hi at S columns 0..15, P_lo at 16..31
 #pragma unroll
           for (int kk = 0; kk < kTN / 32; ++kk) {
-            const uint64_t bd = sw128_desc(va + kk * 4096, kPlane);
+            const uint64_t bd = tc::smem_desc_sw128(va + kk * 4096, kPlane);
             tc::mma_e4m3_ts_warp(tmem + kColO, tmem + kColS + 64 * sb + 8 * kk, bd, id_o, !(j == 0 && kk == 0));
             tc::mma_e4m3_ts_warp(tmem + kColO, tmem + kColS + 64 * sb + 16 + 8 * kk, bd, id_o, true);
           }
         } else {
 #pragma unroll
           for (int kk = 0; kk < kTN / 16; ++kk)
-            tc::mma_bf16_ts_warp(tmem + kColO, tmem + kColS + 64 * sb + 8 * kk, sw128_desc(va + kk * 2048, kPlane),
+            tc::mma_bf16_ts_warp(tmem + kColO, tmem + kColS + 64 * sb + 8 * kk, tc::smem_desc_sw128(va + kk * 2048, kPlane),
                                  id_o, !(j == 0 && kk == 0));
         }
         tc::commit_warp(&sm.vempty[b]);

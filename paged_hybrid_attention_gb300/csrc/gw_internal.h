@@ -166,6 +166,8 @@ cudaError_t launch_wait_selftest(int32_t* status, int32_t* result, int64_t limit
 constexpr int kPageTokens = 16;
 cudaError_t make_local_kv_map(const LocalArgs& a, CUtensorMap* map, int dtype = GW_KV_BF16);
 cudaError_t launch_local_decode(int dtype, int group, const LocalArgs& a, cudaStream_t st);
+// tcgen05 decode kernel (kind::f8f6f4) for e4m3 LOCAL pools, plus the combine
+cudaError_t launch_local_decode_e4m3_tc(int group, const LocalArgs& a, cudaStream_t st);
 cudaError_t launch_global_decode(int layout, const LocalArgs& a, cudaStream_t st);
 cudaError_t launch_local_prompt(int dtype, int group, const LocalArgs& a, int max_q_rows, cudaStream_t st);
 // tcgen05 prompt-row kernel for local layers (bf16 or e4m3 pools); expects

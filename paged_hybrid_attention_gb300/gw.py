@@ -22,7 +22,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 # ---- constants (mirror include/gw.h) -----------------------------------------
 GW_OK, GW_ERR_INVALID_ARG, GW_ERR_UNSUPPORTED, GW_ERR_WORKSPACE, GW_ERR_CUDA = 0, 1, 2, 3, 4
 GW_DEV_SLOT_RANGE, GW_DEV_POS_RANGE, GW_DEV_PAGE_RANGE, GW_DEV_LEN_RANGE = 1, 2, 4, 8
-GW_DEV_TIMEOUT, GW_DEV_WORKSPACE, GW_DEV_Q_RANGE = 16, 32, 64
+GW_DEV_TIMEOUT, GW_DEV_WORKSPACE = 16, 32
 KV_BF16, KV_E4M3 = 0, 1
 LAYOUT_LOCAL, LAYOUT_GLOBAL_FOLDED, LAYOUT_GLOBAL_FULL, LAYOUT_GLOBAL_FOLDED_E4M3 = 0, 1, 2, 3
 LAYOUTS = {"local": LAYOUT_LOCAL, "folded": LAYOUT_GLOBAL_FOLDED, "full": LAYOUT_GLOBAL_FULL,
