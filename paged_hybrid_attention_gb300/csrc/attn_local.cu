@@ -237,6 +237,12 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
   f_done = !grab(0, pg_cur);
   if (!f_done) have_next = grab(1, pg_nxt);
   if (early) {
+    // Warm L2 with the first unit's first pages (K and V of the unit's KV
+    // head, 16 KB each) while the previous kernel finishes: a prefetch only
+    // fills L2, which that kernel's writes (the append of the sequence's
+    // last row) keep coherent; the copies to shared memory follow the wait.
+    if (!f_done && lane < kTcStages && pg_cur >= 0 && pg_cur < a.num_pages)
+      prefetch_l2(a.pool + ((static_cast<int64_t>(pg_cur) * a.kv_heads + sm.ring[0].g) * 2) * kPage * 512, kTcStage);
     pdl_wait();
     pdl_trigger();
     publish_plan(a, ub, threadIdx.x, n_active * 32);
