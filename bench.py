@@ -73,6 +73,9 @@ def parse():
     ap.add_argument("--bucket", type=int, default=0,
                     help="pad every layer's step to this many sequence slots, as a CUDA graph captured for a "
                          "batch bucket runs a smaller batch (0: no padding)")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="append each step's K/V rows with gw_kv_append before the decode call, instead of inside "
+                         "it (gw_append_decode_attn_*, used where the layer's step has decode rows only)")
     ap.add_argument("--no-early-inputs", action="store_true",
                     help="decode kernels read their plan inputs only after the previous kernel has finished "
                          "(gw_set_early_inputs(0)); by default they read them while it runs, which holds here "
@@ -177,6 +180,7 @@ class GpuLayer:
                                      max(1, fam.window), device=dev)
         self.kv_bytes = kv_bytes(layer)
         self.prompt_flops = prompt_flops(layer)
+        self.fused = False
         if bucket > len(sp.lens):
             self._pad_to_bucket(gw, bucket, dev)
 
@@ -213,7 +217,19 @@ class GpuLayer:
                 if fam.kind == "local" else v
             gw.kv_append(self.pool, k, v, s_, p_, self.table, self.status)
 
+    def can_fuse(self, gw):
+        """Whether this layer's step can append inside its decode call
+        (gw_append_decode_attn_*): decode rows only, on a pool it serves."""
+        return self.max_q_rows == 1 and self.fam.kind == "local" and self.fam.dtype == "bf16"
+
     def attend(self, gw, stream):
+        if self.fused:
+            # the step's rows appended by the decode call itself (re-appending
+            # the same bytes when the call is replayed)
+            gw.append_decode_attn_local(self.pool, self.k_new, self.v_new, self.table, self.q, self.out, self.cu,
+                                        self.lens, self.bt, self.ws, self.fam.window, dev_status=self.status,
+                                        stream=stream)
+            return
         if self.fam.kind == "local":
             gw.decode_attn_local(self.pool, self.q, self.out, self.cu, self.lens, self.bt, self.ws, self.fam.window,
                                  max_q_rows=self.max_q_rows, dev_status=self.status, stream=stream)
@@ -249,7 +265,9 @@ class GpuLayer:
                                   max_q_rows=self.max_q_rows, dev_status=self.status, stream=stream)
 
     def run(self, gw, stream, ev=None):
-        gw.kv_append(self.pool, self.k_new, self.v_new, self.slot_new, self.pos_new, self.table, self.status, stream)
+        if not self.fused:
+            gw.kv_append(self.pool, self.k_new, self.v_new, self.slot_new, self.pos_new, self.table, self.status,
+                         stream)
         if ev is not None:
             ev[0].record(stream)
         self.attend(gw, stream)
@@ -702,6 +720,8 @@ def main():
     sp, layers = workload_layers(args.workload, rank)
     gen = torch.Generator(device=dev).manual_seed(sp.seed + 17 * rank)
     glayers = [GpuLayer(l, gw, gen, dev, bucket=args.bucket) for l in layers]
+    for g in glayers:
+        g.fused = not args.separate_append and g.can_fuse(gw)
     arena_in = Arena(glayers, GpuLayer.INPUTS, dev)   # the step's inputs, one upload
     arena_out = Arena(glayers, ("out",), dev)         # the step's outputs, one download
     torch.cuda.synchronize()
@@ -709,7 +729,8 @@ def main():
     step_bytes = sum(g.kv_bytes for g in glayers)
     locals_ = [g for g in glayers if g.fam.kind == "local"]
     dom = locals_ if locals_ else glayers
-    dom_name = "local decode attention call (split-KV decode + combine)" if locals_ else \
+    dom_name = ("local decode attention call (%ssplit-KV decode + combine)"
+                % ("the step's append inside the decode kernel, " if any(g.fused for g in dom) else "")) if locals_ else \
         "global decode attention call (tcgen05 decode with in-kernel plan + combine)"
     dom_bytes = statistics.mean(g.kv_bytes for g in dom)
 
@@ -1001,9 +1022,10 @@ def main():
     cpu = None
     if not args.no_cpu:
         cpu = cpu_baseline(args.workload, pool_budget_s=12.0, single_budget_s=8.0)
-    # gw kernels per layer: append, decode (split plan computed in-kernel) and
-    # combine; prompt rows add a tile plan and the prompt kernel
-    launches_per_step = sum(1 + 2 + (2 if g.max_q_rows > 1 else 0) for g in glayers)
+    # gw kernels per layer: append (unless the decode kernel appends), decode
+    # (split plan computed in-kernel) and combine; prompt rows add a tile plan
+    # and the prompt kernel
+    launches_per_step = sum((0 if g.fused else 1) + 2 + (2 if g.max_q_rows > 1 else 0) for g in glayers)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms, "steps_per_s": 1000.0 / ms, "higher_is_better": True, "scaling": "weak",
@@ -1015,6 +1037,8 @@ def main():
                    "batch": int(len(sp.lens)), "kv_bytes_per_step": step_bytes, "q_heads": sp.num_q_heads,
                    "bucket": args.bucket if args.bucket > len(sp.lens) else None,
                    "early_inputs": not args.no_early_inputs,
+                   "append": ("inside the decode call (%d of %d layers)" % (sum(g.fused for g in glayers), len(glayers))
+                              if any(g.fused for g in glayers) else "gw_kv_append before each decode call"),
                    "l2": "inputs larger than L2: %.2f GB of KV read per step" % (step_bytes / 1e9),
                    "parallelism": "dp%d (sequences sharded, no collective)" % world},
         "roofline": roofline,

@@ -229,6 +229,34 @@ gw_status gw_decode_attn_local(const gw_kv_pool* pool, const void* q, void* out,
                                int32_t* dev_status, void* stream);
 
 /*
+ * gw_append_decode_attn_local - a decode step's append and attention in one
+ * call: the same result as gw_kv_append of each decode row's K/V followed by
+ * gw_decode_attn_local with max_q_rows = 1.
+ *
+ * [pegainfer] "Scheduling" (every active request advances one token per
+ * batched step) and "Architecture notes" (local RoPE over all 256 dims,
+ * theta 10k).  Sequence b with one row (cu_q_rows[b+1] - cu_q_rows[b] == 1)
+ * appends k[r], v[r] (r = cu_q_rows[b]; [rows][kv_heads][256] bf16) at
+ * position pos = seq_lens[b] - 1, in page block_table[b][pos / 16] at offset
+ * pos % 16 - the slot and pos gw_kv_append would be given - with
+ * gw_kv_append's rotation and rounding, so the pool holds the same bytes;
+ * then that row attends over its window, the new key included.  Sequences
+ * without a row are skipped.  The kernel that decodes a KV head's last chunk
+ * writes its row before reading that page, so no second kernel and no
+ * wait between the two.  rope_cs and max_pos as for gw_kv_append.  A row
+ * with pos >= max_pos is not written (GW_DEV_POS_RANGE); a bad page entry is
+ * reported as by gw_decode_attn_local.  Serves bf16 pools.
+ * Errors: those of gw_decode_attn_local; GW_ERR_INVALID_ARG (k, v, rope_cs
+ * NULL or not 16-byte aligned, max_pos < 1); GW_ERR_UNSUPPORTED (an e4m3
+ * pool).
+ */
+gw_status gw_append_decode_attn_local(const gw_kv_pool* pool, const void* k, const void* v, const float* rope_cs,
+                                      int32_t max_pos, const void* q, void* out, int32_t num_q_heads, int32_t batch,
+                                      const int32_t* cu_q_rows, const int32_t* seq_lens, const int32_t* block_table,
+                                      int32_t max_pages_per_seq, int32_t window, float scale, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * gw_decode_attn_global - global attention on a GLOBAL_FOLDED, GLOBAL_FULL or
  * GLOBAL_FOLDED_E4M3 pool: as gw_decode_attn_local with no window
  * (j in [0, p]) and head dim 512.

@@ -28,6 +28,7 @@
 // head (K and V, 16 KB) brought by 8 TMA tensor copies into 128-byte-swizzled
 // shared memory; q.K^T and P.V run on warp-level tensor cores (mma.sync
 // m16n8k16, the G heads of the group as rows) with P kept in registers.
+#include "append_row.cuh"
 #include "plan.cuh"
 #include "tma.cuh"
 
@@ -36,6 +37,7 @@ namespace {
 
 struct Unit {
   int32_t s, g, hp_lo, n, tok_lo, tok_hi, unit, row;
+  int32_t last;  // the sequence's last chunk (its range ends at the sequence's end)
 };
 
 template <class T>
@@ -58,6 +60,7 @@ __device__ __forceinline__ Unit decode_unit(const LocalArgs& a, const int32_t* u
   d.n = (d.tok_hi - 1) / T::kTok + 1 - d.hp_lo;
   d.unit = u;
   d.row = a.cu_q_rows[lo];
+  d.last = d.tok_hi == L;
   return d;
 }
 
@@ -146,19 +149,22 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 }
 
 template <int G>
-__global__ void __launch_bounds__(kTcWarps * 32, 1)
+__global__ void __launch_bounds__(kTcWarps * 32 + 32, 1)
     local_decode_tc_kernel(const LocalArgs a, const __grid_constant__ CUtensorMap kv_map) {
   using T = TcTraits;
   constexpr int kTok = T::kTok;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  TcWarpSmem& sm = reinterpret_cast<TcWarpSmem*>(smem_raw)[warp];
-  if (lane == 0) {
+  TcWarpSmem& sm = reinterpret_cast<TcWarpSmem*>(smem_raw)[warp < kTcWarps ? warp : 0];
+  if (lane == 0 && warp < kTcWarps) {
 #pragma unroll
     for (int i = 0; i < kTcStages; ++i) mbar_init(&sm.bar[i], 1);
     fence_mbar_init();
   }
   int32_t* ub = reinterpret_cast<int32_t*>(smem_raw + sizeof(TcWarpSmem) * kTcWarps);
+  // fused append: units of this CTA (in order) whose rows are written
+  int32_t* app_done = ub + kMaxBatch + 1 + 32;
+  if (threadIdx.x == 0) *app_done = 0;
   // With early inputs the plan and the first units' page numbers are read
   // before the wait on the previous kernel (gw_set_early_inputs).
   const bool early = a.early_inputs != 0;
@@ -171,6 +177,42 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
   if (total_units > a.max_units) {
     if (early) pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.status, GW_DEV_WORKSPACE);
+    return;
+  }
+  if (warp == kTcWarps) {
+    // ---- fused append (launched only with one): the step's K/V row of each
+    // (sequence, KV head) whose last chunk this CTA decodes, at position
+    // L - 1, in the order of the CTA's units; the decode warp of such a unit
+    // waits for it before copying the unit's last page.
+    if (early) {
+      pdl_wait();
+      pdl_trigger();
+    }
+    for (int j = 0;; ++j) {
+      const int u = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
+      if (u >= total_units) break;
+      const int s = plan_seq(ub, a.batch, u);
+      const int nc = (ub[s + 1] - ub[s]) / a.kv_heads;
+      const int r = u - ub[s];
+      if (r % nc == nc - 1) {
+        const int pos = a.seq_lens[s] - 1;
+        const int32_t page = a.block_table[static_cast<int64_t>(s) * a.max_pages + pos / kPage];
+        if (pos >= a.max_pos) {
+          if (lane == 0) set_status(a.status, GW_DEV_POS_RANGE);
+        } else if (page >= 0 && page < a.num_pages) {  // else the decode warp reports the page
+          const int g = r / nc;
+          const int64_t row = static_cast<int64_t>(a.cu_q_rows[s]) * a.kv_heads + g;
+          if (lane < 16)
+            append_local_item<GW_KV_BF16>(const_cast<uint8_t*>(a.pool), a.kv_heads, page, pos % kPage, g,
+                                          a.k_new + row * 256, a.v_new + row * 256,
+                                          load_cs8(a.rope_cs + (static_cast<int64_t>(pos) * 128 + 8 * lane) * 2),
+                                          lane);
+          fence_proxy_async_global();
+        }
+      }
+      __syncwarp();
+      if (lane == 0) st_release_shared(app_done, j + 1);
+    }
     return;
   }
   const int n_active = active_warps(total_units, kTcWarps);
@@ -203,6 +245,13 @@ __global__ void __launch_bounds__(kTcWarps * 32, 1)
     const Unit d = sm.ring[f_slot];
     const int st = issued % kTcStages;
     const int32_t phys = __shfl_sync(0xffffffffu, pg_cur, f_i);  // one page per stage
+    if (a.k_new && d.last && f_i == d.n - 1) {
+      // the page holding the step's row: wait until the append warp wrote it
+      if (lane == 0)
+        wait_counter(app_done, (d.unit - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1, a.status);
+      __syncwarp();
+      fence_proxy_async_global();
+    }
     if (phys < 0 || phys >= a.num_pages) {
       if (lane == 0) {
         sm.valid[st] = 0;
@@ -389,11 +438,11 @@ cudaError_t launch_tc(const LocalArgs& a, cudaStream_t st) {
   CUtensorMap map;
   cudaError_t e = make_local_kv_map(a, &map);
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(TcWarpSmem) * kTcWarps + sizeof(int32_t) * (kMaxBatch + 1 + 32);
+  const size_t smem = sizeof(TcWarpSmem) * kTcWarps + sizeof(int32_t) * (kMaxBatch + 1 + 32 + 4);
   auto kern = local_decode_tc_kernel<G>;
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kTcWarps * 32), smem, st, a, map);
+  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kTcWarps * 32 + (a.k_new ? 32 : 0)), smem, st, a, map);
   if (e != cudaSuccess) return e;
   // the merged partials are dropped from L2 unwritten: their write-back no
   // longer competes with the next layers' streams (serving step 0.2873 vs

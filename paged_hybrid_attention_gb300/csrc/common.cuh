@@ -80,6 +80,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
   return true;
 }
 
+// Orders this thread's earlier global writes (generic proxy) before later
+// asynchronous-proxy accesses, such as a tensor copy of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_release_shared(int32_t* p, int32_t v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t ld_acquire_shared(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
+// Bounded wait until the shared-memory counter *p, raised by another warp of
+// the CTA, reaches `target`.  Returns false (and records GW_DEV_TIMEOUT) if
+// it never does.
+__device__ __forceinline__ bool wait_counter(const int32_t* p, int32_t target, int32_t* status) {
+  if (ld_acquire_shared(p) >= target) return true;
+  const uint64_t t0 = global_ns();
+  while (ld_acquire_shared(p) < target) {
+    if (global_ns() - t0 > kWaitNs) {
+      if (status) atomicOr(status, GW_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(32);
+  }
+  return true;
+}
+
 // One-dimensional bulk copy global -> shared, completion counted on `bar`.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,

@@ -210,15 +210,32 @@ size_t gw_attn_workspace_bytes(const gw_kv_pool* pool, int32_t num_q_heads, int3
       .total;
 }
 
+// The step's K/V rows of a gw_append_decode_attn_* call.
+struct FusedAppend {
+  const void* k;
+  const void* v;
+  const float* rope_cs;
+  int32_t max_pos;
+};
+
 static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool, const void* q, void* out,
                              int32_t num_q_heads, int32_t batch, const int32_t* cu_q_rows, const int32_t* seq_lens,
                              const int32_t* block_table, int32_t max_pages_per_seq, int32_t max_q_rows,
                              int32_t window, float scale, void* workspace, size_t workspace_bytes,
                              int32_t* dev_status, void* stream, bool validate_only = false,
-                             float* lse = nullptr) {
+                             float* lse = nullptr, const FusedAppend* app = nullptr) {
   g_err[0] = 0;
   gw_status s = check_pool(pool, fn);
   if (s != GW_OK) return s;
+  if (app) {
+    if (!app->k || !app->v || !aligned(app->k, 16) || !aligned(app->v, 16))
+      return fail(GW_ERR_INVALID_ARG, fn, "k/v NULL or not 16-byte aligned");
+    if (!app->rope_cs || !aligned(app->rope_cs, 16))
+      return fail(GW_ERR_INVALID_ARG, fn, "rope_cs NULL or not 16-byte aligned");
+    if (app->max_pos < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_pos must be >= 1");
+    if (!local || pool->dtype != GW_KV_BF16)
+      return fail(GW_ERR_UNSUPPORTED, fn, "the fused append serves bf16 local pools");
+  }
   if (local && pool->layout != GW_LAYOUT_LOCAL) return fail(GW_ERR_INVALID_ARG, fn, "pool layout is not LOCAL");
   if (!local && pool->layout == GW_LAYOUT_LOCAL) return fail(GW_ERR_INVALID_ARG, fn, "pool layout is not GLOBAL");
   if (batch < 0) return fail(GW_ERR_INVALID_ARG, fn, "batch < 0");
@@ -277,6 +294,12 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
   a.status = dev_status;
   a.early_inputs = g_early_inputs ? 1 : 0;
   a.lse = lse;
+  if (app) {
+    a.k_new = static_cast<const uint16_t*>(app->k);
+    a.v_new = static_cast<const uint16_t*>(app->v);
+    a.rope_cs = app->rope_cs;
+    a.max_pos = app->max_pos;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (local) {
@@ -313,6 +336,17 @@ gw_status validate_local_call(const char* fn, const gw_kv_pool* pool, const void
 }  // namespace gw
 
 extern "C" {
+
+gw_status gw_append_decode_attn_local(const gw_kv_pool* pool, const void* k, const void* v, const float* rope_cs,
+                                      int32_t max_pos, const void* q, void* out, int32_t num_q_heads, int32_t batch,
+                                      const int32_t* cu_q_rows, const int32_t* seq_lens, const int32_t* block_table,
+                                      int32_t max_pages_per_seq, int32_t window, float scale, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  const FusedAppend app{k, v, rope_cs, max_pos};
+  return attn_common("gw_append_decode_attn_local", true, pool, q, out, num_q_heads, batch, cu_q_rows, seq_lens,
+                     block_table, max_pages_per_seq, 1, window, scale, workspace, workspace_bytes, dev_status, stream,
+                     false, nullptr, &app);
+}
 
 gw_status gw_decode_attn_global(const gw_kv_pool* pool, const void* q, void* out, int32_t num_q_heads, int32_t batch,
                                 const int32_t* cu_q_rows, const int32_t* seq_lens, const int32_t* block_table,

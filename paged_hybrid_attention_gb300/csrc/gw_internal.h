@@ -94,6 +94,12 @@ struct LocalArgs {
   int32_t* status;
   int32_t* prompt_base;  // tile offsets of the prompt-row kernels
   float* lse;            // optional: natural-log log-sum-exp per (decode row, q head)
+  // Fused append (gw_append_decode_attn_*): the K/V row of each decode row,
+  // at position seq_len - 1, written by the decode kernel; k_new null: none.
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const float* rope_cs;
+  int32_t max_pos;
   int32_t early_inputs;  // gw_set_early_inputs: plan before the wait on the previous kernel
 };
 
