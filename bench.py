@@ -220,15 +220,20 @@ class GpuLayer:
     def can_fuse(self, gw):
         """Whether this layer's step can append inside its decode call
         (gw_append_decode_attn_*): decode rows only, on a pool it serves."""
-        return self.max_q_rows == 1 and self.fam.kind == "local" and self.fam.dtype == "bf16"
+        return self.max_q_rows == 1 and (self.fam.kind == "global" or self.fam.dtype == "bf16")
 
     def attend(self, gw, stream):
         if self.fused:
             # the step's rows appended by the decode call itself (re-appending
             # the same bytes when the call is replayed)
-            gw.append_decode_attn_local(self.pool, self.k_new, self.v_new, self.table, self.q, self.out, self.cu,
-                                        self.lens, self.bt, self.ws, self.fam.window, dev_status=self.status,
-                                        stream=stream)
+            if self.fam.kind == "local":
+                gw.append_decode_attn_local(self.pool, self.k_new, self.v_new, self.table, self.q, self.out, self.cu,
+                                            self.lens, self.bt, self.ws, self.fam.window, dev_status=self.status,
+                                            stream=stream)
+            else:
+                gw.append_decode_attn_global(self.pool, self.k_new, self.v_new, self.table, self.q, self.out,
+                                             self.cu, self.lens, self.bt, self.ws, dev_status=self.status,
+                                             stream=stream)
             return
         if self.fam.kind == "local":
             gw.decode_attn_local(self.pool, self.q, self.out, self.cu, self.lens, self.bt, self.ws, self.fam.window,

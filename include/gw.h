@@ -281,6 +281,27 @@ gw_status gw_decode_attn_global(const gw_kv_pool* pool, const void* q, void* out
                                 void* stream);
 
 /*
+ * gw_append_decode_attn_global - a decode step's append and attention on a
+ * global pool in one call: the same result as gw_kv_append of each decode
+ * row's k, v (GLOBAL shapes, [rows][512] bf16) followed by
+ * gw_decode_attn_global with max_q_rows = 1.
+ *
+ * [pegainfer] "Scheduling" and "Architecture notes" (global RoPE on 128 of
+ * 512 dims, theta 1M, denominator 512); [Gewell] "the Why" (the folded row).
+ * Each sequence with one row appends it at pos = seq_lens[b] - 1 as
+ * gw_append_decode_attn_local does; the kernel that decodes the sequence's
+ * last chunk writes the row before copying the tile that holds it.  All
+ * three global layouts.  Errors: those of gw_decode_attn_global;
+ * GW_ERR_INVALID_ARG (k, v, rope_cs NULL or not 16-byte aligned,
+ * max_pos < 1).
+ */
+gw_status gw_append_decode_attn_global(const gw_kv_pool* pool, const void* k, const void* v, const float* rope_cs,
+                                       int32_t max_pos, const void* q, void* out, int32_t num_q_heads, int32_t batch,
+                                       const int32_t* cu_q_rows, const int32_t* seq_lens, const int32_t* block_table,
+                                       int32_t max_pages_per_seq, float scale, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * gw_decode_attn_global_lse - gw_decode_attn_global for decode rows
  * (max_q_rows 1) that also writes each row's log-sum-exp:
  *

@@ -46,8 +46,13 @@
 //              the previous unit's last QK^T has completed, and prefetches
 //              the next unit's rows into L2.
 //   warp 7     P.V issue.
+//   warp 8     (fused append only, gw_append_decode_attn_global) writes the
+//              step's row of each sequence whose last chunk this CTA decodes,
+//              in the order of the CTA's units; the producer waits for it
+//              before copying the tile that holds the sequence's last page.
 // QK^T and P.V are issued by different warps so that QK^T of the next tile
 // never waits behind the softmax of the current one.
+#include "append_row.cuh"
 #include "plan.cuh"
 #include "tcgen05.cuh"
 
@@ -137,6 +142,7 @@ struct GSmem {
   uint64_t s_ready[2], p_ready[2], pfree[2], o_done[2], o_free[2], q_ready[2], q_free[2], qs_ready[4];
   uint32_t tmem_base;
   int32_t flag[2];  // per tile parity: index + 1 of the last tile that asked for a new max
+  int32_t app_done;  // fused append: units of this CTA (in order) whose rows are written
   int32_t ub[kMaxBatch + 1 + 32];  // split plan (+ scan scratch)
 };
 static_assert(sizeof(GSmem<GW_LAYOUT_GLOBAL_FOLDED, 32>) <= 232448, "shared memory of one CTA");
@@ -192,8 +198,10 @@ __device__ __forceinline__ float head_reduce(float (&x)[HQ], int lane) {
   return v;
 }
 
-template <int LAYOUT, int HQ>
-__global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalArgs a) {
+// kApp: the fused-append variant, with warp 8 (its ninth warp lowers the
+// register budget, so the plain call keeps a kernel of its own).
+template <int LAYOUT, int HQ, bool kApp>
+__global__ void __launch_bounds__(kThreads + (kApp ? 32 : 0), 1) global_decode_kernel(const LocalArgs a) {
   using T = GTraits<LAYOUT>;
   using SM = GSmem<LAYOUT, HQ>;
   constexpr int NB = T::kNumBuf;
@@ -208,13 +216,14 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
 
   // Stale tile / P slots must hold finite values: masked tokens get p = 0 and
   // 0 * finite = 0 in the P.V contraction.
-  {
+  if (tid < kThreads) {
     uint4* z = reinterpret_cast<uint4*>(sm.tiles);
     for (int i = tid; i < static_cast<int>(sizeof(sm.tiles) / 16); i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
     uint4* zp = reinterpret_cast<uint4*>(sm.p);
     for (int i = tid; i < static_cast<int>(sizeof(sm.p) / 16); i += kThreads) zp[i] = make_uint4(0, 0, 0, 0);
   }
   if (tid == 0) {
+    sm.app_done = 0;
     for (int b = 0; b < NB; ++b) {
       mbar_init(&sm.full[b], 1);
       for (int j = 0; j < kTilePages; ++j) mbar_init(&sm.slot_empty[b][j], 1);
@@ -308,6 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
       const int b = n % NB;
       const uint32_t k = n / NB;  // use of buffer b
       bool waited = true, ok = false;
+      if (kApp && !end && t == ntiles - 1 && p1 * kPage >= L) {
+        // the tile holds the step's row, which the append warp writes
+        if (lane == 0)
+          wait_counter(&sm.app_done, (u - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1, st);
+        __syncwarp();
+        fence_proxy_async_global();
+      }
       if (lane < kTilePages) {
         // This lane's slot is free once P.V of the buffer's previous tile has
         // read it.  That P.V followed the softmax of that tile, so the
@@ -560,6 +576,33 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
           prefetch_l2(a.q + static_cast<int64_t>(a.cu_q_rows[plan_seq(sm.ub, a.batch, un)]) * HQ * 512, HQ * 1024);
       }
     }
+  } else if (kApp && warp == 8) {
+    // ------------------------------------------------- fused append (warp 8)
+    using R = GlobalRow<LAYOUT>;
+    wait_prev();
+    for (int j = 0;; ++j) {
+      const int u = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
+      if (u >= total_units) break;
+      const int s = plan_seq(sm.ub, a.batch, u);
+      if (u - sm.ub[s] == sm.ub[s + 1] - sm.ub[s] - 1) {  // the sequence's last chunk
+        const int pos = a.seq_lens[s] - 1;
+        const int32_t page = a.block_table[static_cast<int64_t>(s) * a.max_pages + pos / kPage];
+        if (pos >= a.max_pos) {
+          if (lane == 0) set_status(st, GW_DEV_POS_RANGE);
+        } else if (page >= 0 && page < a.num_pages) {  // else the producer reports the page
+          const int64_t row = a.cu_q_rows[s];
+          for (int it = lane; it < R::kItems; it += 32) {
+            const int rt = R::rot_item(it);
+            const CosSin8 cs = rt >= 0 ? load_cs8(a.rope_cs + (static_cast<int64_t>(pos) * 64 + 8 * rt) * 2) : CosSin8{};
+            append_global_item<LAYOUT>(const_cast<uint8_t*>(a.pool), page, pos % kPage, a.k_new + row * 512,
+                                       a.v_new + row * 512, cs, it);
+          }
+          fence_proxy_async_global();
+        }
+      }
+      __syncwarp();
+      if (lane == 0) st_release_shared(&sm.app_done, j + 1);
+    }
   } else if (warp < 4) {
     // ------------------------------------------------- softmax + epilogue
     wait_prev();
@@ -773,11 +816,11 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
 
 template <int LAYOUT, int HQ>
 cudaError_t launch_layout(const LocalArgs& a, cudaStream_t stream) {
-  auto kern = global_decode_kernel<LAYOUT, HQ>;
+  auto kern = a.k_new ? global_decode_kernel<LAYOUT, HQ, true> : global_decode_kernel<LAYOUT, HQ, false>;
   const size_t smem = sizeof(GSmem<LAYOUT, HQ>);
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kThreads), smem, stream, a);
+  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kThreads + (a.k_new ? 32 : 0)), smem, stream, a);
   if (e != cudaSuccess) return e;
   // Dropping the merged partials from L2 unwritten pays for the folded pool
   // (24.7 vs 26.9 us per serving call) but not for the full control (427 vs

@@ -233,8 +233,8 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
     if (!app->rope_cs || !aligned(app->rope_cs, 16))
       return fail(GW_ERR_INVALID_ARG, fn, "rope_cs NULL or not 16-byte aligned");
     if (app->max_pos < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_pos must be >= 1");
-    if (!local || pool->dtype != GW_KV_BF16)
-      return fail(GW_ERR_UNSUPPORTED, fn, "the fused append serves bf16 local pools");
+    if (local && pool->dtype != GW_KV_BF16)
+      return fail(GW_ERR_UNSUPPORTED, fn, "the fused append serves bf16 local pools and the global pools");
   }
   if (local && pool->layout != GW_LAYOUT_LOCAL) return fail(GW_ERR_INVALID_ARG, fn, "pool layout is not LOCAL");
   if (!local && pool->layout == GW_LAYOUT_LOCAL) return fail(GW_ERR_INVALID_ARG, fn, "pool layout is not GLOBAL");
@@ -345,6 +345,17 @@ gw_status gw_append_decode_attn_local(const gw_kv_pool* pool, const void* k, con
   const FusedAppend app{k, v, rope_cs, max_pos};
   return attn_common("gw_append_decode_attn_local", true, pool, q, out, num_q_heads, batch, cu_q_rows, seq_lens,
                      block_table, max_pages_per_seq, 1, window, scale, workspace, workspace_bytes, dev_status, stream,
+                     false, nullptr, &app);
+}
+
+gw_status gw_append_decode_attn_global(const gw_kv_pool* pool, const void* k, const void* v, const float* rope_cs,
+                                       int32_t max_pos, const void* q, void* out, int32_t num_q_heads, int32_t batch,
+                                       const int32_t* cu_q_rows, const int32_t* seq_lens, const int32_t* block_table,
+                                       int32_t max_pages_per_seq, float scale, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  const FusedAppend app{k, v, rope_cs, max_pos};
+  return attn_common("gw_append_decode_attn_global", false, pool, q, out, num_q_heads, batch, cu_q_rows, seq_lens,
+                     block_table, max_pages_per_seq, 1, 0, scale, workspace, workspace_bytes, dev_status, stream,
                      false, nullptr, &app);
 }
 

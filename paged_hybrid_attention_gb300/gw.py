@@ -32,7 +32,8 @@ EXPORTS = ["gw_pool_page_bytes", "gw_kv_append", "gw_decode_attn_local", "gw_dec
            "gw_attn_workspace_bytes", "gw_last_error", "gw_version", "gw_decode_attn_local_noalloc",
            "gw_noalloc_scratch_bytes", "gw_bw_probe", "gw_set_max_ctas", "gw_set_early_launch",
            "gw_set_early_inputs", "gw_rope_cs", "gw_wait_selftest", "gw_bw_probe_tma",
-           "gw_decode_attn_global_lse", "gw_merge_lse", "gw_append_decode_attn_local"]
+           "gw_decode_attn_global_lse", "gw_merge_lse", "gw_append_decode_attn_local",
+           "gw_append_decode_attn_global"]
 
 
 class GwError(RuntimeError):
@@ -59,6 +60,9 @@ _lib.gw_decode_attn_local.restype = _i32
 _lib.gw_append_decode_attn_local.argtypes = [_P, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32,
                                              _f32, _vp, _sz, _vp, _vp]
 _lib.gw_append_decode_attn_local.restype = _i32
+_lib.gw_append_decode_attn_global.argtypes = [_P, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32,
+                                              _f32, _vp, _sz, _vp, _vp]
+_lib.gw_append_decode_attn_global.restype = _i32
 _lib.gw_decode_attn_global.argtypes = [_P, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _sz,
                                        _vp, _vp]
 _lib.gw_decode_attn_global.restype = _i32
@@ -200,6 +204,19 @@ def append_decode_attn_local(pool, k, v, rope_cs, q, out, cu_q_rows, seq_lens, b
                                             _ptr(cu_q_rows), _ptr(seq_lens), _ptr(block_table),
                                             int(block_table.shape[1]), int(window), float(scale), _ptr(workspace),
                                             int(workspace.numel()), _ptr(dev_status), _stream(stream)))
+
+
+def append_decode_attn_global(pool, k, v, rope_cs, q, out, cu_q_rows, seq_lens, block_table, workspace, scale=None,
+                              dev_status=None, stream=None):
+    """gw_append_decode_attn_global: gw_kv_append of each decode row's k, v
+    ([rows, 512]) at position seq_len - 1, then its attention, in one call."""
+    hq = int(q.shape[1])
+    scale = 1.0 / math.sqrt(512) if scale is None else scale
+    _check(_lib.gw_append_decode_attn_global(ctypes.byref(pool.desc), _ptr(k), _ptr(v), _ptr(rope_cs),
+                                             int(rope_cs.shape[0]), _ptr(q), _ptr(out), hq, int(seq_lens.numel()),
+                                             _ptr(cu_q_rows), _ptr(seq_lens), _ptr(block_table),
+                                             int(block_table.shape[1]), float(scale), _ptr(workspace),
+                                             int(workspace.numel()), _ptr(dev_status), _stream(stream)))
 
 
 def decode_attn_global(pool, q, out, cu_q_rows, seq_lens, block_table, workspace, scale=None, max_q_rows=1,

@@ -115,3 +115,28 @@ def test_fused_local_position_beyond_table_is_reported_not_written():
     ref_pool.data.copy_(before)
     G.append(layer, ref_pool, tab, seqs=[0], part="new")
     assert torch.equal(pool.data, ref_pool.data)
+
+
+@pytest.mark.parametrize("key", ["global", "global_full", "global_e4m3"])
+def test_fused_global_tiny(key):
+    _check(synth.Layer(synth.spec("tiny"), key))
+
+
+@pytest.mark.parametrize("early", [False, True])
+@pytest.mark.parametrize("layout,dtype", [("folded", "bf16"), ("full", "bf16"), ("folded_e4m3", "e4m3")])
+@pytest.mark.parametrize("hq", [8, 32])
+def test_fused_global_edges(layout, dtype, hq, early):
+    # lengths around page, tile (4 pages) and chunk (32 pages) edges.  The
+    # e4m3 pool draws N(0, 0.5) like the fp8 workload: at sigma 1 a two-token
+    # softmax reaches max-abs 0.0102 against the oracle (outputs near 3, whose
+    # bf16 rounding alone is up to 0.0078, and P carried as two e4m3 terms),
+    # in the fused and the two-call path alike.
+    lens = [1, 2, 16, 17, 63, 64, 65, 511, 512, 513, 1100]
+    fam = synth.Family("global", dtype, layout, 1, 512, 128, 1e6, 0, sigma=0.5 if dtype == "e4m3" else 1.0)
+    layer = synth.Layer(synth.custom("fused_g", 90 + hq, hq, lens, [1] * len(lens), {"global": fam}), "global")
+    _check(layer, early)
+
+
+@pytest.mark.slow
+def test_fused_global_serving_full():
+    _check(synth.Layer(synth.spec("serving"), "global"), early=True)
