@@ -245,10 +245,9 @@ gw_status gw_decode_attn_local(const gw_kv_pool* pool, const void* q, void* out,
  * writes its row before reading that page, so no second kernel and no
  * wait between the two.  rope_cs and max_pos as for gw_kv_append.  A row
  * with pos >= max_pos is not written (GW_DEV_POS_RANGE); a bad page entry is
- * reported as by gw_decode_attn_local.  Serves bf16 pools.
+ * reported as by gw_decode_attn_local.  bf16 and e4m3 pools.
  * Errors: those of gw_decode_attn_local; GW_ERR_INVALID_ARG (k, v, rope_cs
- * NULL or not 16-byte aligned, max_pos < 1); GW_ERR_UNSUPPORTED (an e4m3
- * pool).
+ * NULL or not 16-byte aligned, max_pos < 1).
  */
 gw_status gw_append_decode_attn_local(const gw_kv_pool* pool, const void* k, const void* v, const float* rope_cs,
                                       int32_t max_pos, const void* q, void* out, int32_t num_q_heads, int32_t batch,

@@ -34,7 +34,12 @@
 //   warp 8     Q.K^T issue and TMEM owner
 //   warp 9     q loader: scaling and the two-term split of the unit's G heads
 //   warp 10    P.V issue
+//   warp 11    (fused append only, gw_append_decode_attn_local) writes the
+//              step's row of each (sequence, KV head) whose last chunk this
+//              CTA decodes, in the order of the CTA's units; the producer
+//              warp that copies that unit's last page waits for it.
 // Every wait is bounded; a timeout raises GW_DEV_TIMEOUT and the roles stop.
+#include "append_row.cuh"
 #include "plan.cuh"
 #include "tcgen05.cuh"
 #include "tma.cuh"
@@ -55,7 +60,7 @@ constexpr int kE8N = 16;                       // UMMA N: [hi (G) | lo (G) | zer
 constexpr uint32_t kE8ColS = 0, kE8ColO = 64;
 
 struct E8Unit {
-  int32_t unit, s, g, row;  // (row unused by the consumers)
+  int32_t unit, s, g, last;  // last: the sequence's last chunk
   int32_t lp0, tok_lo, tok_hi;  // first logical page; token range [tok_lo, tok_hi) in the window
   int32_t mask;                 // pages of the unit that were loaded (bit j: page lp0 + j)
 };
@@ -70,6 +75,7 @@ struct __align__(1024) E8Smem {
   uint64_t full[kE8Stages], empty[kE8Stages];
   uint64_t s_ready[2], p_ready[2], pfree[2], o_done[2], o_free[2], q_ready[2], q_free[2], qs_ready[4];
   uint32_t tmem_base;
+  int32_t app_done;  // fused append: units of this CTA (in order) whose rows are written
   int32_t ub[kMaxBatch + 1 + 32];  // split plan (+ scan scratch)
 };
 static_assert(sizeof(E8Smem) <= 232448, "shared memory of one CTA");
@@ -93,8 +99,9 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   sum = make_float2(hf.x + lf.x, hf.y + lf.y);
 }
 
-template <int G>
-__global__ void __launch_bounds__(kE8Threads, 1)
+// kApp: the fused-append variant, with warp 11.
+template <int G, bool kApp>
+__global__ void __launch_bounds__(kE8Threads + (kApp ? 32 : 0), 1)
     local_decode_e4m3_tc_kernel(const LocalArgs a, const __grid_constant__ CUtensorMap kv_map) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   E8Smem& sm = *reinterpret_cast<E8Smem*>(smem_raw);
@@ -103,8 +110,9 @@ __global__ void __launch_bounds__(kE8Threads, 1)
 
   // the q buffers' padding rows (2G..15) stay zero
   for (int i = tid; i < static_cast<int>(sizeof(sm.q) / 16); i += kE8Threads)
-    reinterpret_cast<uint4*>(sm.q)[i] = make_uint4(0, 0, 0, 0);
+    if (tid < kE8Threads) reinterpret_cast<uint4*>(sm.q)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
+    sm.app_done = 0;
     for (int b = 0; b < kE8Stages; ++b) {
       mbar_init(&sm.full[b], 1);
       mbar_init(&sm.empty[b], 1);
@@ -173,7 +181,7 @@ __global__ void __launch_bounds__(kE8Threads, 1)
       const int lp1 = min(d.lp0 + kE8Chunk, p1 + 1);
       d.tok_lo = max(first, d.lp0 * kPage);
       d.tok_hi = min(L, lp1 * kPage);
-      d.row = 0;
+      d.last = d.tok_hi == L;
       d.mask = 0;
       return d;
     };
@@ -201,6 +209,14 @@ __global__ void __launch_bounds__(kE8Threads, 1)
       const int32_t mine = __shfl_sync(0xffffffffu, pg0, j);
       const bool ok = lane < 8 && ((pages >> j) & 1);
       if (k >= kE8Stages && !warp_wait(&sm.empty[b], ((k / kE8Stages) - 1) & 1, st)) break;
+      if (kApp && d0.last && ((d0.tok_hi - 1) / kPage - d0.lp0) / 2 == pw) {
+        // this warp copies the page holding the step's row: wait until the
+        // append warp wrote it
+        if (lane == 0)
+          wait_counter(&sm.app_done, (u - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1, st);
+        __syncwarp();
+        fence_proxy_async_global();
+      }
       if (pw == 0 && lane == 0) {
         E8Unit e = d0;
         e.mask = static_cast<int32_t>(pages & 0xFF);
@@ -317,6 +333,34 @@ __global__ void __launch_bounds__(kE8Threads, 1)
         mbar_arrive(&sm.qs_ready[k & 3]);
       }
       if (next) load(next);
+    }
+  } else if (kApp && warp == kE8Threads / 32) {
+    // -------------------------------------------------------- fused append
+    wait_prev();
+    for (int j = 0;; ++j) {
+      const int u = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
+      if (u >= total) break;
+      const int s = plan_seq(sm.ub, a.batch, u);
+      const int nc = (sm.ub[s + 1] - sm.ub[s]) / a.kv_heads;
+      const int r = u - sm.ub[s];
+      if (r % nc == nc - 1) {
+        const int pos = a.seq_lens[s] - 1;
+        const int32_t page = a.block_table[static_cast<int64_t>(s) * a.max_pages + pos / kPage];
+        if (pos >= a.max_pos) {
+          if (lane == 0) set_status(st, GW_DEV_POS_RANGE);
+        } else if (page >= 0 && page < a.num_pages) {  // else the producer reports the page
+          const int g = r / nc;
+          const int64_t row = static_cast<int64_t>(a.cu_q_rows[s]) * a.kv_heads + g;
+          if (lane < 16)
+            append_local_item<GW_KV_E4M3>(const_cast<uint8_t*>(a.pool), a.kv_heads, page, pos % kPage, g,
+                                          a.k_new + row * 256, a.v_new + row * 256,
+                                          load_cs8(a.rope_cs + (static_cast<int64_t>(pos) * 128 + 8 * lane) * 2),
+                                          lane);
+          fence_proxy_async_global();
+        }
+      }
+      __syncwarp();
+      if (lane == 0) st_release_shared(&sm.app_done, j + 1);
     }
   } else if (warp < 4) {
     // ------------------------------------------------ softmax + epilogue
@@ -497,11 +541,11 @@ cudaError_t launch_g(const LocalArgs& a, cudaStream_t st) {
   CUtensorMap map;
   cudaError_t e = make_local_kv_map(a, &map, GW_KV_E4M3);
   if (e != cudaSuccess) return e;
-  auto kern = local_decode_e4m3_tc_kernel<G>;
+  auto kern = a.k_new ? local_decode_e4m3_tc_kernel<G, true> : local_decode_e4m3_tc_kernel<G, false>;
   const size_t smem = sizeof(E8Smem);
   e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kE8Threads), smem, st, a, map);
+  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kE8Threads + (a.k_new ? 32 : 0)), smem, st, a, map);
   if (e != cudaSuccess) return e;
   return launch_combine(a, G, 256, local_max_chunks(a.max_pages, a.window, kE8Chunk), true, st);
 }

@@ -233,8 +233,6 @@ static gw_status attn_common(const char* fn, bool local, const gw_kv_pool* pool,
     if (!app->rope_cs || !aligned(app->rope_cs, 16))
       return fail(GW_ERR_INVALID_ARG, fn, "rope_cs NULL or not 16-byte aligned");
     if (app->max_pos < 1) return fail(GW_ERR_INVALID_ARG, fn, "max_pos must be >= 1");
-    if (local && pool->dtype != GW_KV_BF16)
-      return fail(GW_ERR_UNSUPPORTED, fn, "the fused append serves bf16 local pools and the global pools");
   }
   if (local && pool->layout != GW_LAYOUT_LOCAL) return fail(GW_ERR_INVALID_ARG, fn, "pool layout is not LOCAL");
   if (!local && pool->layout == GW_LAYOUT_LOCAL) return fail(GW_ERR_INVALID_ARG, fn, "pool layout is not GLOBAL");

@@ -68,13 +68,15 @@ def test_fused_local_tiny():
 
 
 @pytest.mark.parametrize("early", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
 @pytest.mark.parametrize("kvh,hq", [(2, 2), (2, 4), (1, 4), (2, 16)])
-def test_fused_local_groups_and_edges(kvh, hq, early):
+def test_fused_local_groups_and_edges(kvh, hq, dtype, early):
     # lengths around page, chunk and window edges (first token, page ends,
-    # one past a page, the window, a long tail)
+    # one past a page, the window, a long tail); e4m3 draws N(0, 0.5) like the
+    # fp8 workload
     W = 40
     lens = [1, 2, 15, 16, 17, 32, 33, W - 1, W, W + 1, W + 17, 128, 129, 300]
-    fam = synth.Family("local", "bf16", "local", kvh, 256, 256, 1e4, W)
+    fam = synth.Family("local", dtype, "local", kvh, 256, 256, 1e4, W, sigma=0.5 if dtype == "e4m3" else 1.0)
     layer = synth.Layer(synth.custom("fused", 41 + kvh + hq, hq, lens, [1] * len(lens), {"local": fam}), "local")
     _check(layer, early)
 
@@ -94,6 +96,12 @@ def test_fused_local_window_1024_many_sequences():
 @pytest.mark.slow
 def test_fused_local_serving_full():
     _check(synth.Layer(synth.spec("serving"), "local"), early=True)
+
+
+@pytest.mark.slow
+def test_fused_local_fp8_full():
+    # all 64 sequences of the fp8 workload, every output row against the oracle
+    _check(synth.Layer(synth.spec("fp8_local"), "local"), early=True)
 
 
 def test_fused_local_position_beyond_table_is_reported_not_written():
