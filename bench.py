@@ -52,7 +52,7 @@ UNIT = "GB/s"
 # was captured from; reported as null once the source no longer matches.
 # workload: (bytes, source file under csrc/, sha256)
 NCU_TRAFFIC = {
-    "serving": (275542528, "attn_local.cu", "db9fb085d8075f8b289ad1d35df850b9606686f187eccb4dee26c40c180e501d"),
+    "serving": (276155392, "attn_local.cu", "717bc482be907e762b64b76859a3978a62544ed7b68591d8a8055c741d576191"),
     "fp8_local": (552973312, "attn_local_e4m3_tc.cu", "e348365c2bf236e2255d66c87103cc92c1406a3e1dab7e39b6f6144676afb399"),
     "long_global": (1354496512, "attn_global.cu", "f6add234ef69883f75cd07c7c8ad98348d3192bd7b1e56001c15c1040c3ccc69"),
 }
@@ -1016,8 +1016,9 @@ def main():
                                    "prompt_tflops": dom_flops / (dom_ms * 1e-3) / 1e12}}
     else:
         # the probe whose copy pipeline the dominant kernel uses: tensor-map
-        # boxes for the bf16 local kernel, bulk copies for the others
-        tma_pipe = bool(locals_) and dom[0].fam.dtype == "bf16"
+        # boxes for the local kernels (bf16 and e4m3), bulk copies for the
+        # global kernel
+        tma_pipe = bool(locals_)
         probe = read_gbs_tma if tma_pipe else read_gbs
         roofline = {"kernel": how, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
@@ -1056,10 +1057,10 @@ def main():
                               "clock-sampling window"},
         "bw_probe": None if read_gbs is None else {
             "read_gbs": read_gbs, "read_gbs_tma": read_gbs_tma, "bytes": 4 << 30,
-            "what": "4 GiB streamed with no arithmetic, best of 5: gw_bw_probe through the bulk-copy pipeline "
-                    "(8 warps x 2-stage 8 KiB rings per SM, as the e4m3 local kernel), gw_bw_probe_tma through "
-                    "the tensor-map pipeline (6 warps x 2-stage 16 KiB page-head rings per SM, as the bf16 local "
-                    "kernel)"},
+            "what": "4 GiB streamed with no arithmetic, best of 5: gw_bw_probe through a bulk-copy pipeline "
+                    "(8 warps x 2-stage 8 KiB rings per SM; the global decode copies whole pages in bulk), "
+                    "gw_bw_probe_tma through the tensor-map pipeline (6 warps x 2-stage 16 KiB page-head rings "
+                    "per SM of 2 KB boxes, as the local decode kernels)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,

@@ -440,11 +440,12 @@ gw_status gw_set_early_inputs(int32_t on);
 
 /*
  * gw_bw_probe - a measurement aid, not part of the method: streams the first
- * floor(bytes / 8192) * 8192 bytes of the device buffer `buf` through the
- * copy pipeline of the local decode kernel (one CTA per SM, 8 warps, each
- * with a 2-stage ring of 8 KiB shared-memory stages filled by two 4 KiB
- * cp.async.bulk copies) and discards them, so that its rate is the read
- * bandwidth that pipeline can reach on the GPU.  The pages this library
+ * floor(bytes / 8192) * 8192 bytes of the device buffer `buf` through a
+ * bulk-copy pipeline (one CTA per SM, 8 warps, each with a 2-stage ring of
+ * 8 KiB shared-memory stages filled by two 4 KiB cp.async.bulk copies; the
+ * global decode kernel copies its pages with the same instruction) and
+ * discards them, so that its rate is the read bandwidth such a pipeline can
+ * reach on the GPU.  The pages this library
  * follows have no counterpart of this entry point.
  *   buf          device memory, 16-byte aligned, caller-owned, only read.
  *   bytes        >= 8192.
@@ -456,7 +457,8 @@ gw_status gw_bw_probe(const void* buf, size_t bytes, int32_t* dev_status, void* 
 
 /*
  * gw_bw_probe_tma - as gw_bw_probe, through the copy pipeline of the bf16
- * local decode kernel instead: one CTA per SM, 6 warps, each with a 2-stage
+ * local decode kernel instead (the e4m3 one copies the same 2 KiB boxes):
+ * one CTA per SM, 6 warps, each with a 2-stage
  * ring of 16 KiB shared-memory stages, a stage being one 16-token page head
  * (K then V) brought by 8 tensor-map copies of 2 KiB (128-byte swizzled).
  * The first floor(bytes / 16384) * 16384 bytes of `buf` are read as the
