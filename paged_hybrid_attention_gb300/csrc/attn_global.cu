@@ -46,10 +46,12 @@
 //              the previous unit's last QK^T has completed, and prefetches
 //              the next unit's rows into L2.
 //   warp 7     P.V issue.
-//   warp 8     (fused append only, gw_append_decode_attn_global) writes the
-//              step's row of each sequence whose last chunk this CTA decodes,
-//              in the order of the CTA's units; the producer waits for it
-//              before copying the tile that holds the sequence's last page.
+// With a fused append (gw_append_decode_attn_global) warp 6 also writes the
+// step's row of each sequence whose last chunk this CTA decodes, one unit
+// ahead of its q loads; the producer waits for it before copying the tile
+// that holds the sequence's last page.  (A ninth warp for it would cap the
+// kernel at 168 registers, and the softmax's spills cost long contexts more
+// than the separate append: 245 vs 238-240 us per long-context call.)
 // QK^T and P.V are issued by different warps so that QK^T of the next tile
 // never waits behind the softmax of the current one.
 #include "append_row.cuh"
@@ -198,10 +200,44 @@ __device__ __forceinline__ float head_reduce(float (&x)[HQ], int lane) {
   return v;
 }
 
-// kApp: the fused-append variant, with warp 8 (its ninth warp lowers the
-// register budget, so the plain call keeps a kernel of its own).
+// The fused append, by the q-loader warp: the row of the CTA's j-th unit if
+// that unit is its sequence's last chunk, at position L - 1, with
+// gw_kv_append's arithmetic; then the CTA's count of appended units becomes
+// j + 1 (a release store the producer acquires).
+template <int LAYOUT>
+__device__ __noinline__ void append_unit_row(const LocalArgs& a, const int32_t* ub, int32_t* app_done, int j,
+                                             int total_units) {
+  using R = GlobalRow<LAYOUT>;
+  const int lane = threadIdx.x & 31;
+  const int u = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
+  if (u < total_units) {
+    const int s = plan_seq(ub, a.batch, u);
+    if (u - ub[s] == ub[s + 1] - ub[s] - 1) {  // the sequence's last chunk
+      const int pos = a.seq_lens[s] - 1;
+      const int32_t page = a.block_table[static_cast<int64_t>(s) * a.max_pages + pos / kPage];
+      if (pos >= a.max_pos) {
+        if (lane == 0) set_status(a.status, GW_DEV_POS_RANGE);
+      } else if (page >= 0 && page < a.num_pages) {  // else the producer reports the page
+        const int64_t row = a.cu_q_rows[s];
+        for (int it = lane; it < R::kItems; it += 32) {
+          const int rt = R::rot_item(it);
+          const CosSin8 cs =
+              rt >= 0 ? load_cs8(a.rope_cs + (static_cast<int64_t>(pos) * 64 + 8 * rt) * 2) : CosSin8{};
+          append_global_item<LAYOUT>(const_cast<uint8_t*>(a.pool), page, pos % kPage, a.k_new + row * 512,
+                                     a.v_new + row * 512, cs, it);
+        }
+        fence_proxy_async_global();
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) st_release_shared(app_done, j + 1);
+}
+
+// kApp: the fused-append variant (a kernel of its own, so that the plain
+// call's code is unchanged).
 template <int LAYOUT, int HQ, bool kApp>
-__global__ void __launch_bounds__(kThreads + (kApp ? 32 : 0), 1) global_decode_kernel(const LocalArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalArgs a) {
   using T = GTraits<LAYOUT>;
   using SM = GSmem<LAYOUT, HQ>;
   constexpr int NB = T::kNumBuf;
@@ -216,7 +252,7 @@ __global__ void __launch_bounds__(kThreads + (kApp ? 32 : 0), 1) global_decode_k
 
   // Stale tile / P slots must hold finite values: masked tokens get p = 0 and
   // 0 * finite = 0 in the P.V contraction.
-  if (tid < kThreads) {
+  {
     uint4* z = reinterpret_cast<uint4*>(sm.tiles);
     for (int i = tid; i < static_cast<int>(sizeof(sm.tiles) / 16); i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
     uint4* zp = reinterpret_cast<uint4*>(sm.p);
@@ -463,6 +499,7 @@ __global__ void __launch_bounds__(kThreads + (kApp ? 32 : 0), 1) global_decode_k
   } else if (warp == 6 && kE4) {
     // ------------------------------------------------- q loader, e4m3 pool
     wait_prev();
+    if (kApp) append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, 0, total_units);
     // Unit k's q goes to the Q buffer once the last QK^T of unit k - 1 has
     // completed.  Each head is scaled by an exact power of two 2^e, chosen so
     // that its largest |q| lands in [128, 256), and split into two e4m3
@@ -550,10 +587,12 @@ __global__ void __launch_bounds__(kThreads + (kApp ? 32 : 0), 1) global_decode_k
         if (un < total_units)
           prefetch_l2(a.q + static_cast<int64_t>(a.cu_q_rows[plan_seq(sm.ub, a.batch, un)]) * HQ * 512, HQ * 1024);
       }
+      if (kApp) append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, k + 1, total_units);
     }
   } else if (warp == 6) {
     // -------------------------------------------------------------- q loader
     wait_prev();
+    if (kApp) append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, 0, total_units);
     // Unit k's rows overwrite Q once the last QK^T of unit k - 1 has
     // completed (q_free); by then they are usually in L2 already.
     int k = 0;
@@ -575,33 +614,7 @@ __global__ void __launch_bounds__(kThreads + (kApp ? 32 : 0), 1) global_decode_k
         if (un < total_units)
           prefetch_l2(a.q + static_cast<int64_t>(a.cu_q_rows[plan_seq(sm.ub, a.batch, un)]) * HQ * 512, HQ * 1024);
       }
-    }
-  } else if (kApp && warp == 8) {
-    // ------------------------------------------------- fused append (warp 8)
-    using R = GlobalRow<LAYOUT>;
-    wait_prev();
-    for (int j = 0;; ++j) {
-      const int u = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
-      if (u >= total_units) break;
-      const int s = plan_seq(sm.ub, a.batch, u);
-      if (u - sm.ub[s] == sm.ub[s + 1] - sm.ub[s] - 1) {  // the sequence's last chunk
-        const int pos = a.seq_lens[s] - 1;
-        const int32_t page = a.block_table[static_cast<int64_t>(s) * a.max_pages + pos / kPage];
-        if (pos >= a.max_pos) {
-          if (lane == 0) set_status(st, GW_DEV_POS_RANGE);
-        } else if (page >= 0 && page < a.num_pages) {  // else the producer reports the page
-          const int64_t row = a.cu_q_rows[s];
-          for (int it = lane; it < R::kItems; it += 32) {
-            const int rt = R::rot_item(it);
-            const CosSin8 cs = rt >= 0 ? load_cs8(a.rope_cs + (static_cast<int64_t>(pos) * 64 + 8 * rt) * 2) : CosSin8{};
-            append_global_item<LAYOUT>(const_cast<uint8_t*>(a.pool), page, pos % kPage, a.k_new + row * 512,
-                                       a.v_new + row * 512, cs, it);
-          }
-          fence_proxy_async_global();
-        }
-      }
-      __syncwarp();
-      if (lane == 0) st_release_shared(&sm.app_done, j + 1);
+      if (kApp) append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, k + 1, total_units);
     }
   } else if (warp < 4) {
     // ------------------------------------------------- softmax + epilogue
@@ -820,7 +833,7 @@ cudaError_t launch_layout(const LocalArgs& a, cudaStream_t stream) {
   const size_t smem = sizeof(GSmem<LAYOUT, HQ>);
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kThreads + (a.k_new ? 32 : 0)), smem, stream, a);
+  e = launch_pdl(kern, dim3(grid_ctas()), dim3(kThreads), smem, stream, a);
   if (e != cudaSuccess) return e;
   // Dropping the merged partials from L2 unwritten pays for the folded pool
   // (24.7 vs 26.9 us per serving call) but not for the full control (427 vs
