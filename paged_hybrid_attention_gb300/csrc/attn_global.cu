@@ -48,8 +48,9 @@
 //   warp 7     P.V issue.
 // With a fused append (gw_append_decode_attn_global) warp 6 also writes the
 // step's row of each sequence whose last chunk this CTA decodes, one unit
-// ahead of its q loads; the producer waits for it before copying the tile
-// that holds the sequence's last page.  (A ninth warp for it would cap the
+// ahead of its q loads (the first unit's right after that unit's q); the
+// producer waits for it before copying the tile that holds the sequence's
+// last page.  (A ninth warp for it would cap the
 // kernel at 168 registers, and the softmax's spills cost long contexts more
 // than the separate append: 245 vs 238-240 us per long-context call.)
 // QK^T and P.V are issued by different warps so that QK^T of the next tile
@@ -499,7 +500,6 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
   } else if (warp == 6 && kE4) {
     // ------------------------------------------------- q loader, e4m3 pool
     wait_prev();
-    if (kApp) append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, 0, total_units);
     // Unit k's q goes to the Q buffer once the last QK^T of unit k - 1 has
     // completed.  Each head is scaled by an exact power of two 2^e, chosen so
     // that its largest |q| lands in [128, 256), and split into two e4m3
@@ -587,12 +587,14 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
         if (un < total_units)
           prefetch_l2(a.q + static_cast<int64_t>(a.cu_q_rows[plan_seq(sm.ub, a.batch, un)]) * HQ * 512, HQ * 1024);
       }
-      if (kApp) append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, k + 1, total_units);
+      if (kApp) {  // after the unit's q is published: unit 0's row, then one unit ahead
+        if (k == 0) append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, 0, total_units);
+        append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, k + 1, total_units);
+      }
     }
   } else if (warp == 6) {
     // -------------------------------------------------------------- q loader
     wait_prev();
-    if (kApp) append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, 0, total_units);
     // Unit k's rows overwrite Q once the last QK^T of unit k - 1 has
     // completed (q_free); by then they are usually in L2 already.
     int k = 0;
@@ -614,7 +616,10 @@ __global__ void __launch_bounds__(kThreads, 1) global_decode_kernel(const LocalA
         if (un < total_units)
           prefetch_l2(a.q + static_cast<int64_t>(a.cu_q_rows[plan_seq(sm.ub, a.batch, un)]) * HQ * 512, HQ * 1024);
       }
-      if (kApp) append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, k + 1, total_units);
+      if (kApp) {  // after the unit's q is published: unit 0's row, then one unit ahead
+        if (k == 0) append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, 0, total_units);
+        append_unit_row<LAYOUT>(a, sm.ub, &sm.app_done, k + 1, total_units);
+      }
     }
   } else if (warp < 4) {
     // ------------------------------------------------- softmax + epilogue
