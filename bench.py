@@ -1016,8 +1016,8 @@ def main():
                                    "prompt_tflops": dom_flops / (dom_ms * 1e-3) / 1e12}}
     else:
         # the probe whose copy pipeline the dominant kernel uses: tensor-map
-        # boxes for the local kernels (bf16 and e4m3), bulk copies for the
-        # global kernel
+        # boxes for the local kernels (4 KB for bf16; the e4m3 kernel's 2 KB
+        # boxes stream no faster), bulk copies for the global kernel
         tma_pipe = bool(locals_)
         probe = read_gbs_tma if tma_pipe else read_gbs
         roofline = {"kernel": how, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -1060,7 +1060,7 @@ def main():
             "what": "4 GiB streamed with no arithmetic, best of 5: gw_bw_probe through a bulk-copy pipeline "
                     "(8 warps x 2-stage 8 KiB rings per SM; the global decode copies whole pages in bulk), "
                     "gw_bw_probe_tma through the tensor-map pipeline (6 warps x 2-stage 16 KiB page-head rings "
-                    "per SM of 2 KB boxes, as the local decode kernels)"},
+                    "per SM of 4 KB boxes, as the bf16 local decode kernel)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,

@@ -457,10 +457,12 @@ gw_status gw_bw_probe(const void* buf, size_t bytes, int32_t* dev_status, void* 
 
 /*
  * gw_bw_probe_tma - as gw_bw_probe, through the copy pipeline of the bf16
- * local decode kernel instead (the e4m3 one copies the same 2 KiB boxes):
+ * local decode kernel instead (the e4m3 one copies 2 KiB boxes of one K or V
+ * chunk, which its tensor-core operands need contiguous):
  * one CTA per SM, 6 warps, each with a 2-stage
  * ring of 16 KiB shared-memory stages, a stage being one 16-token page head
- * (K then V) brought by 8 tensor-map copies of 2 KiB (128-byte swizzled).
+ * (K then V) brought by 4 tensor-map copies of 4 KiB (one 128-byte chunk of
+ * its 16 K and 16 V rows each, 128-byte swizzled).
  * The first floor(bytes / 16384) * 16384 bytes of `buf` are read as the
  * pages of a LOCAL bf16 pool with one KV head, in page order, and discarded.
  * A measurement aid with no counterpart in the pages.

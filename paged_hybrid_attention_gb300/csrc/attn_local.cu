@@ -25,7 +25,7 @@
 //     multiplicand format and l sums exactly the rounded weights.
 //
 // bf16 pools (local_decode_tc_kernel, 6 warps): a stage is one 16-token page
-// head (K and V, 16 KB) brought by 8 TMA tensor copies into 128-byte-swizzled
+// head (K and V, 16 KB) brought by 4 TMA tensor copies into 128-byte-swizzled
 // shared memory; q.K^T and P.V run on warp-level tensor cores (mma.sync
 // m16n8k16, the G heads of the group as rows) with P kept in registers.
 #include "append_row.cuh"
@@ -95,9 +95,10 @@ __device__ __forceinline__ void local_plan(const LocalArgs& a, int32_t* ub, bool
 
 // ---------------------------------------------------------------------------
 // bf16 pages on warp-level tensor cores (mma.sync), fed by TMA.  A stage is
-// one 16-token page head: K (4 chunks x 16 rows x 128 B) and V (same), 16 KB
-// copied as 8 tensor boxes of 2 KB issued by 8 lanes, landing 128-byte
-// swizzled so that every ldmatrix below reads 8 distinct bank groups.
+// one 16-token page head: K and V (4 chunks x 16 rows x 128 B each), 16 KB
+// copied as 4 tensor boxes of 4 KB (a chunk's 16 K rows and 16 V rows, which
+// are adjacent in the pool) issued by 4 lanes, landing 128-byte swizzled so
+// that every ldmatrix below reads 8 distinct bank groups.
 //   S[16 x 16]   = Q[16 x 256] . K^T      (m16n8k16 x 2 token halves; rows
 //                                          = the G heads of the KV head)
 //   O^T[256 x 8] += V^T[256 x 16] . P^T   (m16n8k16; columns = heads)
@@ -106,7 +107,10 @@ __device__ __forceinline__ void local_plan(const LocalArgs& a, int32_t* ub, bool
 // registers; about 60 warp instructions per 16 tokens instead of ~700.
 constexpr int kTcWarps = 6;
 constexpr int kTcStages = 2;
-constexpr int kTcStage = 16384;  // K 8 KB then V 8 KB
+// A stage holds, per 64-dim chunk c, the page head's 16 K rows then its 16 V
+// rows (one 4 KB tensor-map box: K and V of a page head are adjacent in the
+// pool), so K chunk c sits at 4096 c and V chunk c at 4096 c + 2048.
+constexpr int kTcStage = 16384;
 
 struct __align__(1024) TcWarpSmem {
   uint8_t stage[kTcStages][kTcStage];
@@ -264,12 +268,9 @@ __global__ void __launch_bounds__(kTcWarps * 32 + 32, 1)
         mbar_arrive_expect_tx(&sm.bar[st], kTcStage);
       }
       __syncwarp();
-      if (lane < 8) {
-        // lane: K (0-3) or V (4-7), 64-dim chunk lane % 4
-        const int kv = lane >> 2, c = lane & 3;
-        tma_rows(smem_u32(sm.stage[st]) + kv * 8192 + c * 2048, &kv_map, c,
-                 ((phys * a.kv_heads + d.g) * 2 + kv) * kPage, &sm.bar[st], pol);
-      }
+      if (lane < 4)  // lane: 64-dim chunk; K and V rows of the page head in one box
+        tma_rows(smem_u32(sm.stage[st]) + lane * 4096, &kv_map, lane, (phys * a.kv_heads + d.g) * 2 * kPage,
+                 &sm.bar[st], pol);
     }
     ++issued;
     if (++f_i == d.n) {
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(kTcWarps * 32 + 32, 1)
       for (uint32_t k = consumed + 1; k < issued; ++k) mbar_wait(&sm.bar[k % kTcStages], (k / kTcStages) & 1, nullptr);
       return;
     }
-    const uint32_t kb = smem_u32(sm.stage[st]), vb = kb + 8192;
+    const uint32_t kb = smem_u32(sm.stage[st]), vb = kb + 2048;  // chunk c: + 4096 c
     const int t0 = (d.hp_lo + c_i) * kTok;
     const bool stage_ok = sm.valid[st] != 0;
 
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(kTcWarps * 32 + 32, 1)
       for (int h = 0; h < 2; ++h) {
         uint32_t b[4];
         const int row = h * 8 + (lane & 7);
-        ldsm4(kb + (s2 >> 1) * 2048 + sw128(row, (s2 & 1) * 4 + (lane >> 3)), b);
+        ldsm4(kb + (s2 >> 1) * 4096 + sw128(row, (s2 & 1) * 4 + (lane >> 3)), b);
         hmma_q(sacc[h], qa[2 * s2][0], qa[2 * s2][1], b[0], b[1]);
         hmma_q(sacc[h], qa[2 * s2 + 1][0], qa[2 * s2 + 1][1], b[2], b[3]);
       }
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(kTcWarps * 32 + 32, 1)
       if (t0 < d.tok_lo || t0 + kTok > d.tok_hi) {
         for (int r = 0; r < kTok; ++r) {
           if (t0 + r >= d.tok_lo && t0 + r < d.tok_hi) continue;
-          *reinterpret_cast<uint4*>(sm.stage[st] + 8192 + (lane >> 3) * 2048 + r * 128 + (lane & 7) * 16) =
+          *reinterpret_cast<uint4*>(sm.stage[st] + 2048 + (lane >> 3) * 4096 + r * 128 + (lane & 7) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();  // ordered before the next TMA into this stage
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(kTcWarps * 32 + 32, 1)
         uint32_t v[4];
         const int m = lane >> 3;
         const int row = (m >> 1) * 8 + (lane & 7);
-        ldsm4_t(vb + (j >> 2) * 2048 + sw128(row, (j & 3) * 2 + (m & 1)), v);
+        ldsm4_t(vb + (j >> 2) * 4096 + sw128(row, (j & 3) * 2 + (m & 1)), v);
         hmma(o[j], v, pb[0], pb[1]);
       }
     }
@@ -436,7 +437,7 @@ __global__ void __launch_bounds__(kTcWarps * 32 + 32, 1)
 template <int G>
 cudaError_t launch_tc(const LocalArgs& a, cudaStream_t st) {
   CUtensorMap map;
-  cudaError_t e = make_local_kv_map(a, &map);
+  cudaError_t e = make_local_kv_map(a, &map, GW_KV_BF16, 32);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(TcWarpSmem) * kTcWarps + sizeof(int32_t) * (kMaxBatch + 1 + 32 + 4);
   auto kern = local_decode_tc_kernel<G>;

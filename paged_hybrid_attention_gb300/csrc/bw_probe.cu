@@ -101,11 +101,9 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1) bw_probe_tma_kernel(int64_t
     const int st = issued % kTmaStages;
     if (lane == 0) mbar_arrive_expect_tx(&sm.bar[st], kTmaStage);
     __syncwarp();
-    if (lane < 8) {
-      const int kv = lane >> 2, c = lane & 3;
-      tma_rows(smem_u32(sm.stage[st]) + kv * 8192 + c * 2048, &map, c, static_cast<int>((next * 2 + kv) * kPage),
-               &sm.bar[st], pol);
-    }
+    if (lane < 4)  // one 4 KB box per 64-dim chunk: the page head's K and V rows
+      tma_rows(smem_u32(sm.stage[st]) + lane * 4096, &map, lane, static_cast<int>(next * 2 * kPage), &sm.bar[st],
+               pol);
     ++issued;
     next += n_warps;
   };
@@ -166,7 +164,7 @@ cudaError_t launch_bw_probe_tma(const void* buf, int64_t pages, int32_t* status,
   a.num_pages = pages;
   a.kv_heads = 1;
   CUtensorMap map;
-  cudaError_t e = make_local_kv_map(a, &map);
+  cudaError_t e = make_local_kv_map(a, &map, GW_KV_BF16, 32);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(TmaProbeWarp) * kTmaWarps;
   e = set_smem_once(reinterpret_cast<const void*>(bw_probe_tma_kernel), smem);

@@ -170,7 +170,9 @@ cudaError_t launch_wait_selftest(int32_t* status, int32_t* result, int64_t limit
 // head) * 2 + {K, V}) * 16 + token; box {one chunk, 1, 16 rows}, 128-byte
 // swizzle.
 constexpr int kPageTokens = 16;
-cudaError_t make_local_kv_map(const LocalArgs& a, CUtensorMap* map, int dtype = GW_KV_BF16);
+// Tensor map of a LOCAL pool: boxes of one 128-byte chunk of `box_rows` rows
+// (16: a page head's K or V; 32: its K and V together), 128-byte swizzled.
+cudaError_t make_local_kv_map(const LocalArgs& a, CUtensorMap* map, int dtype = GW_KV_BF16, int box_rows = 16);
 cudaError_t launch_local_decode(int dtype, int group, const LocalArgs& a, cudaStream_t st);
 // tcgen05 decode kernel (kind::f8f6f4) for e4m3 LOCAL pools, plus the combine
 cudaError_t launch_local_decode_e4m3_tc(int group, const LocalArgs& a, cudaStream_t st);
