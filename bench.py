@@ -53,8 +53,8 @@ UNIT = "GB/s"
 # workload: (bytes, source file under csrc/, sha256)
 NCU_TRAFFIC = {
     "serving": (275910400, "attn_local.cu", "8e861a25e89d42f84f61c42f2fc8414d85ff98300d34fd2e3f49b4b88ce35b11"),
-    "fp8_local": (552973312, "attn_local_e4m3_tc.cu", "e348365c2bf236e2255d66c87103cc92c1406a3e1dab7e39b6f6144676afb399"),
-    "long_global": (1354496512, "attn_global.cu", "f6add234ef69883f75cd07c7c8ad98348d3192bd7b1e56001c15c1040c3ccc69"),
+    "fp8_local": (552674048, "attn_local_e4m3_tc.cu", "1c609757948ca05a747358eeb08e995e3cffe515728d19fb98507efab1d1aa13"),
+    "long_global": (1354160896, "attn_global.cu", "cb628c3d09d39c1e5efd439f40f2a4ca9157ebad9077365c371ca8e1754ff163"),
 }
 
 
