@@ -428,7 +428,8 @@ gw_status gw_set_early_launch(int32_t on);
  * from cu_q_rows and seq_lens and fetch their first units' block-table
  * entries before that wait, which takes two dependent round trips off the
  * call; gw_kv_append likewise reads slot, pos and the RoPE table rows they
- * select before its wait.  KV pages, q, k, v, the workspace, out and
+ * select before its wait, and a gw_append_decode_attn_local call the length,
+ * page and RoPE rows of the first row it appends.  KV pages, q, k, v, the workspace, out and
  * dev_status are still touched only after the wait.  The caller promises
  * that the kernel just before each call in its stream does not write that
  * call's cu_q_rows, seq_lens, block_table, slot, pos or rope_cs, as holds

@@ -28,7 +28,7 @@
 // head (K and V, 16 KB) brought by 4 TMA tensor copies into 128-byte-swizzled
 // shared memory; q.K^T and P.V run on warp-level tensor cores (mma.sync
 // m16n8k16, the G heads of the group as rows) with P kept in registers.
-#include "append_row.cuh"
+#include "local_append.cuh"
 #include "plan.cuh"
 #include "tma.cuh"
 
@@ -185,38 +185,10 @@ __global__ void __launch_bounds__(kTcWarps * 32 + 32, 1)
   }
   if (warp == kTcWarps) {
     // ---- fused append (launched only with one): the step's K/V row of each
-    // (sequence, KV head) whose last chunk this CTA decodes, at position
-    // L - 1, in the order of the CTA's units; the decode warp of such a unit
-    // waits for it before copying the unit's last page.
-    if (early) {
-      pdl_wait();
-      pdl_trigger();
-    }
-    for (int j = 0;; ++j) {
-      const int u = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
-      if (u >= total_units) break;
-      const int s = plan_seq(ub, a.batch, u);
-      const int nc = (ub[s + 1] - ub[s]) / a.kv_heads;
-      const int r = u - ub[s];
-      if (r % nc == nc - 1) {
-        const int pos = a.seq_lens[s] - 1;
-        const int32_t page = a.block_table[static_cast<int64_t>(s) * a.max_pages + pos / kPage];
-        if (pos >= a.max_pos) {
-          if (lane == 0) set_status(a.status, GW_DEV_POS_RANGE);
-        } else if (page >= 0 && page < a.num_pages) {  // else the decode warp reports the page
-          const int g = r / nc;
-          const int64_t row = static_cast<int64_t>(a.cu_q_rows[s]) * a.kv_heads + g;
-          if (lane < 16)
-            append_local_item<GW_KV_BF16>(const_cast<uint8_t*>(a.pool), a.kv_heads, page, pos % kPage, g,
-                                          a.k_new + row * 256, a.v_new + row * 256,
-                                          load_cs8(a.rope_cs + (static_cast<int64_t>(pos) * 128 + 8 * lane) * 2),
-                                          lane);
-          fence_proxy_async_global();
-        }
-      }
-      __syncwarp();
-      if (lane == 0) st_release_shared(app_done, j + 1);
-    }
+    // (sequence, KV head) whose last chunk this CTA decodes (local_append.cuh);
+    // the decode warp of such a unit waits for it before copying the unit's
+    // last page.
+    local_append_warp<GW_KV_BF16>(a, ub, total_units, app_done, early);
     return;
   }
   const int n_active = active_warps(total_units, kTcWarps);

@@ -39,7 +39,7 @@
 //              CTA decodes, in the order of the CTA's units; the producer
 //              warp that copies that unit's last page waits for it.
 // Every wait is bounded; a timeout raises GW_DEV_TIMEOUT and the roles stop.
-#include "append_row.cuh"
+#include "local_append.cuh"
 #include "plan.cuh"
 #include "tcgen05.cuh"
 #include "tma.cuh"
@@ -335,33 +335,8 @@ __global__ void __launch_bounds__(kE8Threads + (kApp ? 32 : 0), 1)
       if (next) load(next);
     }
   } else if (kApp && warp == kE8Threads / 32) {
-    // -------------------------------------------------------- fused append
-    wait_prev();
-    for (int j = 0;; ++j) {
-      const int u = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
-      if (u >= total) break;
-      const int s = plan_seq(sm.ub, a.batch, u);
-      const int nc = (sm.ub[s + 1] - sm.ub[s]) / a.kv_heads;
-      const int r = u - sm.ub[s];
-      if (r % nc == nc - 1) {
-        const int pos = a.seq_lens[s] - 1;
-        const int32_t page = a.block_table[static_cast<int64_t>(s) * a.max_pages + pos / kPage];
-        if (pos >= a.max_pos) {
-          if (lane == 0) set_status(st, GW_DEV_POS_RANGE);
-        } else if (page >= 0 && page < a.num_pages) {  // else the producer reports the page
-          const int g = r / nc;
-          const int64_t row = static_cast<int64_t>(a.cu_q_rows[s]) * a.kv_heads + g;
-          if (lane < 16)
-            append_local_item<GW_KV_E4M3>(const_cast<uint8_t*>(a.pool), a.kv_heads, page, pos % kPage, g,
-                                          a.k_new + row * 256, a.v_new + row * 256,
-                                          load_cs8(a.rope_cs + (static_cast<int64_t>(pos) * 128 + 8 * lane) * 2),
-                                          lane);
-          fence_proxy_async_global();
-        }
-      }
-      __syncwarp();
-      if (lane == 0) st_release_shared(&sm.app_done, j + 1);
-    }
+    // -------------------------------------------- fused append (local_append.cuh)
+    local_append_warp<GW_KV_E4M3>(a, sm.ub, total, &sm.app_done, early);
   } else if (warp < 4) {
     // ------------------------------------------------ softmax + epilogue
     // The four warps meet at a named barrier twice per unit, so none may
