@@ -219,10 +219,13 @@ class GpuLayer:
 
     def can_fuse(self, gw):
         """Whether this layer's step appends inside its decode call
-        (gw_append_decode_attn_*): decode rows only.  Not on an e4m3 local
-        pool, where the fused call measured slower than the two calls (fp8
-        workload: 98.4 vs 95.3 us per call, step 102.6 vs 100.6 us)."""
-        return self.max_q_rows == 1 and not (self.fam.kind == "local" and self.fam.dtype == "e4m3")
+        (gw_append_decode_attn_*): decode rows only, on the bf16 local and
+        bf16 folded global pools, where the fused call measured faster (one
+        box: serving step 259.7 vs 275.0 us, long-context folded call 238.6
+        vs 239.0 us).  On the e4m3 local pool (98.8 vs 94.6 us per fp8
+        call), the full control (410.9 vs 406.7 us) and the e4m3 folded pool
+        (200.9 vs 198.0 us) the two calls measured faster."""
+        return self.max_q_rows == 1 and self.fam.dtype == "bf16" and self.fam.layout in ("local", "folded")
 
     def attend(self, gw, stream):
         if self.fused:
