@@ -211,3 +211,41 @@ def test_cp_entry_points_host_validation():
     assert L.gw_merge_lse(2, bad, arr, f, None, 4, 8, 512, None) == gw.GW_ERR_INVALID_ARG      # misaligned part
     assert "part 1" in gw.last_error()
     assert L.gw_merge_lse(2, arr, arr, f, None, 0, 8, 512, None) == gw.GW_OK                   # no rows
+
+
+def test_fused_append_entry_points_host_validation():
+    """gw_append_decode_attn_local / _global refuse bad rows, RoPE tables and
+    workspaces on the host, with the attention checks of their two-call
+    counterparts; every refusal here comes before any launch."""
+    L = gw.lib()
+    f, ws = _fake(), _fake(1 << 28)
+    d = _desc()
+
+    def loc(desc=d, k=f, v=f, rope=f, max_pos=4096, hq=32, ws_bytes=1 << 30, window=1024):
+        return L.gw_append_decode_attn_local(ctypes.byref(desc), k, v, rope, max_pos, f, f, hq, 2, f, f, f, 64,
+                                             window, 0.0625, ws, ws_bytes, None, None)
+
+    assert loc(k=None) == gw.GW_ERR_INVALID_ARG and "k/v" in gw.last_error()
+    assert loc(v=_fake((1 << 24) + 8)) == gw.GW_ERR_INVALID_ARG              # v not 16-byte aligned
+    assert loc(rope=None) == gw.GW_ERR_INVALID_ARG and "rope_cs" in gw.last_error()
+    assert loc(max_pos=0) == gw.GW_ERR_INVALID_ARG and "max_pos" in gw.last_error()
+    assert loc(hq=24) == gw.GW_ERR_INVALID_ARG                               # not a multiple of kv heads
+    assert loc(window=0) == gw.GW_ERR_INVALID_ARG
+    assert loc(ws_bytes=100) == gw.GW_ERR_WORKSPACE
+    assert gw.last_error().startswith("gw_append_decode_attn_local:")
+    assert loc(desc=_desc(dtype=gw.KV_E4M3), ws_bytes=100) == gw.GW_ERR_WORKSPACE   # e4m3 pools are served
+    g = _desc(gw.LAYOUT_GLOBAL_FOLDED, kvh=1, hd=512, rd=128)
+    assert loc(desc=g) == gw.GW_ERR_INVALID_ARG                              # global pool on the local entry
+
+    def glo(desc=g, k=f, rope=f, max_pos=4096, hq=32, ws_bytes=1 << 30):
+        return L.gw_append_decode_attn_global(ctypes.byref(desc), k, f, rope, max_pos, f, f, hq, 2, f, f, f, 64,
+                                              0.04, ws, ws_bytes, None, None)
+
+    assert glo(k=None) == gw.GW_ERR_INVALID_ARG
+    assert glo(rope=_fake((1 << 24) + 4)) == gw.GW_ERR_INVALID_ARG           # rope_cs not 16-byte aligned
+    assert glo(hq=12) == gw.GW_ERR_UNSUPPORTED
+    assert glo(ws_bytes=100) == gw.GW_ERR_WORKSPACE
+    assert gw.last_error().startswith("gw_append_decode_attn_global:")
+    e8 = _desc(gw.LAYOUT_GLOBAL_FOLDED_E4M3, gw.KV_E4M3, kvh=1, hd=512, rd=128)
+    assert glo(desc=e8, ws_bytes=100) == gw.GW_ERR_WORKSPACE                  # all three global layouts
+    assert glo(desc=d) == gw.GW_ERR_INVALID_ARG                              # local pool on the global entry
